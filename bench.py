@@ -1,0 +1,287 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 GEMM hot path on GB300.
+
+One step = one complete mxfp4_gemm call (A quantized inside the call, MMA, split-K
+reduction, bf16 epilogue) on the M=8, N=2112, K=7168 weight-streaming workload; B is
+quantized and prepacked once, outside the timed region (the pages prepare B in their
+harness too). Inputs are resident in HBM and rotate over enough copies that every step
+streams its weights from DRAM rather than L2.
+
+Prints ONE JSON line. `value` is microseconds per call (lower is better); TFLOPS, GB/s and
+the roofline fraction ride along, with the same measurement for every workload in
+`per_shape`. `--impl reference` times the CPU oracle instead (the method has no runnable
+reference implementation here).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_scaled_mxfp4_bf16_gb300 import workloads  # noqa: E402
+
+METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor roofline"
+HEADLINE = "M8_N2112_K7168"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_DEFAULT = 126 * 1024 * 1024
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background while the GPU is under load."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
+        busy = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _events():
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float = 0.0, e2e: bool = False):
+    """Time `steps` back-to-back mxfp4_gemm calls of workload w. Returns a dict."""
+    dev = torch.device("cuda")
+    a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
+    b = b_cpu.to(dev)
+    bq, bs = mx.mxfp4_quantize(b)
+    packed0 = mx.mxfp4_prepack_b(bq, bs)
+    del b, bq, bs
+    a0 = a_cpu.to(dev)
+    per_copy = packed0.numel() + a0.numel() * 2 + w.M * w.N * 2
+    copies = max(2, min(256, -(-3 * l2_bytes // per_copy)))
+    packs = [packed0] + [packed0.clone() for _ in range(copies - 1)]
+    As = [a0] + [a0.clone() for _ in range(copies - 1)]
+    Cs = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    plan = mx.mxfp4_gemm_plan(w.M, w.N, w.K)
+    ws = torch.empty(max(1, mx.mxfp4_gemm_workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=dev)
+    mx.mxfp4_workspace_init(ws)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % copies
+        mx.mxfp4_gemm(As[j], packs[j], w.N, c=Cs[j], workspace=ws, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if soak_s > 0:
+        t_end = time.time() + soak_s
+        i = 0
+        while time.time() < t_end:
+            for _ in range(200):
+                step(i)
+                i += 1
+            torch.cuda.synchronize()
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    status = mx.mxfp4_device_status()
+    res = {"us_per_call": 1000.0 * ms / steps, "elapsed_ms": ms, "copies": copies, "plan": plan,
+           "kernels_per_call": 1 if plan["path"] == 1 else 2, "status": status}
+    if e2e:
+        # end to end through the public call: pinned host A -> device, GEMM, C -> pinned host
+        a_host = a_cpu.pin_memory()
+        c_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
+        for i in range(3):
+            As[0].copy_(a_host, non_blocking=True)
+            step(0)
+            c_host.copy_(Cs[0], non_blocking=True)
+        torch.cuda.synchronize()
+        n_e2e = max(20, steps // 10)
+        e0.record(stream)
+        for i in range(n_e2e):
+            j = i % copies
+            As[j].copy_(a_host, non_blocking=True)
+            step(j)
+            c_host.copy_(Cs[j], non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        res["e2e_us_per_call"] = 1000.0 * e0.elapsed_time(e1) / n_e2e
+        res["h2d_bytes"] = w.M * w.K * 2
+        res["d2h_bytes"] = w.M * w.N * 2
+    del packs, As, Cs, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_oracle_step_time(w, budget_s: float = 12.0):
+    """The oracle as it stands on the host cores: quantize A, dequantize, fp64 GEMM, bf16 cast.
+    Bounded sample: whole calls of workload w, repeated until budget_s has passed (min 1)."""
+    import oracle
+    a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
+    bq, bs = oracle.quantize(workloads.bf16_bits(b_cpu))     # B pre-quantized: not timed
+    a_bits = workloads.bf16_bits(a_cpu)
+    # a sample of rows keeps one step of the big workloads inside the budget
+    rows = w.M if w.M * w.N * w.K <= 4e9 else max(1, int(4e9 // (w.N * w.K)))
+    a_bits = np.ascontiguousarray(a_bits[:rows])
+    n, t0 = 0, time.time()
+    while True:
+        aq, as_ = oracle.quantize(a_bits)
+        c = oracle.mxfp4_gemm_ref(aq, as_, bq, bs)
+        oracle.to_bf16(c)
+        n += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = (time.time() - t0) / n
+    scale = w.M / rows
+    return {"us_per_call": 1e6 * dt * scale, "cores": oracle.num_threads(),
+            "sample": f"{n} oracle call(s) on {rows} of {w.M} rows of {w.name}, time scaled by {scale:g}"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-shapes", action="store_true", help="skip the per-shape sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workloads.by_name(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = cpu_oracle_step_time(w)
+        line = {"impl": "reference", "metric": METRIC, "value": r["us_per_call"], "unit": "us/call",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": r["us_per_call"] / 1000.0, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+                "cpu_baseline": {"value": r["us_per_call"], "unit": "us/call", "cores": r["cores"],
+                                 "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": r["us_per_call"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    mx.load_library()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size or L2_BYTES_DEFAULT
+    peak, peak_kind = measured_peaks()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    main_res = bench_workload(mx, w, args.steps, args.warmup, l2, soak_s=1.0, e2e=True)
+    clocks = sampler.stop()
+
+    t_us = main_res["us_per_call"]
+    if world > 1:
+        t = torch.tensor([main_res["elapsed_ms"]], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_us = 1000.0 * float(t.item()) / (args.steps * world)
+
+    per_shape = {}
+    if not args.no_shapes:
+        for ws_ in workloads.WORKLOADS:
+            r = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2)
+            gbs = ws_.algorithmic_bytes / (r["us_per_call"] * 1e-6) / 1e9
+            per_shape[ws_.name] = {"us_per_call": round(r["us_per_call"], 3),
+                                   "tflops": round(ws_.flops / (r["us_per_call"] * 1e-6) / 1e12, 2),
+                                   "algorithmic_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+                                   "path": r["plan"]["path"], "splits": r["plan"]["splits"],
+                                   "ctas": r["plan"]["ctas"], "status": r["status"]}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu:
+        c = cpu_oracle_step_time(w)
+        cpu = {"value": c["us_per_call"], "unit": "us/call", "cores": c["cores"], "kind": "oracle",
+               "sample": c["sample"]}
+    gbs = w.algorithmic_bytes / (main_res["us_per_call"] * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(t_us, 4), "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_us / 1000.0, 7), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xe2m1->f32->bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "l2": f"inputs rotate over {main_res['copies']} copies (> 3x L2) so weights stream from HBM",
+                   "path": main_res["plan"]["path"], "splits": main_res["plan"]["splits"],
+                   "ctas": main_res["plan"]["ctas"]},
+        "tflops": round(w.flops / (t_us * 1e-6) / 1e12, 3),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": w.algorithmic_bytes},
+        "e2e": {"value": round(main_res["e2e_us_per_call"], 3), "unit": "us/call",
+                "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},
+        "gpu_launches": args.steps * main_res["kernels_per_call"],
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "per_shape": per_shape,
+        "device_status": main_res["status"],
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,215 @@
-"""GB300-native block-scaled MXFP4 GEMM: C[M,N] (bf16) = MXFP4(A bf16) . MXFP4(B)^T."""
+"""GB300-native block-scaled MXFP4 GEMM: C[M,N] (bf16) = MXFP4(A[M,K] bf16) . MXFP4(B[N,K])^T.
+
+Thin Python binding over the C ABI in ``include/mxfp4_gb300.h`` (libmxfp4_gb300.so, built
+in-tree for sm_103a). The functions keep the C names and only marshal arguments: PyTorch
+provides device memory and the current CUDA stream; every step of the computation runs in
+the library's CUDA kernels. There is no CPU fallback: if the library cannot be loaded or
+built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "Mxfp4Error", "load_library", "mxfp4_quantize", "mxfp4_prepack_b_size", "mxfp4_prepack_b",
+    "mxfp4_gemm_workspace_size", "mxfp4_workspace_init", "mxfp4_gemm", "mxfp4_gemm_plan",
+    "mxfp4_device_status", "mxfp4_selftest_timeout", "mxfp4_version",
+]
+
+_LOCK = threading.Lock()
+_LIB = None
+_WS: dict = {}
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _LIB
+        name = lib.mxfp4_status_string(status).decode() if lib is not None else str(status)
+        extra = ""
+        if lib is not None and name == "MXFP4_ERR_CUDA":
+            extra = f" (cudaError {lib.mxfp4_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+        self.status = status
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("splits", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+
+
+def load_library() -> ctypes.CDLL:
+    """Load (building first if needed) libmxfp4_gb300.so. Raises if that is impossible."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.LIB_PATH
+            if not _build.up_to_date():
+                path = _build.build()
+            L = ctypes.CDLL(path)
+            L.mxfp4_status_string.restype = ctypes.c_char_p
+            L.mxfp4_status_string.argtypes = [_int]
+            L.mxfp4_last_cuda_error.restype = _int
+            L.mxfp4_version.restype = _int
+            L.mxfp4_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
+            L.mxfp4_quantize.restype = _int
+            L.mxfp4_prepack_b_size.argtypes = [_i64, _i64]
+            L.mxfp4_prepack_b_size.restype = _sz
+            L.mxfp4_prepack_b.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp]
+            L.mxfp4_prepack_b.restype = _int
+            L.mxfp4_gemm_workspace_size.argtypes = [_i64, _i64, _i64]
+            L.mxfp4_gemm_workspace_size.restype = _sz
+            L.mxfp4_gemm_workspace_size_ex.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options)]
+            L.mxfp4_gemm_workspace_size_ex.restype = _sz
+            L.mxfp4_workspace_init.argtypes = [_vp, _sz, _vp]
+            L.mxfp4_workspace_init.restype = _int
+            L.mxfp4_gemm.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _sz, _vp]
+            L.mxfp4_gemm.restype = _int
+            L.mxfp4_gemm_ex.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _sz,
+                                        ctypes.POINTER(_Options), _vp]
+            L.mxfp4_gemm_ex.restype = _int
+            L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options)] + [ctypes.POINTER(_int)] * 5
+            L.mxfp4_gemm_plan.restype = _int
+            L.mxfp4_device_status.argtypes = [_vp]
+            L.mxfp4_device_status.restype = _int
+            L.mxfp4_selftest_timeout.argtypes = [_int, _vp]
+            L.mxfp4_selftest_timeout.restype = _int
+            _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise Mxfp4Error(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _opts(path: int, splits: int):
+    return ctypes.byref(_Options(path, splits))
+
+
+def mxfp4_version() -> int:
+    return load_library().mxfp4_version()
+
+
+def mxfp4_quantize(x: torch.Tensor, q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                   stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """bf16 [rows, K] (row stride may exceed K) -> (e2m1 uint8 [rows, K/2], e8m0 uint8 [rows, K/32])."""
+    L = load_library()
+    _dev(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bf16 tensor with unit column stride")
+    rows, K = x.shape
+    if q is None:
+        q = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, K // 32, dtype=torch.uint8, device=x.device)
+    _check(L.mxfp4_quantize(x.data_ptr(), rows, K, x.stride(0), q.data_ptr(), scales.data_ptr(), _stream(stream)),
+           "mxfp4_quantize")
+    return q, scales
+
+
+def mxfp4_prepack_b_size(N: int, K: int) -> int:
+    return int(load_library().mxfp4_prepack_b_size(N, K))
+
+
+def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Pre-quantized B (e2m1 [N, K/2], e8m0 [N, K/32]) -> packed uint8 buffer for mxfp4_gemm."""
+    L = load_library()
+    _dev(bq, "bq")
+    N, K = bq.shape[0], bq.shape[1] * 2
+    if bs.shape != (N, K // 32) or not bq.is_contiguous() or not bs.is_contiguous():
+        raise ValueError("bq [N, K/2] and bs [N, K/32] must be contiguous and consistent")
+    size = mxfp4_prepack_b_size(N, K)
+    if size == 0:
+        raise Mxfp4Error(2, "mxfp4_prepack_b_size")
+    if packed is None:
+        packed = torch.empty(size + 1024, dtype=torch.uint8, device=bq.device)
+        off = (-packed.data_ptr()) % 1024
+        packed = packed[off:off + size]
+    _check(L.mxfp4_prepack_b(bq.data_ptr(), bs.data_ptr(), N, K, packed.data_ptr(), _stream(stream)),
+           "mxfp4_prepack_b")
+    return packed
+
+
+def mxfp4_gemm_workspace_size(M: int, N: int, K: int, path: int = 0, splits: int = 0) -> int:
+    return int(load_library().mxfp4_gemm_workspace_size_ex(M, N, K, _opts(path, splits)))
+
+
+def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(load_library().mxfp4_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "mxfp4_workspace_init")
+
+
+def _workspace(device: torch.device, nbytes: int, stream) -> torch.Tensor | None:
+    """A zero-initialised workspace of at least nbytes per device, grown on demand."""
+    if nbytes == 0:
+        return None
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        mxfp4_workspace_init(ws, stream)
+        _WS[key] = ws
+    return ws
+
+
+def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
+               stream=None) -> torch.Tensor:
+    """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b."""
+    L = load_library()
+    _dev(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    M, K = a.shape
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
+    st = _stream(stream)
+    need = mxfp4_gemm_workspace_size(M, N, K, path, splits) if M and N else 0
+    if workspace is None:
+        workspace = _workspace(a.device, need, stream)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(L.mxfp4_gemm_ex(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
+                           ws_ptr, ws_bytes, _opts(path, splits), st), "mxfp4_gemm")
+    return c
+
+
+def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0) -> dict:
+    L = load_library()
+    out = [ctypes.c_int() for _ in range(5)]
+    _check(L.mxfp4_gemm_plan(M, N, K, _opts(path, splits), *[ctypes.byref(o) for o in out]), "mxfp4_gemm_plan")
+    return dict(zip(["path", "splits", "m_tile", "ctas", "stages"], [o.value for o in out]))
+
+
+def mxfp4_device_status(stream=None) -> int:
+    return int(load_library().mxfp4_device_status(_stream(stream)))
+
+
+def mxfp4_selftest_timeout(limit_us: int, stream=None) -> None:
+    _check(load_library().mxfp4_selftest_timeout(limit_us, _stream(stream)), "mxfp4_selftest_timeout")

@@ -1,0 +1,102 @@
+// Device-side MXFP4 block quantizer: 32 bf16 values -> 16 packed e2m1 bytes + 1 e8m0 byte.
+//
+// The arithmetic is the one submission 711914 of the amd-mxfp4-mm leaderboard spells out in
+// `_mxfp4_quant_tile`:
+//   amax   = max |x| over the block (fp32);
+//   amax_r = bits(amax) + 0x200000, mantissa cleared  (power of two, rounding up from 1.75);
+//   s      = clamp(floor(log2(amax_r)) - 2, -127, 127), stored as s + 127;
+//   code   = e2m1(x * 2^-s): nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to even,
+//            saturating at 6, sign in bit 3 even when the magnitude rounds to 0;
+//   byte   = code(even element) | code(odd element) << 4.
+// Here amax is taken on the integer bit patterns (|x| of a finite float orders like its
+// bit pattern), floor(log2) is read off the exponent field, and the element rounding uses
+// the sm_100+ conversion cvt.rn.satfinite.e2m1x2.f32 on the exactly scaled fp32 value.
+#pragma once
+#include <cstdint>
+
+namespace mxfp4 {
+
+// Unbiased scale exponent s from the fp32 bit pattern of the block's max |x|.
+__device__ __forceinline__ int scale_exponent(uint32_t amax_bits) {
+    const uint32_t r = (amax_bits + 0x200000u) & 0xFF800000u;
+    if (r == 0u) return -127;              // log2(0) = -inf, clamped
+    if (r >= 0x7F800000u) return 127;      // rounded up to +inf, clamped
+    const int e = static_cast<int>(r >> 23) - 127 - 2;
+    return e < -127 ? -127 : e;            // e <= 125 here
+}
+
+// 2^-s as an fp32 (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float inv_scale(int s) {
+    const uint32_t bits = (s == 127) ? 0x00400000u : static_cast<uint32_t>(127 - s) << 23;
+    return __uint_as_float(bits);
+}
+
+// Two scaled fp32 values -> one byte: `lo` in bits 0..3, `hi` in bits 4..7.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+#ifndef MXFP4_SOFTWARE_ENCODE
+    uint16_t r;
+    // the first source operand lands in the upper nibble, the second in the lower
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+#else
+    // Threshold count: the code is the number of grid midpoints below |v|, where a value
+    // sitting exactly on a midpoint moves up only if that lands on an even code.
+    auto enc = [](float v) -> uint32_t {
+        const float a = fabsf(v);
+        uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+        return c | ((__float_as_uint(v) >> 28) & 8u);
+    };
+    return enc(lo) | (enc(hi) << 4);
+#endif
+}
+
+// Quantize one 1x32 block held as 16 words of bf16 pairs (element 2i in the low half of
+// word i). Writes 4 words of packed codes (element 2i in the low nibble of its byte) and
+// returns the e8m0 byte.
+__device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&w)[16], uint32_t (&out)[4]) {
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
+    const uint32_t amax_bits = max(mx & 0xFFFFu, mx >> 16) << 16;
+    const int s = scale_exponent(amax_bits);
+    const float m = inv_scale(s);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t packed = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t word = w[4 * j + i];
+            const float even = __fmul_rn(__uint_as_float(word << 16), m);
+            const float odd = __fmul_rn(__uint_as_float(word & 0xFFFF0000u), m);
+            packed |= e2m1x2(even, odd) << (8 * i);
+        }
+        out[j] = packed;
+    }
+    return static_cast<uint32_t>(s + 127);
+}
+
+// Load 32 consecutive bf16 (64 bytes, 16-byte aligned) as 16 words.
+__device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[16]) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(p + i);
+        w[4 * i + 0] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+}
+
+// Byte offset of (row r, 32-block kb) inside the tensor-core scale-factor layout:
+// 512-byte chunks of 128 rows x 4 blocks, chunk index (r / 128) * groups + kb / 4; within a
+// chunk, row r % 32 owns 16 bytes holding rows r%32, +32, +64, +96 (4 blocks each).
+__device__ __forceinline__ uint32_t sf_chunk_offset(uint32_t r, uint32_t kb, uint32_t groups) {
+    return ((r >> 7) * groups + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (kb & 3u);
+}
+
+}  // namespace mxfp4

@@ -1,0 +1,176 @@
+/*
+ * mxfp4_gb300.h -- C ABI of the GB300 (sm_103a) block-scaled MXFP4 GEMM library.
+ *
+ *   C[M,N] (bf16) = MXFP4(A[M,K] bf16) . MXFP4(B[N,K])^T
+ *
+ * MXFP4 here is the format the "amd-mxfp4-mm" leaderboard submissions compute (submission
+ * 711914, `_mxfp4_quant_tile`; submission 608632, `_hw_mxfp4_quant_op`): along K, every
+ * block of 32 consecutive elements of a row shares one e8m0 scale byte; each element is a
+ * 4-bit e2m1 code (bit 3 sign, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) and two codes share a
+ * byte, the even-indexed element in the low nibble.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers (cudaMalloc'd or equivalent) unless stated.
+ *     The caller owns every buffer; the library never allocates, frees or synchronizes
+ *     (except mxfp4_device_status, which synchronizes the given stream by design).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Work is
+ *     enqueued asynchronously on it.
+ *   - Matrices are row-major with the K dimension contiguous. Sizes are element counts.
+ *   - Return value: an mxfp4_status. Arguments are validated before anything is enqueued;
+ *     on an error nothing is written. MXFP4_ERR_CUDA reports a launch failure (see
+ *     mxfp4_last_cuda_error). Kernel-side failures (a bounded wait that ran out) are not
+ *     visible in the return value of the asynchronous call; read them with
+ *     mxfp4_device_status.
+ *   - Inputs must be finite; NaN or Inf in A or B gives unspecified (but memory-safe)
+ *     results. Scale bytes of 255 (e8m0 NaN) in B likewise.
+ *   - The library targets compute capability 10.3 (GB300) only; other devices give
+ *     MXFP4_ERR_ARCH.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_ARG = 1,       /* null pointer, negative size, bad option value */
+    MXFP4_ERR_SHAPE = 2,     /* K not a positive multiple of 64, ld smaller than K, too large */
+    MXFP4_ERR_ALIGN = 3,     /* pointer or leading dimension misaligned (see each call) */
+    MXFP4_ERR_ARCH = 4,      /* current device is not compute capability 10.3 */
+    MXFP4_ERR_CUDA = 5,      /* a CUDA runtime/driver call or a launch failed */
+    MXFP4_ERR_TIMEOUT = 6,   /* a device-side bounded wait ran out (from mxfp4_device_status) */
+    MXFP4_ERR_WORKSPACE = 7  /* workspace missing or smaller than mxfp4_gemm_workspace_size */
+} mxfp4_status;
+
+/* Human-readable name of a status code (static string). */
+const char *mxfp4_status_string(int status);
+
+/* Last CUDA error code (cudaError_t as int) recorded by a call that returned MXFP4_ERR_CUDA
+ * on this host thread, 0 if none. */
+int mxfp4_last_cuda_error(void);
+
+/* Library ABI version (major*100 + minor). */
+int mxfp4_version(void);
+
+/*
+ * mxfp4_quantize -- quantize a bf16 matrix to MXFP4 (one e8m0 scale per 1x32 block).
+ * Follows submission 711914, `_mxfp4_quant_tile`: amax = max|x| of the block in fp32; the
+ * amax bit pattern plus 0x200000, masked with 0xFF800000, rounds it to a power of two;
+ * s = clamp(floor(log2(amax_r)) - 2, -127, 127); scale byte = s + 127; each element
+ * x * 2^-s is rounded to the nearest e2m1 value (ties to even, saturating at 6, the sign
+ * kept even when the value rounds to zero) and packed even-low / odd-high.
+ *   x       : bf16 [rows, K], row stride `ld` elements (ld >= K). 16-byte aligned, ld % 8 == 0.
+ *   q       : out, uint8 [rows, K/2], row stride K/2 bytes. 16-byte aligned.
+ *   scales  : out, uint8 [rows, K/32], row stride K/32 bytes (no alignment requirement).
+ *   K       : multiple of 32.  rows == 0 or K == 0 is a no-op.
+ * Bytes are bit-identical to the CPU oracle.
+ */
+int mxfp4_quantize(const void *x, int64_t rows, int64_t K, int64_t ld,
+                   void *q, void *scales, void *stream);
+
+/*
+ * mxfp4_prepack_b_size -- bytes of the packed-B buffer mxfp4_prepack_b writes for an
+ * [N, K] weight matrix: the e2m1 bytes (N*K/2, natural layout) followed, at the next
+ * 1024-byte boundary, by the scale factors rearranged into the tensor-core layout
+ * (ceil(N/128) tiles x ceil(K/256)*2 groups x 512 bytes). 0 for invalid sizes.
+ */
+size_t mxfp4_prepack_b_size(int64_t N, int64_t K);
+
+/*
+ * mxfp4_prepack_b -- one-time relayout of a pre-quantized weight matrix B for mxfp4_gemm.
+ * The pages prepare B outside the timed call too (their harness shuffles B and its scales
+ * for the MFMA layout, submission 608632 `_new_generate_input`); here the e2m1 bytes keep
+ * their layout and the e8m0 scales move into the 128-row x 4-block chunks the tcgen05
+ * block-scaled MMA reads from tensor memory.
+ *   bq     : uint8 [N, K/2] packed e2m1 (even element low nibble). 16-byte aligned.
+ *   bs     : uint8 [N, K/32] e8m0 scales (as written by mxfp4_quantize).
+ *   K      : positive multiple of 64.  N >= 1.
+ *   packed : out, mxfp4_prepack_b_size(N, K) bytes, 1024-byte aligned. Must not overlap
+ *            bq or bs.
+ */
+int mxfp4_prepack_b(const void *bq, const void *bs, int64_t N, int64_t K,
+                    void *packed, void *stream);
+
+/*
+ * mxfp4_gemm_workspace_size -- bytes of device workspace mxfp4_gemm needs for this shape
+ * on the CURRENT device (the split-K plan depends on its SM count). The workspace holds
+ * the quantized A for the two-kernel path, fp32 split-K partial tiles and one arrival
+ * counter per output tile.
+ */
+size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * mxfp4_workspace_init -- zero a workspace before its first use (cudaMemsetAsync on
+ * `stream`). The split-K arrival counters must start at zero; every completed mxfp4_gemm
+ * leaves them at zero again, so this is needed once per buffer (and again after a call
+ * whose device status reported an error).
+ */
+int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * mxfp4_gemm -- C = MXFP4(A) . MXFP4(B)^T in bf16, A quantized inside the call.
+ * The products of e2m1 values and e8m0 scales are accumulated in fp32 on the tensor cores
+ * (tcgen05.mma kind::mxf4, block size 32) and rounded once to bf16 (round to nearest even).
+ *   a        : bf16 [M, K], row stride lda elements (lda >= K, lda % 8 == 0), 16-byte aligned.
+ *   packed_b : buffer written by mxfp4_prepack_b for the same N and K.
+ *   c        : out, bf16 [M, N], row stride ldc elements (ldc >= N), 2-byte aligned.
+ *   workspace: ws_bytes >= mxfp4_gemm_workspace_size(M, N, K), 256-byte aligned, zeroed
+ *              once by mxfp4_workspace_init. Calls sharing a workspace must be ordered
+ *              (same stream, or synchronized); overlapping calls on one workspace race.
+ *   K        : positive multiple of 64.  M == 0 or N == 0 is a no-op.
+ * A is quantized exactly like mxfp4_quantize (bit-identical codes and scales). With split-K
+ * the fp32 partial sums are added in a fixed order, so results are run-to-run identical.
+ */
+int mxfp4_gemm(const void *a, int64_t M, int64_t K, int64_t lda,
+               const void *packed_b, int64_t N,
+               void *c, int64_t ldc,
+               void *workspace, size_t ws_bytes, void *stream);
+
+/* Plan overrides for mxfp4_gemm_ex (tests and measurement). Zero-initialise, then set. */
+typedef struct {
+    int path;    /* 0 = automatic, 1 = A quantized inside the GEMM's producer warps (fused),
+                    2 = standalone quantize kernel into the workspace, then the GEMM */
+    int splits;  /* 0 = automatic, else the number of K slices per output tile (>= 1) */
+    int reserved[6];
+} mxfp4_gemm_options;
+
+/* mxfp4_gemm with an explicit plan. The workspace must be at least
+ * mxfp4_gemm_workspace_size_ex(M, N, K, opts). opts == NULL is the automatic plan. */
+int mxfp4_gemm_ex(const void *a, int64_t M, int64_t K, int64_t lda,
+                  const void *packed_b, int64_t N,
+                  void *c, int64_t ldc,
+                  void *workspace, size_t ws_bytes,
+                  const mxfp4_gemm_options *opts, void *stream);
+size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts);
+
+/* The plan mxfp4_gemm_ex would run: path (1 fused / 2 two-kernel), splits, M tile, number
+ * of CTAs, pipeline stages. Returns MXFP4_OK or an argument error. */
+int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts,
+                    int *path, int *splits, int *m_tile, int *ctas, int *stages);
+
+/*
+ * mxfp4_device_status -- synchronize `stream`, then read and clear the library's device
+ * error word for the current device: MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait (the kernel then skipped its remaining work and released its resources;
+ * its outputs are undefined). Returns MXFP4_ERR_CUDA if the synchronization failed.
+ */
+int mxfp4_device_status(void *stream);
+
+/*
+ * mxfp4_selftest_timeout -- launch one CTA that waits on a barrier nothing ever signals,
+ * with a wait limit of `limit_us` microseconds (1..1000000). The kernel gives up, records
+ * MXFP4_ERR_TIMEOUT in the device error word and exits normally, so a following
+ * mxfp4_device_status returns MXFP4_ERR_TIMEOUT. Exercises the failure path without a fault.
+ */
+int mxfp4_selftest_timeout(int limit_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_H */

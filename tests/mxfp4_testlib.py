@@ -1,0 +1,81 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI binding and the
+CPU oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from block_scaled_mxfp4_bf16_gb300 import workloads
+
+REL_TOL = 8e-3       # |C - C_ref| <= REL_TOL * |C_ref| + RMS_TOL * rms(C_ref)
+RMS_TOL = 1e-3
+
+
+def gpu_available() -> bool:
+    return torch.cuda.is_available()
+
+
+def to_np_u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.uint8)
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_to_f64(workloads.bf16_bits(t))
+
+
+def quantize_both(x_cpu: torch.Tensor):
+    """(gpu_q, gpu_s, ref_q, ref_s) for a CPU bf16 matrix."""
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    q, s = mx.mxfp4_quantize(x_cpu.cuda())
+    rq, rs = oracle.quantize(workloads.bf16_bits(x_cpu))
+    torch.cuda.synchronize()
+    return to_np_u8(q), to_np_u8(s), rq, rs
+
+
+def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str) -> None:
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        r, c = bad[0]
+        raise AssertionError(f"{what}: {len(bad)} mismatching bytes, first at {tuple(bad[0])}: "
+                             f"got {got[r, c]:#04x} want {want[r, c]:#04x}")
+
+
+def check_tolerance(c: np.ndarray, c_ref: np.ndarray, what: str) -> float:
+    ok, worst = oracle.tolerance_ok(c, c_ref, REL_TOL, RMS_TOL)
+    if not ok:
+        err = np.abs(c - c_ref)
+        i = np.unravel_index(np.argmax(err - REL_TOL * np.abs(c_ref)), c.shape)
+        raise AssertionError(f"{what}: tolerance exceeded (worst ratio {worst:.3g}); at {i}: "
+                             f"got {c[i]!r} want {c_ref[i]!r}")
+    return worst
+
+
+def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: int = 0, lda_pad: int = 0,
+             ldc_pad: int = 0, canary: float = 777.0):
+    """Quantize B and prepack it on the GPU, run mxfp4_gemm, check the B bytes against the
+    oracle and that nothing outside C[:M,:N] was written. Returns (C as fp64 [M,N], Bq, Bs)."""
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    M, K = a_cpu.shape
+    N = b_cpu.shape[0]
+    b = b_cpu.cuda()
+    bq, bs = mx.mxfp4_quantize(b)
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a_store = torch.zeros(M, K + lda_pad, dtype=torch.bfloat16, device="cuda")
+    a_store[:, :K] = a_cpu.cuda()
+    a = a_store[:, :K]
+    c_store = torch.full((M + 1, N + ldc_pad), canary, dtype=torch.bfloat16, device="cuda")
+    c = c_store[:M, :N]
+    mx.mxfp4_gemm(a, packed, N, c=c, path=path, splits=splits)
+    torch.cuda.synchronize()
+    st = mx.mxfp4_device_status()
+    assert st == 0, f"device status {st}"
+    outside = torch.ones_like(c_store, dtype=torch.bool)
+    outside[:M, :N] = False
+    assert bool((c_store[outside] == canary).all()), "GEMM wrote outside C"
+    return bf16_to_f64(c.cpu()), to_np_u8(bq), to_np_u8(bs)
+
+
+def oracle_c(a_cpu: torch.Tensor, bq: np.ndarray, bs: np.ndarray) -> np.ndarray:
+    aq, as_ = oracle.quantize(workloads.bf16_bits(a_cpu))
+    return oracle.mxfp4_gemm_ref(aq, as_, bq, bs)

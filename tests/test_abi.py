@@ -1,0 +1,63 @@
+"""CPU-only checks of the boundary: the library builds for sm_103a, loads without a GPU and
+exports every function include/mxfp4_gb300.h declares; pure host helpers answer correctly."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4_gb300.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_mxfp4_bf16_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_three_calls():
+    names = _declared_functions()
+    for required in ("mxfp4_quantize", "mxfp4_prepack_b", "mxfp4_gemm"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.mxfp4_status_string.restype = ctypes.c_char_p
+    assert lib.mxfp4_status_string(0) == b"MXFP4_OK"
+    assert lib.mxfp4_status_string(6) == b"MXFP4_ERR_TIMEOUT"
+    assert lib.mxfp4_version() >= 100
+
+
+def test_prepack_size_is_pure_host_arithmetic(lib):
+    lib.mxfp4_prepack_b_size.restype = ctypes.c_size_t
+    lib.mxfp4_prepack_b_size.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    # e2m1 bytes, then 1 KB aligned: ceil(N/128) tiles x 2*ceil(K/256) groups x 512 bytes
+    assert lib.mxfp4_prepack_b_size(2112, 7168) == 2112 * 3584 + 17 * 56 * 512
+    assert lib.mxfp4_prepack_b_size(100, 64) == 4096 + 1 * 2 * 512
+    assert lib.mxfp4_prepack_b_size(100, 96) == 0     # K must be a multiple of 64
+    assert lib.mxfp4_prepack_b_size(0, 64) == 0
+
+
+def test_no_cpu_fallback_when_cuda_missing(lib):
+    # without a GPU every compute entry point must refuse, not compute on the host
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib.mxfp4_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    buf = ctypes.create_string_buffer(256)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    assert lib.mxfp4_quantize(p, 1, 32, 32, p, p, None) != 0

@@ -1,0 +1,132 @@
+"""GPU GEMM parity: C from mxfp4_gemm (tcgen05 kind::mxf4, through the C ABI) against the
+fp64 oracle, within |C - C_ref| <= 8e-3 |C_ref| + 1e-3 rms(C_ref)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_mxfp4_bf16_gb300 import workloads
+from mxfp4_testlib import assert_bytes_equal, bf16_to_f64, check_tolerance, oracle_c, run_gemm, to_np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def _mx():
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    return mx
+
+
+def test_single_product_lands_in_place():
+    # one nonzero per operand: exposes any error in operand, scale-factor or output layout
+    M, N, K = 5, 200, 512
+    for (m, n, k) in [(0, 0, 0), (3, 131, 300), (4, 199, 511), (1, 64, 33)]:
+        a = torch.zeros(M, K, dtype=torch.bfloat16)
+        b = torch.zeros(N, K, dtype=torch.bfloat16)
+        a[m, k] = 3.0
+        b[n, k] = -0.75
+        for path in (1, 2):
+            c, _, _ = run_gemm(a, b, path=path)
+            want = np.zeros((M, N))
+            want[m, n] = -2.25
+            assert np.array_equal(c, want), (m, n, k, path, np.argwhere(c != want)[:5])
+
+
+SMALL = [
+    # M, N, K -- tails in every dimension, K not a multiple of 256, M past one 256-token tile
+    (1, 128, 64), (5, 200, 192), (16, 384, 512), (8, 2112, 1024), (17, 130, 320),
+    (32, 256, 1536), (33, 640, 256), (64, 512, 768), (100, 300, 512), (256, 256, 256), (300, 136, 128),
+]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_gemm_small_shapes_vs_oracle(M, N, K, path):
+    a = workloads.random_bf16(M, K, seed=M * 1000 + K)
+    b = workloads.random_bf16(N, K, seed=N * 1000 + K + 1, scale=0.5)
+    for splits in (0, 1, 3):
+        c, bq, bs = run_gemm(a, b, path=path, splits=splits, lda_pad=8, ldc_pad=3)
+        rq, rs = oracle.quantize(workloads.bf16_bits(b))
+        assert_bytes_equal(bq, rq, "B e2m1")
+        assert_bytes_equal(bs, rs, "B scales")
+        check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} path {path} splits {splits}")
+
+
+@pytest.mark.parametrize("w", workloads.WORKLOADS, ids=lambda w: w.name)
+def test_gemm_workloads_sampled_vs_oracle(w):
+    # full-size workloads in the automatic plan the benchmark times; the oracle computes a
+    # sample of outputs one by one (every row, 384 random columns)
+    a, b = workloads.make_inputs(w, seed=0)
+    c, bq, bs = run_gemm(a, b)
+    rq, rs = oracle.quantize(workloads.bf16_bits(b))
+    assert_bytes_equal(bs, rs, "B scales")
+    assert_bytes_equal(bq, rq, "B e2m1")
+    aq, as_ = oracle.quantize(workloads.bf16_bits(a))
+    rng = np.random.default_rng(1)
+    cols = np.concatenate([rng.choice(w.N, 380, replace=False), [0, w.N - 1, 127, 128]])
+    im = np.repeat(np.arange(w.M), cols.size)
+    inn = np.tile(cols, w.M)
+    ref = oracle.gemm_entries(aq, as_, bq, bs, im, inn)
+    check_tolerance(c[im, inn], ref, w.name)
+
+
+@pytest.mark.parametrize("w", workloads.EXTRA_WORKLOADS, ids=lambda w: w.name)
+def test_gemm_leaderboard_shapes_full_oracle(w):
+    a, b = workloads.make_inputs(w, seed=2)
+    c, bq, bs = run_gemm(a, b)
+    check_tolerance(c, oracle_c(a, bq, bs), w.name)
+
+
+def test_gemm_outlier_workload_full_oracle_both_paths():
+    w = workloads.by_name("M32_N4096_K512")
+    a, b = workloads.make_inputs(w, seed=0)
+    for path in (1, 2):
+        c, bq, bs = run_gemm(a, b, path=path)
+        check_tolerance(c, oracle_c(a, bq, bs), f"{w.name} path {path}")
+
+
+def test_gemm_run_to_run_identical():
+    mx = _mx()
+    w = workloads.by_name("M8_N2112_K7168")
+    a, b = workloads.make_inputs(w, seed=4)
+    a, b = a.cuda(), b.cuda()
+    bq, bs = mx.mxfp4_quantize(b)
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c1 = mx.mxfp4_gemm(a, packed, w.N).clone()
+    c2 = mx.mxfp4_gemm(a, packed, w.N).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    assert mx.mxfp4_gemm_plan(w.M, w.N, w.K)["splits"] > 1
+
+
+def test_gemm_empty_and_errors():
+    mx = _mx()
+    L = mx.load_library()
+    st = torch.cuda.current_stream().cuda_stream
+    a = torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda")
+    bq = torch.zeros(64, 64, dtype=torch.uint8, device="cuda")
+    bs = torch.zeros(64, 4, dtype=torch.uint8, device="cuda")
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    # M == 0 and N == 0 are no-ops
+    assert L.mxfp4_gemm(a.data_ptr(), 0, 128, 128, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 0
+    assert L.mxfp4_gemm(a.data_ptr(), 4, 128, 128, packed.data_ptr(), 0, c.data_ptr(), 64, None, 0, st) == 0
+    # K not a multiple of 64, lda < K, misaligned A, missing workspace
+    assert L.mxfp4_gemm(a.data_ptr(), 4, 96, 128, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 2
+    assert L.mxfp4_gemm(a.data_ptr(), 4, 128, 64, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 2
+    assert L.mxfp4_gemm(a.data_ptr() + 2, 4, 128, 128, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 3
+    need = mx.mxfp4_gemm_workspace_size(4, 64, 128)
+    if need:
+        assert L.mxfp4_gemm(a.data_ptr(), 4, 128, 128, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 7
+    assert L.mxfp4_prepack_b_size(64, 96) == 0
+
+
+def test_timeout_is_reported_not_hung():
+    mx = _mx()
+    assert mx.mxfp4_device_status() == 0
+    mx.mxfp4_selftest_timeout(2000)          # waits 2 ms on a barrier nobody signals
+    assert mx.mxfp4_device_status() == 6     # MXFP4_ERR_TIMEOUT, context still usable
+    assert mx.mxfp4_device_status() == 0     # cleared by the read
+    x = torch.ones(2, 64, dtype=torch.bfloat16, device="cuda")
+    q, s = mx.mxfp4_quantize(x)
+    torch.cuda.synchronize()
+    assert int(s[0, 0].item()) == 125
