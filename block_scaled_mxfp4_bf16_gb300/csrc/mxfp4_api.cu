@@ -365,3 +365,108 @@ int mxfp4_selftest_timeout(int limit_us, void* stream) {
 }
 
 }  // extern "C"
+
+// ====================================================================== no-allocation variant
+//
+// mxfp4_gemm_noalloc: the same launches as mxfp4_gemm_ex, with the workspace replaced by
+// the file-scope array below. Host code must not use the array's name as a device pointer
+// (on the host it only names a stand-in); its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+
+namespace mxfp4 {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MXFP4_NOALLOC_SCRATCH_BYTES];
+
+static int noalloc_scratch(int device, uint8_t** out) {
+    static std::mutex mu;
+    static uint8_t* addr[64] = {};
+    if (device < 0 || device >= 64) return MXFP4_ERR_ARG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        addr[device] = static_cast<uint8_t*>(p);
+    }
+    *out = addr[device];
+    return MXFP4_OK;
+}
+
+}  // namespace mxfp4
+
+extern "C" int mxfp4_gemm_noalloc(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
+                                  void* c, int64_t ldc, void* stream) {
+    if (M < 0 || N < 0 || K < 0) return MXFP4_ERR_ARG;
+    if (K == 0 || K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (M == 0 || N == 0) return MXFP4_OK;
+    if (lda < K || ldc < N) return MXFP4_ERR_SHAPE;
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 30)) return MXFP4_ERR_SHAPE;
+    if (!a || !packed_b || !c) return MXFP4_ERR_ARG;
+    if (!aligned(a, 16) || lda % 8 != 0 || !aligned(packed_b, 1024) || !aligned(c, 2)) return MXFP4_ERR_ALIGN;
+    DeviceInfo di;
+    int st = device_info(&di);
+    if (st != MXFP4_OK) return st;
+    // the automatic plan; fewer K slices while its scratch does not fit the array
+    GemmPlan plan;
+    st = make_plan(M, N, K, 0, 0, di.sm_count, &plan);
+    if (st != MXFP4_OK) return st;
+    while (plan.ws_total > MXFP4_NOALLOC_SCRATCH_BYTES && plan.splits > 1) {
+        st = make_plan(M, N, K, plan.path, plan.splits / 2, di.sm_count, &plan);
+        if (st != MXFP4_OK) return st;
+    }
+    if (plan.ws_total > MXFP4_NOALLOC_SCRATCH_BYTES) return MXFP4_ERR_WORKSPACE;
+    uint8_t* ws = nullptr;
+    st = noalloc_scratch(di.device, &ws);
+    if (st != MXFP4_OK) return st;
+    auto s = static_cast<cudaStream_t>(stream);
+    const uint8_t* pb = static_cast<const uint8_t*>(packed_b);
+    CUtensorMap tmap_b, tmap_a;
+    st = make_map(&tmap_b, pb, N, K / 2, kTileN);
+    if (st != MXFP4_OK) return st;
+    tmap_a = tmap_b;
+    if (plan.path == 2) {
+        st = make_map(&tmap_a, ws + plan.ws_aq, M, K / 2, plan.m_tile);
+        if (st != MXFP4_OK) return st;
+    }
+    if (plan.splits > 1) {   // the array keeps the last call's contents: start the counters at zero
+        cudaError_t e = cudaMemsetAsync(ws + plan.ws_ctr, 0,
+                                        static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (plan.path == 2) {
+        const int64_t rows_cover = static_cast<int64_t>(align_up(static_cast<size_t>(plan.m_tiles) * plan.m_tile, 128));
+        cudaError_t e = launch_quantize(static_cast<const uint16_t*>(a), M, K, lda, ws + plan.ws_aq, ws + plan.ws_sfa,
+                                        rows_cover, plan.groups, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    GemmArgs g = {};
+    g.a = static_cast<const uint16_t*>(a);
+    g.lda = lda;
+    g.sfa = ws + plan.ws_sfa;
+    g.sfb = pb + packed_sf_offset(N, K);
+    g.c = static_cast<uint16_t*>(c);
+    g.ldc = ldc;
+    g.part = plan.splits > 1 ? reinterpret_cast<float*>(ws + plan.ws_part) : nullptr;
+    g.ctr = plan.splits > 1 ? reinterpret_cast<uint32_t*>(ws + plan.ws_ctr) : nullptr;
+    g.status = di.status;
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.m_tile = plan.m_tile;
+    g.nmc = plan.nmc;
+    g.m_tiles = plan.m_tiles;
+    g.n_tiles = plan.n_tiles;
+    g.splits = plan.splits;
+    g.k_atoms = plan.k_atoms;
+    g.groups = plan.groups;
+    g.stages = plan.stages;
+    g.off_a = plan.off_a;
+    g.off_sfb = plan.off_sfb;
+    g.off_sfa = plan.off_sfa;
+    g.off_bar = plan.off_bar;
+    g.tmem_cols = plan.tmem_cols;
+    g.fused = plan.path == 1 ? 1 : 0;
+    g.wait_limit_ns = g_wait_limit_ns;
+    cudaError_t e = launch_gemm(plan, tmap_b, tmap_a, g, s);
+    return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+}

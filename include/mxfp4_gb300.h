@@ -169,6 +169,37 @@ int mxfp4_device_status(void *stream);
  */
 int mxfp4_selftest_timeout(int limit_us, void *stream);
 
+/*
+ * mxfp4_gemm_noalloc -- mxfp4_gemm for callers that cannot allocate device memory.
+ * (No counterpart in the pages: it exists for callers, not for the method.)
+ *
+ * Some callers have no way to hand the library a workspace: a plugin running inside an
+ * inference engine whose host owns the whole device-memory plan and forbids allocation once
+ * it runs, or a latency-critical serving loop that must never call cudaMalloc/cudaFree
+ * because those can synchronize the whole device. This entry point needs no workspace
+ * argument: its scratch (split-K partial tiles, split-K arrival counters and the quantized A
+ * of the two-kernel path) lives in one statically sized array inside the library, which
+ * every GPU that loads the library keeps for the life of the process.
+ *
+ *   Arguments and results are those of mxfp4_gemm without `workspace` / `ws_bytes`; the
+ *   output equals mxfp4_gemm's within the library's tolerance (the split-K slice count may be
+ *   lowered to fit the array, which can change the fp32 summation order).
+ *   Scratch limit: MXFP4_NOALLOC_SCRATCH_BYTES. A shape whose scratch cannot fit even
+ *   without split-K (the quantized A of the two-kernel path, M*K/2 bytes plus its scales and
+ *   64 KB of counters) returns MXFP4_ERR_WORKSPACE before anything is enqueued.
+ *   No allocation: the call never calls cudaMalloc, cudaFree or any allocating routine.
+ *   First call per device: it looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: all calls on a device share the one array and it keeps the previous call's
+ *   contents. Each call clears the counters it uses (cudaMemsetAsync on `stream`) before its
+ *   kernels. Calls that can overlap on the GPU (different streams without ordering, or
+ *   several host threads) race on the array and give wrong results: order them.
+ */
+#define MXFP4_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int mxfp4_gemm_noalloc(const void *a, int64_t M, int64_t K, int64_t lda,
+                       const void *packed_b, int64_t N,
+                       void *c, int64_t ldc, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

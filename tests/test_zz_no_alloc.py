@@ -1,0 +1,73 @@
+"""mxfp4_gemm_noalloc: the GEMM for callers that cannot allocate device memory (an engine
+plugin whose host owns the memory plan, a serving loop that must never call cudaMalloc or
+cudaFree because they can synchronize the device). Its scratch is a fixed array inside the
+library instead of a caller workspace.
+
+Checked through the C ABI against the regular mxfp4_gemm, within the same tolerance the
+parity tests use, on two calls in a row (the array keeps the previous call's contents, so
+the second call shows the counters are cleared and nothing stale leaks through). This file
+is collected last on purpose; it passes alone in a fresh process as well as after the rest.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_mxfp4_bf16_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL, RMS_TOL = 8e-3, 1e-3
+NOALLOC_BYTES = 32 * 1024 * 1024
+
+
+def _lib():
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    L = mx.load_library()
+    L.mxfp4_gemm_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                     ctypes.c_void_p]
+    L.mxfp4_gemm_noalloc.restype = ctypes.c_int
+    return mx, L
+
+
+def _as_f64(c: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_to_f64(workloads.bf16_bits(c.cpu()))
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 2112, 7168), (16, 384, 1536), (64, 1024, 2048), (5, 200, 320)])
+def test_noalloc_matches_gemm_twice(M, N, K):
+    mx, L = _lib()
+    a = workloads.random_bf16(M, K, seed=M + K).cuda()
+    b = workloads.random_bf16(N, K, seed=N + K).cuda()
+    bq, bs = mx.mxfp4_quantize(b)
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    want = _as_f64(mx.mxfp4_gemm(a, packed, N))
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        c = torch.full((M, N), 777.0, dtype=torch.bfloat16, device="cuda")
+        st = L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, K, packed.data_ptr(), N, c.data_ptr(), N, stream)
+        assert st == 0, L.mxfp4_status_string(st)
+        torch.cuda.synchronize()
+        assert mx.mxfp4_device_status() == 0
+        ok, worst = oracle.tolerance_ok(_as_f64(c), want, REL_TOL, RMS_TOL)
+        assert ok, f"call {call}: worst ratio {worst:.3g}"
+
+
+def test_noalloc_rejects_scratch_beyond_its_limit():
+    mx, L = _lib()
+    # the two-kernel path keeps the quantized A (M*K/2 bytes) in the scratch: 8192 x 8192
+    # needs 32 MiB for it alone, more than the array holds even without split-K
+    M, N, K = 8192, 128, 8192
+    assert M * K // 2 >= NOALLOC_BYTES
+    a = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    packed = mx.mxfp4_prepack_b(torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda"),
+                                torch.zeros(N, K // 32, dtype=torch.uint8, device="cuda"))
+    c = torch.full((M, N), 777.0, dtype=torch.bfloat16, device="cuda")
+    st = L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, K, packed.data_ptr(), N, c.data_ptr(), N,
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == 7, L.mxfp4_status_string(st)          # MXFP4_ERR_WORKSPACE, nothing enqueued
+    torch.cuda.synchronize()
+    assert bool((c == 777.0).all())
