@@ -87,7 +87,12 @@ def _events():
 
 
 def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float = 0.0, e2e: bool = False):
-    """Time `steps` back-to-back mxfp4_gemm calls of workload w. Returns a dict."""
+    """Time exactly `steps` back-to-back mxfp4_gemm calls of workload w.
+
+    The calls are captured in CUDA graphs (programmatic-launch edges kept) and replayed, so
+    the number is device time per call with host launch cost out of the way; each call uses
+    its own copy of A, packed B and C, rotating over enough copies (> 3x L2) that the
+    weights stream from HBM. Returns a dict."""
     dev = torch.device("cuda")
     a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
     b = b_cpu.to(dev)
@@ -96,66 +101,93 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
     del b, bq, bs
     a0 = a_cpu.to(dev)
     per_copy = packed0.numel() + a0.numel() * 2 + w.M * w.N * 2
-    copies = max(2, min(256, -(-3 * l2_bytes // per_copy)))
+    copies = max(2, min(512, -(-3 * l2_bytes // per_copy)))
     packs = [packed0] + [packed0.clone() for _ in range(copies - 1)]
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
     Cs = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
     plan = mx.mxfp4_gemm_plan(w.M, w.N, w.K)
     ws = torch.empty(max(1, mx.mxfp4_gemm_workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=dev)
-    mx.mxfp4_workspace_init(ws)
-    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
 
-    def step(i):
+    def step(i, stream):
         j = i % copies
         mx.mxfp4_gemm(As[j], packs[j], w.N, c=Cs[j], workspace=ws, stream=stream)
 
-    for i in range(warmup):
-        step(i)
+    with torch.cuda.stream(side):
+        for i in range(max(warmup, copies)):
+            step(i, side)
+    torch.cuda.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n):
+                step(i, side)
+        return g
+
+    chunk = min(steps, 1024)
+    g_main = capture(chunk)
+    tail = steps % chunk
+    g_tail = capture(tail) if tail else None
+    reps = steps // chunk
+    for _ in range(2):
+        g_main.replay()
     torch.cuda.synchronize()
     if soak_s > 0:
         t_end = time.time() + soak_s
-        i = 0
         while time.time() < t_end:
-            for _ in range(200):
-                step(i)
-                i += 1
+            g_main.replay()
             torch.cuda.synchronize()
     if torch.distributed.is_initialized():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0, e1 = _events()
-    e0.record(stream)
-    for i in range(steps):
-        step(i)
-    e1.record(stream)
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for _ in range(reps):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        e1.record(side)
     e1.synchronize()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     status = mx.mxfp4_device_status()
     res = {"us_per_call": 1000.0 * ms / steps, "elapsed_ms": ms, "copies": copies, "plan": plan,
            "kernels_per_call": 1 if plan["path"] == 1 else 2, "status": status}
+    # the same calls launched one by one from the host (no graph), for comparison
+    n_direct = min(steps, 2000)
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for i in range(n_direct):
+            step(i, side)
+        e1.record(side)
+    e1.synchronize()
+    res["direct_us_per_call"] = 1000.0 * e0.elapsed_time(e1) / n_direct
     if e2e:
         # end to end through the public call: pinned host A -> device, GEMM, C -> pinned host
         a_host = a_cpu.pin_memory()
         c_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
-        for i in range(3):
-            As[0].copy_(a_host, non_blocking=True)
-            step(0)
-            c_host.copy_(Cs[0], non_blocking=True)
-        torch.cuda.synchronize()
-        n_e2e = max(20, steps // 10)
-        e0.record(stream)
-        for i in range(n_e2e):
-            j = i % copies
-            As[j].copy_(a_host, non_blocking=True)
-            step(j)
-            c_host.copy_(Cs[j], non_blocking=True)
-        e1.record(stream)
+        n_e2e = max(20, min(steps, 2000))
+        with torch.cuda.stream(side):
+            for i in range(3):
+                As[0].copy_(a_host, non_blocking=True)
+                step(0, side)
+                c_host.copy_(Cs[0], non_blocking=True)
+            side.synchronize()
+            e0.record(side)
+            for i in range(n_e2e):
+                j = i % copies
+                As[j].copy_(a_host, non_blocking=True)
+                step(j, side)
+                c_host.copy_(Cs[j], non_blocking=True)
+            e1.record(side)
         e1.synchronize()
         res["e2e_us_per_call"] = 1000.0 * e0.elapsed_time(e1) / n_e2e
         res["h2d_bytes"] = w.M * w.K * 2
         res["d2h_bytes"] = w.M * w.N * 2
-    del packs, As, Cs, ws
+    del packs, As, Cs, ws, g_main, g_tail
+    torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
 
@@ -243,6 +275,7 @@ def main():
             r = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2)
             gbs = ws_.algorithmic_bytes / (r["us_per_call"] * 1e-6) / 1e9
             per_shape[ws_.name] = {"us_per_call": round(r["us_per_call"], 3),
+                                   "direct_us_per_call": round(r["direct_us_per_call"], 3),
                                    "tflops": round(ws_.flops / (r["us_per_call"] * 1e-6) / 1e12, 2),
                                    "algorithmic_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
                                    "path": r["plan"]["path"], "splits": r["plan"]["splits"],
@@ -273,6 +306,8 @@ def main():
         "e2e": {"value": round(main_res["e2e_us_per_call"], 3), "unit": "us/call",
                 "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},
         "gpu_launches": args.steps * main_res["kernels_per_call"],
+        "timing": "CUDA-graph replay of back-to-back calls; direct host launches: "
+                  f"{main_res['direct_us_per_call']:.3f} us/call",
         "clocks": clocks,
         "cpu_baseline": cpu,
         "per_shape": per_shape,

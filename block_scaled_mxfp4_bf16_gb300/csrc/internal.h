@@ -8,52 +8,68 @@
 namespace mxfp4 {
 
 constexpr int kMaxStages = 8;
-constexpr int kGemmThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 quant + epilogue
+constexpr int kGemmThreads = 192;          // warp 0 copies, warp 1 MMA, warps 2..5 quant + epilogue
 constexpr int kTileN = 128;                // weight rows per MMA (the MMA's M)
 constexpr int kAtomK = 256;                // K elements per pipeline step (128-byte rows)
 constexpr int kMaxMTile = 256;             // tokens per tile (the MMA's N)
-constexpr uint32_t kBStageBytes = kTileN * kAtomK / 2;   // 16 KB
+constexpr int kMaxSplits = 16;             // K slices per tile = cluster size (> 8 needs the non-portable opt-in)
+constexpr int kAutoMaxSplits = 8;          // the automatic plan stays within portable cluster sizes
+constexpr uint32_t kBRowsBytes = kTileN * kAtomK / 2;    // 16 KB of e2m1 per weight tile per atom
 constexpr uint32_t kSfChunk = 512;         // 128 rows x 4 scale bytes
 constexpr size_t kSmemLimit = 227 * 1024;
-// Split-K arrival counters live in a fixed region at the start of every workspace and are
-// used for nothing else, so whatever plan ran before, a completed call leaves them all at 0.
-constexpr int kMaxCounters = 16384;
-constexpr size_t kCounterBytes = kMaxCounters * sizeof(uint32_t);
 
-// Two-level tiling of one mxfp4_gemm call.
+// Operand blocks. Each (tile, 256-K atom) of an operand is stored in global memory as the exact
+// shared-memory image the MMA reads, so one contiguous bulk copy fills a pipeline stage:
+//   rows:   row r of the tile at byte r*128; its eight 16-byte chunks (chunk c = 32 e2m1 values =
+//           one 1x32 block) at (c ^ (r % 8)) * 16 -- the 128-byte swizzle the MMA descriptor
+//           names (the 1 KB-aligned base keeps the pattern aligned);
+//   scales: after the rows, for every 128 rows two 512-byte chunks (4-block groups 2j and 2j+1 of
+//           atom j); in a chunk, row r sits at (r%32)*16 + ((r/32)%4)*4 + (block%4), the layout
+//           tcgen05.cp 32x128b.warpx4 spreads over tensor memory.
+// Weight block (128 rows): 16384 + 1024 = 17408 bytes. Token block of m rows:
+// m*128 + ceil(m/128)*1024 bytes.
+constexpr uint32_t kWBlock = kBRowsBytes + 2 * kSfChunk;
+
+__host__ __device__ inline uint32_t swz_chunk_offset(uint32_t r, uint32_t c) {
+    return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+__host__ __device__ inline uint32_t block_sf_offset(uint32_t r, uint32_t kb_in_atom) {
+    return ((r >> 7) * 2u + (kb_in_atom >> 2)) * kSfChunk + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u +
+           (kb_in_atom & 3u);
+}
+
+// Tiling of one mxfp4_gemm call.
 struct GemmPlan {
-    int path;          // 1: A quantized by the GEMM's producer warps; 2: standalone quantize first
-    int splits;        // K slices per output tile
+    int path;          // 1: A quantized by the GEMM's own warps; 2: standalone quantize first
+    int splits;        // K slices per output tile (= thread-block cluster size)
     int m_tile;        // tokens per tile = MMA N (multiple of 16, <= 256)
     int nmc;           // 128-row scale chunks per token tile
     int m_tiles, n_tiles;
     int k_atoms;       // ceil(K / 256)
-    int groups;        // scale-factor 4-block groups per row, padded to 2 per atom
     int atoms_max;     // most atoms any split gets
     int stages;
     int ctas;
-    uint32_t off_a, off_sfb, off_sfa, off_bar;  // shared-memory layout (bytes from a 1 KB base)
+    uint32_t a_block;  // bytes of one token block
+    uint32_t off_a, off_bar;   // shared-memory layout (bytes from a 1 KB-aligned base)
     size_t smem_bytes;
     uint32_t tmem_cols;
-    // workspace layout (bytes)
-    size_t ws_aq, ws_sfa, ws_part, ws_ctr, ws_total;
+    size_t ws_total;   // workspace: the two-kernel path's token blocks [m_tiles][k_atoms][a_block]
 };
 
 struct GemmArgs {
-    const uint16_t* a;    // bf16 A (fused path)
+    const uint16_t* a;     // bf16 A (fused path)
     int64_t lda;
-    const uint8_t* sfa;   // A scale chunks (two-kernel path)
-    const uint8_t* sfb;   // B scale chunks (packed B)
+    const uint8_t* ablk;   // token blocks (two-kernel path)
+    const uint8_t* bblk;   // weight blocks (packed B)
     uint16_t* c;
     int64_t ldc;
-    float* part;          // split-K partial tiles
-    uint32_t* ctr;        // split-K arrival counters, one per output tile
-    uint32_t* status;     // device error word
+    uint32_t* status;      // device error word
     int M, N, K;
-    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, groups, stages;
-    uint32_t off_a, off_sfb, off_sfa, off_bar;
+    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages;
+    uint32_t a_block, off_a, off_bar;
     uint32_t tmem_cols;
     int fused;
+    int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)
     uint64_t wait_limit_ns;
 };
 
@@ -63,23 +79,27 @@ struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
     size_t smem_optin;
-    uint32_t* status;     // address of the device error word on this device
+    uint32_t* status;      // address of the device error word on this device
 };
 
-int device_info(DeviceInfo* out);                 // MXFP4_OK or an error status
-size_t packed_sf_offset(int64_t N, int64_t K);
+int device_info(DeviceInfo* out);   // MXFP4_OK or an error status
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int sm_count, GemmPlan* plan);
+size_t packed_b_bytes(int64_t N, int64_t K);
 
 // Kernel launchers (return cudaError_t).
-// chunk_rows > 0: scales go to the tensor-core chunk layout covering chunk_rows rows (a
-// multiple of 128) and `groups` 4-block groups, padding zeroed; 0: natural [rows, K/32].
+// Natural layout: q [rows, K/2], scales [rows, K/32].
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q,
-                            uint8_t* scales, int64_t chunk_rows, int groups, cudaStream_t s);
-cudaError_t launch_prepack_sf(const uint8_t* bs, int64_t N, int64_t K, uint8_t* sf_out, int groups,
-                              cudaStream_t s);
-cudaError_t launch_gemm(const GemmPlan& plan, const CUtensorMap& tmap_b, const CUtensorMap& tmap_a,
-                        const GemmArgs& args, cudaStream_t s);
+                            uint8_t* scales, cudaStream_t s);
+// Token blocks for the GEMM, [m_tiles][k_atoms][a_block]; rows past `rows` and K past `K` zeroed.
+cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* blocks,
+                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s);
+// Pre-quantized B (natural layout) -> weight blocks [n_tiles][k_atoms][kWBlock].
+cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out,
+                           cudaStream_t s);
+cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t s);
 cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
+// Clusters of `cluster_size` GEMM CTAs with this much shared memory resident at once (0 if unknown).
+int max_active_clusters(int cluster_size, size_t smem_bytes);
 
 // Launch with programmatic stream serialization so a dependent kernel can start early.
 template <typename Kernel, typename... Args>

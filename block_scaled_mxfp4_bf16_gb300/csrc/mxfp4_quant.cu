@@ -1,69 +1,98 @@
-// Standalone MXFP4 quantizer and the B scale-factor prepack.
-//
-// quantize_kernel: one thread per (row, group of four 1x32 blocks) = 128 bf16 in, 64 bytes of
-// packed e2m1 + 4 scale bytes out, all with 16-byte vector accesses. The scales go either to
-// the natural [rows, K/32] layout (public mxfp4_quantize) or straight into the 512-byte
-// tensor-core chunks the GEMM copies into tensor memory (two-kernel GEMM path), padding
-// included, so the GEMM never reads an unwritten scale byte.
+// Standalone MXFP4 quantizer (natural layout and the GEMM's token blocks) and the weight
+// prepack. One thread per 1x32 block: 64 bytes of bf16 in (four 16-byte loads in flight),
+// 16 bytes of packed e2m1 and one e8m0 byte out.
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_device.cuh"
 
 namespace mxfp4 {
 
-template <bool kChunkLayout>
+// Natural layout: q [rows, K/2], scales [rows, K/32].
 __global__ void __launch_bounds__(256)
 quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
-                uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
-                int64_t rows_cover, int groups_cover) {
+                uint8_t* __restrict__ q, uint8_t* __restrict__ scales) {
     pdl_launch_dependents();
     pdl_wait_prior_grid();   // x may come from the previous kernel; q/scales may still be read by it
     const int64_t nblk = K / 32;
-    const int64_t items = rows_cover * groups_cover;
+    const int64_t items = rows * nblk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
-        const int64_t r = it / groups_cover;
-        const int g = static_cast<int>(it - r * groups_cover);
-        uint32_t sc = 0u;
-        if (r < rows) {
-            const uint16_t* xrow = x + r * ld;
-            uint8_t* qrow = q + r * (K / 2);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int64_t kb = 4 * static_cast<int64_t>(g) + b;
-                if (kb < nblk) {
-                    uint32_t w[16], out[4];
-                    load_block32(xrow + kb * 32, w);
-                    const uint32_t byte = quantize_block32(w, out);
-                    *reinterpret_cast<uint4*>(qrow + kb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
-                    sc |= byte << (8 * b);
-                    if (!kChunkLayout) scales[r * nblk + kb] = static_cast<uint8_t>(byte);
-                }
-            }
-        }
-        if (kChunkLayout)
-            *reinterpret_cast<uint32_t*>(scales + sf_chunk_offset(static_cast<uint32_t>(r), 4u * g, groups_cover)) = sc;
+        const int64_t r = it / nblk;
+        const int64_t kb = it - r * nblk;
+        uint32_t w[16], out[4];
+        load_block32(x + r * ld + kb * 32, w);
+        const uint32_t byte = quantize_block32(w, out);
+        *reinterpret_cast<uint4*>(q + r * (K / 2) + kb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+        scales[it] = static_cast<uint8_t>(byte);
     }
 }
 
-// Scale bytes of a pre-quantized B [N, K/32] -> tensor-core chunks, zero padded to whole
-// 128-row tiles and to `groups` 4-block groups per row.
+// Token blocks (layout in internal.h): block (mt, j) at (mt * k_atoms + j) * a_block. Items run
+// over every (row, block) of the padded [m_tiles*m_tile, k_atoms*256] matrix, so padding rows and
+// the K tail are written as zeros. Four consecutive lanes own the four blocks of one scale word.
 __global__ void __launch_bounds__(256)
-prepack_sf_kernel(const uint8_t* __restrict__ bs, int64_t N, int64_t K, uint8_t* __restrict__ out, int groups) {
+quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
+                       uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
+    pdl_launch_dependents();
+    pdl_wait_prior_grid();
     const int64_t nblk = K / 32;
-    const int64_t rows_cover = (N + 127) / 128 * 128;
-    const int64_t items = rows_cover * groups;
+    const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
+    const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    // the loop bound is uniform per warp (warps start at multiples of 32) so the shuffles below
+    // always see all 32 lanes
+    for (int64_t wbase = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); wbase < items;
+         wbase += stride) {
+        const int64_t it = wbase + lane;
+        const bool in_range = it < items;
+        const int64_t r = in_range ? it / row_items : 0;
+        const int64_t kbp = in_range ? it - r * row_items : 0;     // block index within the padded row
+        const bool live = in_range && r < rows && kbp < nblk;
+        uint32_t w[16], out[4] = {0u, 0u, 0u, 0u}, byte = 0u;
+        if (live) {
+            load_block32(x + r * ld + kbp * 32, w);
+            byte = quantize_block32(w, out);
+        }
+        uint32_t word = byte << (8 * (lane & 3));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (in_range) {
+            const int mt = static_cast<int>(r / m_tile);
+            const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
+            const uint32_t c = static_cast<uint32_t>(kbp & 7);
+            uint8_t* blk = blocks + (static_cast<size_t>(mt) * k_atoms + static_cast<size_t>(kbp >> 3)) * a_block;
+            *reinterpret_cast<uint4*>(blk + swz_chunk_offset(rr, c)) = make_uint4(out[0], out[1], out[2], out[3]);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<uint32_t*>(blk + static_cast<uint32_t>(m_tile) * 128u + block_sf_offset(rr, c)) = word;
+        }
+    }
+}
+
+// Weight prepack: one thread per (row, block) of the padded [n_tiles*128, k_atoms*256] matrix;
+// copies 16 bytes of e2m1 into the swizzled rows and the scale byte into its chunk.
+__global__ void __launch_bounds__(256)
+prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, int64_t N, int64_t K,
+               uint8_t* __restrict__ out, int k_atoms) {
+    const int64_t nblk = K / 32;
+    const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
+    const int64_t rows_cover = (N + kTileN - 1) / kTileN * kTileN;
+    const int64_t items = rows_cover * row_items;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
-        const int64_t r = it / groups;
-        const int g = static_cast<int>(it - r * groups);
-        uint32_t v = 0u;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int64_t kb = 4 * static_cast<int64_t>(g) + b;
-            if (r < N && kb < nblk) v |= static_cast<uint32_t>(bs[r * nblk + kb]) << (8 * b);
+        const int64_t r = it / row_items;
+        const int64_t kbp = it - r * row_items;
+        const uint32_t rr = static_cast<uint32_t>(r % kTileN);
+        const uint32_t c = static_cast<uint32_t>(kbp & 7);
+        uint8_t* blk = out + (static_cast<size_t>(r / kTileN) * k_atoms + static_cast<size_t>(kbp >> 3)) * kWBlock;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t sc = 0;
+        if (r < N && kbp < nblk) {
+            v = __ldg(reinterpret_cast<const uint4*>(bq + r * (K / 2) + kbp * 16));
+            sc = bs[r * nblk + kbp];
         }
-        *reinterpret_cast<uint32_t*>(out + sf_chunk_offset(static_cast<uint32_t>(r), 4u * g, groups)) = v;
+        *reinterpret_cast<uint4*>(blk + swz_chunk_offset(rr, c)) = v;
+        blk[kBRowsBytes + block_sf_offset(rr, c)] = sc;
     }
 }
 
@@ -74,23 +103,26 @@ static int grid_for(int64_t items, int threads) {
     return static_cast<int>(blocks);
 }
 
-cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q,
-                            uint8_t* scales, int64_t chunk_rows, int groups, cudaStream_t s) {
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q, uint8_t* scales,
+                            cudaStream_t s) {
     const int threads = 256;
-    if (chunk_rows > 0) {
-        const int64_t rows_cover = chunk_rows;
-        return launch_pdl(quantize_kernel<true>, dim3(grid_for(rows_cover * groups, threads)), dim3(threads), 0, s,
-                          x, rows, K, ld, q, scales, rows_cover, groups);
-    }
-    const int gc = static_cast<int>((K / 32 + 3) / 4);
-    return launch_pdl(quantize_kernel<false>, dim3(grid_for(rows * gc, threads)), dim3(threads), 0, s,
-                      x, rows, K, ld, q, scales, rows, gc);
+    return launch_pdl(quantize_kernel, dim3(grid_for(rows * (K / 32), threads)), dim3(threads), 0, s, x, rows, K,
+                      ld, q, scales);
 }
 
-cudaError_t launch_prepack_sf(const uint8_t* bs, int64_t N, int64_t K, uint8_t* sf_out, int groups, cudaStream_t s) {
+cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* blocks,
+                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s) {
     const int threads = 256;
-    const int64_t rows_cover = (N + 127) / 128 * 128;
-    prepack_sf_kernel<<<grid_for(rows_cover * groups, threads), threads, 0, s>>>(bs, N, K, sf_out, groups);
+    const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * 8 * k_atoms;
+    return launch_pdl(quantize_blocks_kernel, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K, ld,
+                      blocks, m_tile, m_tiles, k_atoms, a_block);
+}
+
+cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out, cudaStream_t s) {
+    const int threads = 256;
+    const int k_atoms = static_cast<int>((K + kAtomK - 1) / kAtomK);
+    const int64_t rows_cover = (N + kTileN - 1) / kTileN * kTileN;
+    prepack_kernel<<<grid_for(rows_cover * 8 * k_atoms, threads), threads, 0, s>>>(bq, bs, N, K, out, k_atoms);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA (cp.async.bulk), tcgen05
-// (tensor-memory allocation, block-scaled MMA, scale-factor copies, loads), PDL control.
+// Inline-PTX building blocks for sm_103a: mbarriers, bulk copies (cp.async.bulk), tcgen05
+// (tensor-memory allocation, block-scaled MMA, scale-factor copies, loads), PDL control,
+// thread-block clusters and distributed shared memory.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -74,18 +75,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-// 2-D tiled tensor load global -> shared, completion counted on `bar` in bytes.
-// x is the innermost (contiguous) coordinate in elements; x * elemsize must be a multiple
-// of 16 bytes (callers pass multiples of 128 bytes).
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(smem_addr(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
 // Contiguous bulk copy global -> shared (16-byte aligned addresses, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
@@ -94,10 +83,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         " [%0], [%1], %2, [%3], %4;"
         ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA, tcgen05).
@@ -186,9 +171,36 @@ __device__ __forceinline__ void tmem_load_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Named barrier over `count` threads (multiple of 32).
+// Named barrier over `count` threads (multiple of 32): wait, or only arrive.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------------------------------ clusters
+
+// Full cluster barrier (all threads of all CTAs of the cluster) with release/acquire ordering
+// of shared-memory accesses across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_address), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ bool elect_one() {

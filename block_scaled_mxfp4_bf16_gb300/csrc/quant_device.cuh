@@ -92,11 +92,4 @@ __device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[
     }
 }
 
-// Byte offset of (row r, 32-block kb) inside the tensor-core scale-factor layout:
-// 512-byte chunks of 128 rows x 4 blocks, chunk index (r / 128) * groups + kb / 4; within a
-// chunk, row r % 32 owns 16 bytes holding rows r%32, +32, +64, +96 (4 blocks each).
-__device__ __forceinline__ uint32_t sf_chunk_offset(uint32_t r, uint32_t kb, uint32_t groups) {
-    return ((r >> 7) * groups + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (kb & 3u);
-}
-
 }  // namespace mxfp4

@@ -75,18 +75,20 @@ int mxfp4_quantize(const void *x, int64_t rows, int64_t K, int64_t ld,
 
 /*
  * mxfp4_prepack_b_size -- bytes of the packed-B buffer mxfp4_prepack_b writes for an
- * [N, K] weight matrix: the e2m1 bytes (N*K/2, natural layout) followed, at the next
- * 1024-byte boundary, by the scale factors rearranged into the tensor-core layout
- * (ceil(N/128) tiles x ceil(K/256)*2 groups x 512 bytes). 0 for invalid sizes.
+ * [N, K] weight matrix: ceil(N/128) x ceil(K/256) blocks of 17408 bytes, one per 128-row
+ * tile and 256-element K step, each holding that piece's e2m1 rows (16 KB, swizzled the
+ * way the tensor cores read shared memory) and its e8m0 scales (1 KB, in the tensor-memory
+ * scale-factor layout). Rows past N and K past the last multiple of 256 are zero padding.
+ * 0 for invalid sizes.
  */
 size_t mxfp4_prepack_b_size(int64_t N, int64_t K);
 
 /*
  * mxfp4_prepack_b -- one-time relayout of a pre-quantized weight matrix B for mxfp4_gemm.
  * The pages prepare B outside the timed call too (their harness shuffles B and its scales
- * for the MFMA layout, submission 608632 `_new_generate_input`); here the e2m1 bytes keep
- * their layout and the e8m0 scales move into the 128-row x 4-block chunks the tcgen05
- * block-scaled MMA reads from tensor memory.
+ * for the MFMA layout, submission 608632 `_new_generate_input`); here every (128-row tile,
+ * 256-K step) becomes one contiguous block that is the exact shared-memory image the tcgen05
+ * block-scaled MMA reads, so the GEMM streams the weights with one bulk copy per step.
  *   bq     : uint8 [N, K/2] packed e2m1 (even element low nibble). 16-byte aligned.
  *   bs     : uint8 [N, K/32] e8m0 scales (as written by mxfp4_quantize).
  *   K      : positive multiple of 64.  N >= 1.
@@ -98,17 +100,15 @@ int mxfp4_prepack_b(const void *bq, const void *bs, int64_t N, int64_t K,
 
 /*
  * mxfp4_gemm_workspace_size -- bytes of device workspace mxfp4_gemm needs for this shape
- * on the CURRENT device (the split-K plan depends on its SM count). The workspace holds
- * the quantized A for the two-kernel path, fp32 split-K partial tiles and one arrival
- * counter per output tile.
+ * on the CURRENT device (the plan depends on its SM count). The workspace holds the
+ * quantized A (as token blocks) of the two-kernel path used for M > 32; the fused path
+ * needs none and returns 0. Split-K partial sums never leave the chip.
  */
 size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * mxfp4_workspace_init -- zero a workspace before its first use (cudaMemsetAsync on
- * `stream`). The split-K arrival counters must start at zero; every completed mxfp4_gemm
- * leaves them at zero again, so this is needed once per buffer (and again after a call
- * whose device status reported an error).
+ * mxfp4_workspace_init -- zero-fill a workspace (cudaMemsetAsync on `stream`). Optional:
+ * the GEMM never depends on the workspace's previous contents.
  */
 int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
@@ -119,12 +119,14 @@ int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  *   a        : bf16 [M, K], row stride lda elements (lda >= K, lda % 8 == 0), 16-byte aligned.
  *   packed_b : buffer written by mxfp4_prepack_b for the same N and K.
  *   c        : out, bf16 [M, N], row stride ldc elements (ldc >= N), 2-byte aligned.
- *   workspace: ws_bytes >= mxfp4_gemm_workspace_size(M, N, K), 256-byte aligned, zeroed
- *              once by mxfp4_workspace_init. Calls sharing a workspace must be ordered
- *              (same stream, or synchronized); overlapping calls on one workspace race.
+ *   workspace: ws_bytes >= mxfp4_gemm_workspace_size(M, N, K), 256-byte aligned; may be
+ *              NULL when that size is 0. Calls sharing a workspace must be ordered (same
+ *              stream, or synchronized); overlapping calls on one workspace race.
  *   K        : positive multiple of 64.  M == 0 or N == 0 is a no-op.
  * A is quantized exactly like mxfp4_quantize (bit-identical codes and scales). With split-K
- * the fp32 partial sums are added in a fixed order, so results are run-to-run identical.
+ * the K slices of an output tile run as one thread-block cluster and their fp32 partial
+ * sums are added in slice order through distributed shared memory, so results are
+ * run-to-run identical.
  */
 int mxfp4_gemm(const void *a, int64_t M, int64_t K, int64_t lda,
                const void *packed_b, int64_t N,
@@ -177,23 +179,22 @@ int mxfp4_selftest_timeout(int limit_us, void *stream);
  * inference engine whose host owns the whole device-memory plan and forbids allocation once
  * it runs, or a latency-critical serving loop that must never call cudaMalloc/cudaFree
  * because those can synchronize the whole device. This entry point needs no workspace
- * argument: its scratch (split-K partial tiles, split-K arrival counters and the quantized A
- * of the two-kernel path) lives in one statically sized array inside the library, which
- * every GPU that loads the library keeps for the life of the process.
+ * argument: its scratch (the quantized A that the two-kernel path, M > 32, hands from its
+ * quantize kernel to the GEMM kernel) lives in one statically sized array inside the
+ * library, which every GPU that loads the library keeps for the life of the process.
  *
- *   Arguments and results are those of mxfp4_gemm without `workspace` / `ws_bytes`; the
- *   output equals mxfp4_gemm's within the library's tolerance (the split-K slice count may be
- *   lowered to fit the array, which can change the fp32 summation order).
- *   Scratch limit: MXFP4_NOALLOC_SCRATCH_BYTES. A shape whose scratch cannot fit even
- *   without split-K (the quantized A of the two-kernel path, M*K/2 bytes plus its scales and
- *   64 KB of counters) returns MXFP4_ERR_WORKSPACE before anything is enqueued.
+ *   Arguments and results are those of mxfp4_gemm without `workspace` / `ws_bytes`; it runs
+ *   the same plan, so the output is the same.
+ *   Scratch limit: MXFP4_NOALLOC_SCRATCH_BYTES. A shape whose scratch does not fit (about
+ *   M*K/2 bytes plus M*K/32 of scales, rounded up to whole tiles) returns
+ *   MXFP4_ERR_WORKSPACE before anything is enqueued.
  *   No allocation: the call never calls cudaMalloc, cudaFree or any allocating routine.
  *   First call per device: it looks up the array's device address (cudaGetSymbolAddress)
  *   with that device current; make that first call before any stream capture.
  *   Sharing: all calls on a device share the one array and it keeps the previous call's
- *   contents. Each call clears the counters it uses (cudaMemsetAsync on `stream`) before its
- *   kernels. Calls that can overlap on the GPU (different streams without ordering, or
- *   several host threads) race on the array and give wrong results: order them.
+ *   contents; nothing in it has to start at zero (each call rewrites every byte it reads).
+ *   Calls that can overlap on the GPU (different streams without ordering, or several host
+ *   threads) race on the array and give wrong results: order them.
  */
 #define MXFP4_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int mxfp4_gemm_noalloc(const void *a, int64_t M, int64_t K, int64_t lda,

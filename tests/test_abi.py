@@ -44,9 +44,10 @@ def test_status_strings_and_version(lib):
 def test_prepack_size_is_pure_host_arithmetic(lib):
     lib.mxfp4_prepack_b_size.restype = ctypes.c_size_t
     lib.mxfp4_prepack_b_size.argtypes = [ctypes.c_int64, ctypes.c_int64]
-    # e2m1 bytes, then 1 KB aligned: ceil(N/128) tiles x 2*ceil(K/256) groups x 512 bytes
-    assert lib.mxfp4_prepack_b_size(2112, 7168) == 2112 * 3584 + 17 * 56 * 512
-    assert lib.mxfp4_prepack_b_size(100, 64) == 4096 + 1 * 2 * 512
+    # one 17408-byte block (16 KB of swizzled e2m1 rows + 1 KB of scales) per 128-row tile
+    # and 256-element K step
+    assert lib.mxfp4_prepack_b_size(2112, 7168) == 17 * 28 * 17408
+    assert lib.mxfp4_prepack_b_size(100, 64) == 1 * 1 * 17408
     assert lib.mxfp4_prepack_b_size(100, 96) == 0     # K must be a multiple of 64
     assert lib.mxfp4_prepack_b_size(0, 64) == 0
 
