@@ -8,7 +8,9 @@
 namespace mxfp4 {
 
 constexpr int kMaxStages = 8;
-constexpr int kGemmThreads = 192;          // warp 0 copies, warp 1 MMA, warps 2..5 quant + epilogue
+constexpr int kEpiWarps = 8;               // warps 2..9: A quantization (fused path) and the epilogue
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kGemmThreads = 64 + kEpiThreads;   // warp 0 copies, warp 1 MMA
 constexpr int kTileN = 128;                // weight rows per MMA (the MMA's M)
 constexpr int kAtomK = 256;                // K elements per pipeline step (128-byte rows)
 constexpr int kMaxMTile = 256;             // tokens per tile (the MMA's N)
@@ -50,7 +52,11 @@ struct GemmPlan {
     int stages;
     int ctas;
     uint32_t a_block;  // bytes of one token block
-    uint32_t off_a, off_bar;   // shared-memory layout (bytes from a 1 KB-aligned base)
+    // shared-memory layout (bytes from a 1 KB-aligned base): weight stages at 0, token blocks
+    // at off_a, the fused path's bf16 A slice at off_araw, the reduction's receive buffer at
+    // off_recv (over the pipeline buffers unless recv_dedicated), barriers at off_bar
+    uint32_t off_a, off_araw, off_recv, off_bar;
+    int recv_dedicated;
     size_t smem_bytes;
     uint32_t tmem_cols;
     size_t ws_total;   // workspace: the two-kernel path's token blocks [m_tiles][k_atoms][a_block]
@@ -65,8 +71,9 @@ struct GemmArgs {
     int64_t ldc;
     uint32_t* status;      // device error word
     int M, N, K;
-    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages;
-    uint32_t a_block, off_a, off_bar;
+    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages, atoms_max;
+    uint32_t a_block, off_a, off_araw, off_recv, off_bar;
+    int recv_dedicated;
     uint32_t tmem_cols;
     int fused;
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)

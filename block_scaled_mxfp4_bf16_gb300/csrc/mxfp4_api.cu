@@ -71,20 +71,33 @@ static int plan_layout(GemmPlan& p) {
     p.atoms_max = static_cast<int>(cdiv(p.k_atoms, p.splits));
     const size_t bar_bytes = 256;
     const size_t budget = kSmemLimit - 1024 - bar_bytes;
-    size_t fixed = 0, per_stage = kWBlock;
-    if (p.path == 1) fixed = static_cast<size_t>(p.atoms_max) * p.a_block;   // every atom's tokens resident
+    // fused: every atom's token block and the whole bf16 A slice stay resident
+    const size_t raw_bytes = p.path == 1 ? static_cast<size_t>(p.m_tile) * p.atoms_max * kAtomK * 2 : 0;
+    size_t fixed = raw_bytes, per_stage = kWBlock;
+    if (p.path == 1) fixed += static_cast<size_t>(p.atoms_max) * p.a_block;
     else per_stage += p.a_block;
     if (fixed + per_stage > budget) return MXFP4_ERR_SHAPE;
     p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(kMaxStages), static_cast<size_t>(p.atoms_max),
                                                   (budget - fixed) / per_stage}));
     p.off_a = static_cast<uint32_t>(p.stages) * kWBlock;
     const int a_slots = p.path == 1 ? p.atoms_max : p.stages;
-    p.off_bar = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
-    // the fp32 output tile is staged over the (then idle) pipeline buffers; at least ~half the
-    // shared memory is taken so one CTA runs per SM and tensor memory is never contended
-    const size_t floor_bytes = std::max<size_t>(static_cast<size_t>(p.m_tile) * kTileN * sizeof(float),
-                                                120 * 1024 - bar_bytes - 1024);
-    if (p.off_bar < floor_bytes) p.off_bar = static_cast<uint32_t>(align_up(floor_bytes, 1024));
+    p.off_araw = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
+    size_t end = align_up(p.off_araw + raw_bytes, 1024);
+    // reduction receive buffer: [source rank][rows owned][128] fp32
+    const size_t rows_per = static_cast<size_t>(cdiv(p.m_tile, p.splits));
+    const size_t recv_bytes = static_cast<size_t>(p.splits) * rows_per * kTileN * sizeof(float);
+    if (p.splits > 1 && end + recv_bytes <= budget) {
+        p.recv_dedicated = 1;
+        p.off_recv = static_cast<uint32_t>(end);
+        end = align_up(end + recv_bytes, 1024);
+    } else {
+        p.recv_dedicated = 0;       // over the pipeline buffers, written once every MMA is done
+        p.off_recv = 0;
+        end = std::max(end, align_up(recv_bytes, 1024));
+    }
+    // at least ~half the shared memory, so one CTA runs per SM and tensor memory is never contended
+    end = std::max(end, align_up(120 * 1024 - bar_bytes - 1024, 1024));
+    p.off_bar = static_cast<uint32_t>(end);
     p.smem_bytes = p.off_bar + bar_bytes + 1024;
     if (p.smem_bytes > kSmemLimit) return MXFP4_ERR_SHAPE;
     const uint32_t cols = static_cast<uint32_t>(p.m_tile) + static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc);
@@ -199,8 +212,12 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     g.splits = plan.splits;
     g.k_atoms = plan.k_atoms;
     g.stages = plan.stages;
+    g.atoms_max = plan.atoms_max;
     g.a_block = plan.a_block;
     g.off_a = plan.off_a;
+    g.off_araw = plan.off_araw;
+    g.off_recv = plan.off_recv;
+    g.recv_dedicated = plan.recv_dedicated;
     g.off_bar = plan.off_bar;
     g.tmem_cols = plan.tmem_cols;
     g.fused = plan.path == 1 ? 1 : 0;

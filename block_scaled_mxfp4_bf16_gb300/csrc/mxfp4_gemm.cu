@@ -18,13 +18,13 @@
 //   warp 1    : tensor-memory allocation and the single MMA-issuing thread: per 256-K step it
 //               copies the scale factors into tensor memory (tcgen05.cp) and issues four
 //               128 x N x 64 block-scaled MMAs.
-//   warps 2-5 : in the fused path they first quantize the CTA's token slice from bf16 straight
-//               into the token-block layout in shared memory (the pages' in-register A
-//               quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`); then they move
-//               the accumulator to an fp32 tile in shared memory.
-// Reduction: after a cluster barrier each CTA of the cluster sums its share of the tile's rows
-// over all K slices through distributed shared memory, in slice order (run-to-run identical),
-// and stores bf16 C.
+//   warps 2-9 : in the fused path they quantize the CTA's bf16 token slice (staged in shared
+//               memory by one bulk copy per row) into the token-block layout (the pages'
+//               in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`);
+//               then they move the accumulator out of tensor memory.
+// Reduction: each output row has an owner CTA in the cluster; the K slices post their fp32 rows
+// into the owner's shared memory, and after a cluster barrier the owner sums them in slice
+// order (run-to-run identical) and stores bf16 C.
 // Every wait on an mbarrier is bounded; on timeout the kernel records an error in the device
 // status word and unwinds (outputs undefined, no hang, tensor memory released).
 #include <cuda_bf16.h>
@@ -47,31 +47,32 @@ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t n_mma) {
          | ((uint32_t(kTileN) >> 4) << 24); // M / 16
 }
 
-// OR of a predicate over the 128 threads of warps 2..5 (named barrier 2).
-__device__ __forceinline__ bool any_of_128(bool pred) {
+// OR of a predicate over the epilogue warps (named barrier 2).
+__device__ __forceinline__ bool any_of_epilogue(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred p, 2, 128, p;\n\t"
+        "bar.red.or.pred p, 2, %2, p;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
+        : "r"(static_cast<uint32_t>(pred)), "n"(kEpiThreads)
         : "memory");
     return r != 0;
 }
 
+// Two fp32 -> two bf16 (round to nearest even) in one word, `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
+
+__device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp == 2 && lane == 0; }
 
 __device__ __forceinline__ void fail(const GemmArgs& p, volatile uint32_t* abort_flag) {
     atomicOr(p.status, 1u);
     *abort_flag = 1u;
 }
-
-constexpr int kRedBatch = 8;   // output items a thread reduces at once (loads in flight per source)
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mxfp4_gemm_kernel(const GemmArgs p) {
@@ -79,25 +80,28 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* sB = smem;                           // stages x kWBlock
     uint8_t* sA = smem + p.off_a;                 // token blocks: stages (two-kernel) or atoms (fused)
+    const uint16_t* sAraw = reinterpret_cast<const uint16_t*>(smem + p.off_araw);   // fused: bf16 A slice
+    float* sRecv = reinterpret_cast<float*>(smem + p.off_recv);   // fp32 rows this CTA reduces / stages
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + kMaxStages;
     uint64_t* a_full = empty + kMaxStages;
     uint64_t* acc_full = a_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* a_raw = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_raw + 1);
     volatile uint32_t* flags = tmem_slot + 1;    // [0] abort
-    float* sC = reinterpret_cast<float*>(smem);   // fp32 output tile [token][row], over the idle pipeline
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     // ---- work unit: (token tile, weight tile, K slice)
-    const int split = blockIdx.x % p.splits;      // = rank in the cluster
-    const int tile = blockIdx.x / p.splits;
+    const int S = p.splits;
+    const int split = blockIdx.x % S;              // = rank in the cluster
+    const int tile = blockIdx.x / S;
     const int nt = tile % p.n_tiles;
     const int mt = tile / p.n_tiles;
     const int n0 = nt * kTileN;
     const int m0 = mt * p.m_tile;
-    const int base = p.k_atoms / p.splits, rem = p.k_atoms % p.splits;
+    const int base = p.k_atoms / S, rem = p.k_atoms % S;
     const int a0 = split * base + (split < rem ? split : rem);
     const int na = base + (split < rem ? 1 : 0);
     const int m_valid = (p.M - m0) < p.m_tile ? (p.M - m0) : p.m_tile;
@@ -105,19 +109,30 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const uint32_t a_block = p.a_block;
     const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
     const uint64_t lim = p.wait_limit_ns;
+    // rows of the output tile reduced (and stored) by CTA `rank` of the cluster
+    const int rows_per = (m_valid + S - 1) / S;   // >= 1
+    const int r0 = split * rows_per;
+    const int r1 = min(m_valid, r0 + rows_per);
+    // fused path: this CTA's bf16 A slice, rows of kslice elements
+    const int kslice = min(na * kAtomK, p.K - a0 * kAtomK);
+    const uint32_t raw_row = static_cast<uint32_t>(p.atoms_max) * kAtomK * 2u;   // bytes per staged row
 
+    if (threadIdx.x == 0) MXFP4_PHASE(0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(a_full, 128);
+        mbar_init(a_full, kEpiThreads);
         mbar_init(acc_full, 1);
+        mbar_init(a_raw, 1);
         flags[0] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
     pdl_launch_dependents();
+    uint32_t tmem_base = 0;
+    bool ok = true;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -132,10 +147,19 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
             }
-            pdl_wait_prior_grid();   // token blocks are written by the previous grid
-            if (!p.fused)
+            MXFP4_PHASE(1);
+            pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
+            if (p.fused) {
+                // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip
+                const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
+                mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
+                for (int r = 0; r < m_valid; ++r)
+                    bulk_load(smem + p.off_araw + r * raw_row,
+                              p.a + static_cast<int64_t>(m0 + r) * p.lda + a0 * kAtomK, row_bytes, a_raw, pol_a);
+            } else {
                 for (int j = 0; j < npro; ++j)
                     bulk_load(sA + j * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[j], pol_a);
+            }
             int issued = npro;
             for (int j = npro; j < na; ++j) {
                 const int s = j % stages;
@@ -149,6 +173,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             // never leave copies in flight into shared memory that is about to be reused or freed
             for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
+            if (p.fused) mbar_wait(a_raw, 0, lim);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------------- MMA issuer
@@ -158,21 +183,25 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
         tmem_relinquish();
         tc_fence_before_sync();
-        named_barrier_arrive(1, 160);             // publish the column base to warps 2..5
+        named_barrier_arrive(1, 32 + kEpiThreads);   // publish the column base to the epilogue warps
         __syncwarp();
         tc_fence_after_sync();
-        const uint32_t tmem_base = *tmem_slot;
+        tmem_base = *tmem_slot;
         if (lane == 0) {
             const uint32_t t_acc = tmem_base;
             const uint32_t t_sfb = tmem_base + static_cast<uint32_t>(p.m_tile);
             const uint32_t t_sfa = t_sfb + static_cast<uint32_t>(stages) * 8u;
             const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
-            bool ok = true;
-            if (p.fused) ok = mbar_wait(a_full, 0, lim);
+            bool mok = true;
+            MXFP4_PHASE(2);
+            if (p.fused) mok = mbar_wait(a_full, 0, lim);
+            MXFP4_PHASE(3);
             tc_fence_after_sync();
-            for (int j = 0; ok && j < na; ++j) {
+            for (int j = 0; mok && j < na; ++j) {
                 const int s = j % stages;
-                if (!mbar_wait(&full[s], (j / stages) & 1, lim)) { ok = false; break; }
+                if (!mbar_wait(&full[s], (j / stages) & 1, lim)) { mok = false; break; }
+                if (j == 0) MXFP4_PHASE(4);
+                if (j == na - 1) MXFP4_PHASE(5);
                 tc_fence_after_sync();
                 const uint8_t* bb = sB + s * kWBlock;
                 const uint8_t* ab = sA + (p.fused ? j : s) * a_block;
@@ -196,137 +225,166 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 }
                 tc_commit(&empty[s]);
             }
-            if (!ok) fail(p, flags);
+            if (!mok) fail(p, flags);
             tc_commit(acc_full);
         }
     } else {
-        // -------------------------------------------------------------------- warps 2..5
+        // -------------------------------------------------------------------- warps 2..9
         const int et = threadIdx.x - 64;
-        pdl_wait_prior_grid();   // A may come from the previous grid; C may still be read by it
         if (p.fused) {
-            // Quantize this CTA's token rows of its K slice into token blocks in shared memory,
-            // one 1x32 block per item; two items' loads are issued before either is converted.
+            // Quantize the staged bf16 slice into token blocks in shared memory, one 1x32 block
+            // per item; rows past M and K past the end become zeros.
+            const bool got = mbar_wait(a_raw, 0, lim);
+            if (et == 0) MXFP4_PHASE(10);
+            if (!got) fail(p, flags);
             const int nblk = na * (kAtomK / 32);
-            const int total = p.m_tile * nblk;   // rows past M are written as zeros
-            for (int first = et; first < total; first += 256) {
-                uint32_t w[2][16];
-                int rr[2], kk[2];
-                bool live[2], inside[2];
+            const int total = p.m_tile * nblk;
+            for (int idx = et; idx < total; idx += kEpiThreads) {
+                const int r = idx / nblk;
+                const int kb = idx - r * nblk;
+                uint32_t out[4] = {0u, 0u, 0u, 0u}, sbyte = 0u;
+                if (got && r < m_valid && kb * 32 < kslice) {
+                    uint32_t w[16];
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint8_t*>(sAraw) + r * raw_row + kb * 64);
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int idx = first + 128 * u;
-                    live[u] = idx < total;
-                    rr[u] = live[u] ? idx / nblk : 0;
-                    kk[u] = live[u] ? idx - rr[u] * nblk : 0;
-                    const int gk = (a0 + (kk[u] >> 3)) * kAtomK + (kk[u] & 7) * 32;
-                    inside[u] = live[u] && rr[u] < m_valid && gk < p.K;
-                    if (inside[u]) load_block32(p.a + static_cast<int64_t>(m0 + rr[u]) * p.lda + gk, w[u]);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = src[i];
+                        w[4 * i + 0] = v.x;
+                        w[4 * i + 1] = v.y;
+                        w[4 * i + 2] = v.z;
+                        w[4 * i + 3] = v.w;
+                    }
+                    sbyte = quantize_block32(w, out);
                 }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (!live[u]) continue;
-                    uint32_t out[4] = {0u, 0u, 0u, 0u};
-                    const uint32_t sbyte = inside[u] ? quantize_block32(w[u], out) : 0u;
-                    const uint32_t r = static_cast<uint32_t>(rr[u]), c = static_cast<uint32_t>(kk[u] & 7);
-                    uint8_t* blk = sA + (kk[u] >> 3) * a_block;
-                    *reinterpret_cast<uint4*>(blk + swz_chunk_offset(r, c)) = make_uint4(out[0], out[1], out[2], out[3]);
-                    blk[a_rows + block_sf_offset(r, c)] = static_cast<uint8_t>(sbyte);
-                }
+                const uint32_t c = static_cast<uint32_t>(kb & 7);
+                uint8_t* blk = sA + (kb >> 3) * a_block;
+                *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(r), c)) =
+                    make_uint4(out[0], out[1], out[2], out[3]);
+                blk[a_rows + block_sf_offset(static_cast<uint32_t>(r), c)] = static_cast<uint8_t>(sbyte);
             }
             fence_proxy_async_smem();
             mbar_arrive(a_full);
         }
         const bool waited = mbar_wait(acc_full, 0, lim);
-        named_barrier(1, 160);                    // the column base from warp 1
+        if (et == 0) MXFP4_PHASE(6);
+        named_barrier(1, 32 + kEpiThreads);       // the column base from warp 1
         tc_fence_after_sync();
+        tmem_base = *tmem_slot;
         if (!waited) fail(p, flags);
-        // one decision for all 128 threads (tcgen05.ld is warp-collective)
-        const bool ok = !any_of_128(!waited || flags[0] != 0u);
-        if (ok) {
-            // accumulator D = C^T (lane = weight row, column = token) -> fp32 tile [token][row]
-            const int q = warp & 3;               // this warp's 32-lane slice of tensor memory
-            const int nl = q * 32 + lane;
-            const uint32_t trow = *tmem_slot + (static_cast<uint32_t>(q * 32) << 16);
-            for (int cb = 0; cb < m_valid; cb += 32) {
+        // one decision for all epilogue threads (tcgen05.ld is warp-collective)
+        ok = !any_of_epilogue(!waited || flags[0] != 0u);
+    }
+
+    // ------------------------------------------------------------------------ output
+    // Accumulator D = C^T: tensor-memory lane = weight row n, column = token m. Epilogue warp w
+    // reads the lanes of quadrant w % 4 and every other 32-column chunk (two warps per quadrant).
+    const int half = ((warp - 2) >> 2) & 1;
+    const int nl = (warp & 3) * 32 + lane;
+    const int n = n0 + nl;
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    __syncwarp();
+    if (S == 1) {
+        // one K slice: tensor memory -> bf16 C directly, one output column per thread
+        if (warp >= 2 && ok) {
+            for (int cb = half * 32; cb < m_valid; cb += 64) {
                 uint32_t r[32];
                 tmem_load_16(trow + cb, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
                 if (cb + 16 < m_valid) tmem_load_16(trow + cb + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
                 tmem_load_wait();
+                if (n < p.N) {
+                    uint16_t* cp = p.c + static_cast<int64_t>(m0 + cb) * p.ldc + n;
+                    const int cnt = min(32, m_valid - cb);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (cb + i < m_valid) sC[(cb + i) * kTileN + nl] = __uint_as_float(r[i]);
-            }
-        }
-    }
-
-    // ------------------------------------------------------------------------ tile reduction
-    __syncwarp();
-    tc_fence_before_sync();
-    if (p.splits > 1) cluster_sync();
-    else __syncthreads();
-    if (warp >= 2) {
-        const int et = threadIdx.x - 64;
-        const int S = p.splits;
-        const int rows_per = (m_valid + S - 1) / S;
-        const int r0 = split * rows_per;
-        const int r1 = min(m_valid, r0 + rows_per);
-        const int items = r1 > r0 ? (r1 - r0) * (kTileN / 4) : 0;   // 4 output columns per item
-        const uint32_t sC_addr = smem_addr(sC);
-        for (int first = et; first < items; first += 128 * kRedBatch) {
-            float4 acc[kRedBatch];
-            uint32_t off[kRedBatch];
-#pragma unroll
-            for (int u = 0; u < kRedBatch; ++u) {
-                const int i = first + 128 * u;
-                const int m = r0 + i / (kTileN / 4);
-                off[u] = static_cast<uint32_t>(m * kTileN + (i % (kTileN / 4)) * 4) * 4u;
-                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            // slice order 0, 1, ..., S-1: the same sum whichever CTA finished first
-            for (int src = 0; src < S; ++src) {
-                const uint32_t peer = S == 1 ? sC_addr : map_to_rank(sC_addr, static_cast<uint32_t>(src));
-                float4 v[kRedBatch];
-#pragma unroll
-                for (int u = 0; u < kRedBatch; ++u) {
-                    if (first + 128 * u >= items) continue;
-                    if (S == 1) v[u] = *reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(sC) + off[u]);
-                    else v[u] = ld_cluster_f32x4(peer + off[u]);
-                }
-#pragma unroll
-                for (int u = 0; u < kRedBatch; ++u) {
-                    if (first + 128 * u < items) {
-                        acc[u].x += v[u].x;
-                        acc[u].y += v[u].y;
-                        acc[u].z += v[u].z;
-                        acc[u].w += v[u].w;
+                    for (int i = 0; i < 32; ++i) {
+                        if (i < cnt) *cp = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i])));
+                        cp += p.ldc;
                     }
                 }
             }
+            if (et_first_lane(warp, lane)) MXFP4_PHASE(11);
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after_sync();
+            tmem_dealloc(tmem_base, p.tmem_cols);
+        }
+        return;
+    }
+
+    // K slices > 1. Row m of the tile belongs to CTA m / rows_per of the cluster. Every CTA
+    // posts its fp32 accumulator rows from tensor memory straight into the owner's receive
+    // buffer (slot = source rank); after one cluster barrier each owner sums its rows over the
+    // sources in rank order (run-to-run identical) and stores bf16. Without a dedicated
+    // receive buffer a first barrier makes sure every peer's MMAs are done before its pipeline
+    // buffers are overwritten.
+    if (!p.recv_dedicated) cluster_sync();
+    if (threadIdx.x == 64) MXFP4_PHASE(7);
+    if (warp >= 2 && ok) {
+        const uint32_t recv_addr = smem_addr(sRecv);
+        const uint32_t own_off = static_cast<uint32_t>((split * rows_per) * kTileN + nl) * 4u;
+        for (int cb = half * 32; cb < m_valid; cb += 64) {
+            uint32_t r[32];
+            tmem_load_16(trow + cb, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+            if (cb + 16 < m_valid) tmem_load_16(trow + cb + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+            tmem_load_wait();
+            int owner = cb / rows_per;
+            int lm = cb - owner * rows_per;
+            uint32_t addr = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
+                            static_cast<uint32_t>(lm) * (kTileN * 4u);
+            const int cnt = min(32, m_valid - cb);
 #pragma unroll
-            for (int u = 0; u < kRedBatch; ++u) {
-                const int i = first + 128 * u;
-                if (i >= items) continue;
-                const int m = r0 + i / (kTileN / 4);
-                const int n = n0 + (i % (kTileN / 4)) * 4;
-                uint16_t* crow = p.c + static_cast<int64_t>(m0 + m) * p.ldc;
-                const uint32_t lo = pack_bf16x2(acc[u].x, acc[u].y), hi = pack_bf16x2(acc[u].z, acc[u].w);
-                if (p.c_vec4 && n + 3 < p.N) {
-                    *reinterpret_cast<uint2*>(crow + n) = make_uint2(lo, hi);
-                } else {
-                    const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                           static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (n + t < p.N) crow[n + t] = h[t];
+            for (int i = 0; i < 32; ++i) {
+                if (i < cnt) {
+                    st_cluster_f32(addr, __uint_as_float(r[i]));
+                    addr += kTileN * 4u;
+                    if (++lm == rows_per) {
+                        lm = 0;
+                        ++owner;
+                        if (owner < S) addr = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                    }
                 }
             }
         }
     }
+    if (threadIdx.x == 64) MXFP4_PHASE(8);
     __syncwarp();
-    if (p.splits > 1) cluster_sync();   // keep this CTA's staged tile alive until every peer read it
+    tc_fence_before_sync();
+    cluster_sync();
+    if (threadIdx.x == 64) MXFP4_PHASE(9);
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(*tmem_slot, p.tmem_cols);
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+    if (warp >= 2) {
+        // owner: rows r0 .. r1 of the tile, 4 output columns per thread per row
+        const int et = threadIdx.x - 64;
+        const int nl4 = (et & 31) * 4;
+        const int n4 = n0 + nl4;
+        const bool vec = p.c_vec4 && n4 + 3 < p.N;
+        for (int lm = et >> 5; lm < r1 - r0; lm += kEpiWarps) {
+            float4 acc = *reinterpret_cast<const float4*>(sRecv + lm * kTileN + nl4);
+            for (int src = 1; src < S; ++src) {
+                const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * rows_per + lm) * kTileN + nl4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
+            const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
+            if (vec) {
+                *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
+            } else {
+                const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                       static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (n4 + t < p.N) crow[n4 + t] = h[t];
+            }
+        }
+        if (et == 0) MXFP4_PHASE(11);
     }
 }
 
@@ -404,3 +462,10 @@ cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStr
 }
 
 }  // namespace mxfp4
+
+#ifdef MXFP4_TRACE
+extern "C" int mxfp4_trace_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, mxfp4::trace_buffer, bytes));
+}
+extern "C" int mxfp4_trace_clusters(int size, size_t smem) { return mxfp4::max_active_clusters(size, smem); }
+#endif

@@ -5,7 +5,20 @@
 #include <cstdint>
 #include <cuda.h>
 
+// Phase markers for a timing build: compiled with -DMXFP4_TRACE, MXFP4_PHASE(slot) records the
+// global timer for this CTA into mxfp4_trace (read back with mxfp4_trace_read); otherwise it
+// compiles to nothing.
+#ifdef MXFP4_TRACE
+#define MXFP4_PHASE(slot) (::mxfp4::trace_buffer[blockIdx.x % 4096][(slot)] = ::mxfp4::global_timer_ns())
+#else
+#define MXFP4_PHASE(slot) ((void)0)
+#endif
+
 namespace mxfp4 {
+
+#ifdef MXFP4_TRACE
+static __device__ unsigned long long trace_buffer[4096][16];
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -194,13 +207,9 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t 
     return r;
 }
 
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
+// Posted store of one fp32 into (possibly another CTA's) shared memory of this cluster.
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ bool elect_one() {
