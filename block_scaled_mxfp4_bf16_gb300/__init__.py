@@ -44,7 +44,8 @@ class Mxfp4Error(RuntimeError):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("path", ctypes.c_int), ("splits", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("path", ctypes.c_int), ("splits", ctypes.c_int), ("m_tile", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
 
 def load_library() -> ctypes.CDLL:
@@ -105,8 +106,8 @@ def _dev(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
-def _opts(path: int, splits: int):
-    return ctypes.byref(_Options(path, splits))
+def _opts(path: int, splits: int, m_tile: int = 0):
+    return ctypes.byref(_Options(path, splits, m_tile))
 
 
 def mxfp4_version() -> int:
@@ -154,8 +155,8 @@ def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | N
     return packed
 
 
-def mxfp4_gemm_workspace_size(M: int, N: int, K: int, path: int = 0, splits: int = 0) -> int:
-    return int(load_library().mxfp4_gemm_workspace_size_ex(M, N, K, _opts(path, splits)))
+def mxfp4_gemm_workspace_size(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> int:
+    return int(load_library().mxfp4_gemm_workspace_size_ex(M, N, K, _opts(path, splits, m_tile)))
 
 
 def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
@@ -178,7 +179,7 @@ def _workspace(device: torch.device, nbytes: int, stream) -> torch.Tensor | None
 
 def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
-               stream=None) -> torch.Tensor:
+               stream=None, m_tile: int = 0) -> torch.Tensor:
     """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b."""
     L = load_library()
     _dev(a, "a")
@@ -190,20 +191,21 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
     st = _stream(stream)
-    need = mxfp4_gemm_workspace_size(M, N, K, path, splits) if M and N else 0
+    need = mxfp4_gemm_workspace_size(M, N, K, path, splits, m_tile) if M and N else 0
     if workspace is None:
         workspace = _workspace(a.device, need, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(L.mxfp4_gemm_ex(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
-                           ws_ptr, ws_bytes, _opts(path, splits), st), "mxfp4_gemm")
+                           ws_ptr, ws_bytes, _opts(path, splits, m_tile), st), "mxfp4_gemm")
     return c
 
 
-def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0) -> dict:
+def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> dict:
     L = load_library()
     out = [ctypes.c_int() for _ in range(5)]
-    _check(L.mxfp4_gemm_plan(M, N, K, _opts(path, splits), *[ctypes.byref(o) for o in out]), "mxfp4_gemm_plan")
+    _check(L.mxfp4_gemm_plan(M, N, K, _opts(path, splits, m_tile), *[ctypes.byref(o) for o in out]),
+           "mxfp4_gemm_plan")
     return dict(zip(["path", "splits", "m_tile", "ctas", "stages"], [o.value for o in out]))
 
 

@@ -32,6 +32,25 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // m*128 + ceil(m/128)*1024 bytes.
 constexpr uint32_t kWBlock = kBRowsBytes + 2 * kSfChunk;
 
+// Split-K reduction: the tile's rows are dealt to the cluster's CTAs in runs of rows_per (a
+// multiple of 4); an owner receives [source][weight row n][recv_stride] fp32, where the stride
+// (in floats) pads the run so that consecutive rows n land 16 bytes apart modulo 32 banks.
+__host__ __device__ inline int red_rows_per(int m_valid, int splits) {
+    return ((m_valid + splits - 1) / splits + 3) / 4 * 4;
+}
+__host__ __device__ inline int red_stride(int rows_per) {
+    const int units = rows_per / 4 + 1;          // 16-byte units, made odd
+    return 4 * (units + ((units & 1) == 0 ? 1 : 0));
+}
+// Short runs go as 16-byte stores into [source][n][stride]; long runs as rows of the tile,
+// [source][row][n], one contiguous 128-byte segment per warp store (remote stores coalesce
+// per contiguous segment).
+constexpr int kRedVecMaxRows = 16;
+__host__ __device__ inline size_t red_recv_floats(int rows_per, int splits) {
+    return rows_per <= kRedVecMaxRows ? static_cast<size_t>(splits) * 128 * red_stride(rows_per)
+                                      : static_cast<size_t>(splits) * rows_per * 128;
+}
+
 __host__ __device__ inline uint32_t swz_chunk_offset(uint32_t r, uint32_t c) {
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }
@@ -90,7 +109,8 @@ struct DeviceInfo {
 };
 
 int device_info(DeviceInfo* out);   // MXFP4_OK or an error status
-int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int sm_count, GemmPlan* plan);
+int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
+              GemmPlan* plan);
 size_t packed_b_bytes(int64_t N, int64_t K);
 
 // Kernel launchers (return cudaError_t).

@@ -83,9 +83,9 @@ static int plan_layout(GemmPlan& p) {
     const int a_slots = p.path == 1 ? p.atoms_max : p.stages;
     p.off_araw = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
     size_t end = align_up(p.off_araw + raw_bytes, 1024);
-    // reduction receive buffer: [source rank][rows owned][128] fp32
-    const size_t rows_per = static_cast<size_t>(cdiv(p.m_tile, p.splits));
-    const size_t recv_bytes = static_cast<size_t>(p.splits) * rows_per * kTileN * sizeof(float);
+    // reduction receive buffer: [source rank][weight row][padded run of owned rows] fp32
+    const size_t recv_bytes = p.splits > 1 ? red_recv_floats(red_rows_per(p.m_tile, p.splits), p.splits) * sizeof(float)
+                                           : static_cast<size_t>(p.m_tile) * kTileN * sizeof(float);
     if (p.splits > 1 && end + recv_bytes <= budget) {
         p.recv_dedicated = 1;
         p.off_recv = static_cast<uint32_t>(end);
@@ -121,10 +121,15 @@ static int active_clusters(int device, int size, size_t smem) {
     return n;
 }
 
-int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int sm_count, GemmPlan* P) {
+int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
+              GemmPlan* P) {
     GemmPlan p = {};
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_SHAPE;
-    p.m_tile = M <= kMaxMTile ? static_cast<int>(cdiv(M, 16) * 16) : kMaxMTile;
+    if (mtile_req < 0 || mtile_req > kMaxMTile || mtile_req % 16 != 0) return MXFP4_ERR_ARG;
+    // Token tile: all of M up to 128; 128 up to M = 512 (half the A traffic and reduction per
+    // CTA of a 256 tile, measured faster on 256x4096x7168); 256 beyond.
+    p.m_tile = M <= 128 ? static_cast<int>(cdiv(M, 16) * 16) : (M <= 512 ? 128 : kMaxMTile);
+    if (mtile_req > 0) p.m_tile = std::min(static_cast<int>(cdiv(M, 16) * 16), mtile_req);
     p.nmc = (p.m_tile + 127) / 128;
     p.m_tiles = static_cast<int>(cdiv(M, p.m_tile));
     p.n_tiles = static_cast<int>(cdiv(N, kTileN));
@@ -132,9 +137,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     p.a_block = static_cast<uint32_t>(p.m_tile) * 128u + static_cast<uint32_t>(p.nmc) * 2u * kSfChunk;
     const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
-    // Fused quantization repeats A's quantization once per weight tile; keep it where A is
-    // small next to the weight stream (M <= 32, the pages' small-M split), else quantize once.
-    p.path = path_req ? path_req : (M <= 32 ? 1 : 2);
+    // Fused quantization puts A's load and quantization on the GEMM's critical path (behind the
+    // dependency wait), while the two-kernel path overlaps them with the weight prologue; the
+    // fused path only wins for the smallest token counts (measured on M = 8 and 16).
+    p.path = path_req ? path_req : (M <= 16 ? 1 : 2);
     if (p.path != 1 && p.path != 2) return MXFP4_ERR_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -155,8 +161,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     }
     // Automatic: as many K slices as fill the SMs (within the portable cluster size), fewer if
     // that many clusters would not all be resident at once.
+    // A split must buy more than its reduction costs: with few output tiles (under a quarter of
+    // the SMs) each slice keeps at least two 256-K steps, otherwise at least eight (measured on
+    // the 32x4096x512, 64x7168x2048 and 256x4096x7168 workloads).
     const int64_t fill = std::max<int64_t>(1, sm_count / std::max<int64_t>(1, units));
-    const int s_max = static_cast<int>(std::min<int64_t>({fill, static_cast<int64_t>(p.k_atoms),
+    const int64_t by_atoms = units * 4 < sm_count ? p.k_atoms / 2 : p.k_atoms / 8;
+    const int s_max = static_cast<int>(std::min<int64_t>({fill, std::max<int64_t>(1, by_atoms),
                                                           static_cast<int64_t>(kAutoMaxSplits)}));
     for (int s = s_max; s >= 1; --s) {
         GemmPlan q = p;
@@ -291,7 +301,7 @@ size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4
     DeviceInfo di;
     if (device_info(&di) != MXFP4_OK) return 0;
     GemmPlan plan;
-    if (make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, di.sm_count, &plan) != MXFP4_OK) return 0;
+    if (make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan) != MXFP4_OK) return 0;
     return plan.ws_total;
 }
 
@@ -310,12 +320,12 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
                     int* m_tile, int* ctas, int* stages) {
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 64 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, di.sm_count, &plan);
+    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
     if (st != MXFP4_OK) return st;
     if (path) *path = plan.path;
     if (splits) *splits = plan.splits;
@@ -327,14 +337,14 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
 
 int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
                   int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts, void* stream) {
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     int st = check_gemm_args(a, M, K, lda, packed_b, N, c, ldc);
     if (st != MXFP4_OK || M == 0 || N == 0) return st;
     DeviceInfo di;
     st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, di.sm_count, &plan);
+    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
     if (st != MXFP4_OK) return st;
     if (plan.ws_total > 0) {
         if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
@@ -410,7 +420,7 @@ extern "C" int mxfp4_gemm_noalloc(const void* a, int64_t M, int64_t K, int64_t l
     if (st != MXFP4_OK) return st;
     // the automatic plan, whose scratch must fit the array
     GemmPlan plan;
-    st = make_plan(M, N, K, 0, 0, di.sm_count, &plan);
+    st = make_plan(M, N, K, 0, 0, 0, di.sm_count, &plan);
     if (st != MXFP4_OK) return st;
     if (plan.ws_total > MXFP4_NOALLOC_SCRATCH_BYTES) return MXFP4_ERR_WORKSPACE;
     uint8_t* ws = nullptr;

@@ -110,8 +110,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
     const uint64_t lim = p.wait_limit_ns;
     // rows of the output tile reduced (and stored) by CTA `rank` of the cluster
-    const int rows_per = (m_valid + S - 1) / S;   // >= 1
-    const int r0 = split * rows_per;
+    const int rows_per = red_rows_per(m_valid, S);   // multiple of 4
+    const int r0 = min(m_valid, split * rows_per);
     const int r1 = min(m_valid, r0 + rows_per);
     // fused path: this CTA's bf16 A slice, rows of kslice elements
     const int kslice = min(na * kAtomK, p.K - a0 * kAtomK);
@@ -147,8 +147,13 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
             }
+            if (p.fused)   // warm L2 with this CTA's A rows while the previous grid finishes
+                for (int r = 0; r < m_valid; ++r)
+                    prefetch_l2_bulk(p.a + static_cast<int64_t>(m0 + r) * p.lda + a0 * kAtomK,
+                                     static_cast<uint32_t>(kslice) * 2u);
             MXFP4_PHASE(1);
             pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
+            MXFP4_PHASE(2);
             if (p.fused) {
                 // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip
                 const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
@@ -188,42 +193,59 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         tc_fence_after_sync();
         tmem_base = *tmem_slot;
         if (lane == 0) {
+            // The issue loop is kept to integer adds: a shared-memory descriptor's start-address
+            // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
             const uint32_t t_acc = tmem_base;
-            const uint32_t t_sfb = tmem_base + static_cast<uint32_t>(p.m_tile);
-            const uint32_t t_sfa = t_sfb + static_cast<uint32_t>(stages) * 8u;
+            const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.m_tile);
+            const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
+            const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);      // columns per stage
             const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
+            const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
+            const uint64_t b_desc0 = desc_sw128(smem_addr(sB));
+            const uint64_t a_desc0 = desc_sw128(smem_addr(sA));
+            const uint64_t sfb_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
+            const uint64_t sfa_desc0 = desc_sf(smem_addr(sA + a_rows));
+            const uint32_t b_step = kWBlock >> 4, a_step = a_block >> 4, chunk_step = kSfChunk >> 4;
+            const bool two_chunks = p.nmc == 2;
             bool mok = true;
-            MXFP4_PHASE(2);
             if (p.fused) mok = mbar_wait(a_full, 0, lim);
             MXFP4_PHASE(3);
             tc_fence_after_sync();
+            int s = 0;
+            uint32_t phase = 0;
+#pragma unroll 1
             for (int j = 0; mok && j < na; ++j) {
-                const int s = j % stages;
-                if (!mbar_wait(&full[s], (j / stages) & 1, lim)) { mok = false; break; }
+                if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
                 if (j == 0) MXFP4_PHASE(4);
                 if (j == na - 1) MXFP4_PHASE(5);
                 tc_fence_after_sync();
-                const uint8_t* bb = sB + s * kWBlock;
-                const uint8_t* ab = sA + (p.fused ? j : s) * a_block;
-                const uint32_t sfb_cols = t_sfb + static_cast<uint32_t>(s) * 8u;
-                const uint32_t sfa_cols = t_sfa + static_cast<uint32_t>(s) * 8u * p.nmc;
-                for (int g = 0; g < 2; ++g) {
-                    tc_copy_sf(sfb_cols + 4u * g, desc_sf(smem_addr(bb + kBRowsBytes + kSfChunk * g)));
-                    for (int c = 0; c < p.nmc; ++c)
-                        tc_copy_sf(sfa_cols + 4u * (g * p.nmc + c),
-                                   desc_sf(smem_addr(ab + a_rows + kSfChunk * (2 * c + g))));
+                const uint32_t slot = static_cast<uint32_t>(p.fused ? j : s);
+                const uint64_t bd = b_desc0 + static_cast<uint32_t>(s) * b_step;
+                const uint64_t ad = a_desc0 + slot * a_step;
+                const uint64_t sfbd = sfb_desc0 + static_cast<uint32_t>(s) * b_step;
+                const uint64_t sfad = sfa_desc0 + slot * a_step;
+                const uint32_t sfb_cols = t_sfb0 + static_cast<uint32_t>(s) * 8u;
+                const uint32_t sfa_cols = t_sfa0 + static_cast<uint32_t>(s) * sfa_step;
+                // scale factors: weight groups 2j, 2j+1 -> 4 columns each; token chunks likewise
+                tc_copy_sf(sfb_cols, sfbd);
+                tc_copy_sf(sfb_cols + 4u, sfbd + chunk_step);
+                if (!two_chunks) {
+                    tc_copy_sf(sfa_cols, sfad);
+                    tc_copy_sf(sfa_cols + 4u, sfad + chunk_step);
+                } else {   // 256 tokens: chunks (c, g) at 512 * (2c + g), columns 4 * (2g + c)
+                    tc_copy_sf(sfa_cols, sfad);
+                    tc_copy_sf(sfa_cols + 4u, sfad + 2 * chunk_step);
+                    tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
+                    tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
                 }
-                const uint32_t b_addr = smem_addr(bb);
-                const uint32_t a_addr = smem_addr(ab);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t g = kk >> 1;
-                    const uint32_t sf_id = (kk & 1) * 2u;   // scale bytes {0,1} or {2,3} of the column
-                    const uint32_t idesc = idesc0 | (sf_id << 29) | (sf_id << 4);
-                    mma_mxf4(t_acc, desc_sw128(b_addr + 32u * kk), desc_sw128(a_addr + 32u * kk), idesc,
-                             sfb_cols + 4u * g, sfa_cols + 4u * g * p.nmc, (j | kk) != 0);
-                }
+                const uint32_t sfa_g1 = sfa_cols + 4u * static_cast<uint32_t>(p.nmc);
+                // K step kk of the atom: +32 bytes in both operands (descriptor +2)
+                mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != 0);
+                mma_mxf4(t_acc, bd + 2, ad + 2, idesc1, sfb_cols, sfa_cols, 1);
+                mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
+                mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
                 tc_commit(&empty[s]);
+                if (++s == stages) { s = 0; phase ^= 1u; }
             }
             if (!mok) fail(p, flags);
             tc_commit(acc_full);
@@ -313,17 +335,23 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         return;
     }
 
-    // K slices > 1. Row m of the tile belongs to CTA m / rows_per of the cluster. Every CTA
-    // posts its fp32 accumulator rows from tensor memory straight into the owner's receive
-    // buffer (slot = source rank); after one cluster barrier each owner sums its rows over the
-    // sources in rank order (run-to-run identical) and stores bf16. Without a dedicated
-    // receive buffer a first barrier makes sure every peer's MMAs are done before its pipeline
-    // buffers are overwritten.
+    // K slices > 1. Runs of rows_per rows of the tile belong to successive CTAs of the cluster.
+    // Every CTA posts its fp32 accumulator straight from tensor memory into the owners' receive
+    // buffers (slot = source rank): short runs as 16-byte stores of four tokens, long runs as
+    // contiguous 128-byte rows. After one cluster barrier each owner sums its rows over the
+    // sources in rank order (run-to-run identical) and stores bf16.
+    // Without a dedicated receive buffer a first barrier makes sure every peer's MMAs are done
+    // before its pipeline buffers are overwritten.
+    const bool vec = rows_per <= kRedVecMaxRows;
+    const int stride = red_stride(rows_per);
     if (!p.recv_dedicated) cluster_sync();
     if (threadIdx.x == 64) MXFP4_PHASE(7);
     if (warp >= 2 && ok) {
         const uint32_t recv_addr = smem_addr(sRecv);
-        const uint32_t own_off = static_cast<uint32_t>((split * rows_per) * kTileN + nl) * 4u;
+        // this source's slot in an owner: [n][stride] (vector form) or [row][n] (row form)
+        const uint32_t own_off = vec ? static_cast<uint32_t>((split * kTileN + nl) * stride) * 4u
+                                     : static_cast<uint32_t>(split * rows_per * kTileN + nl) * 4u;
+        const uint32_t row_step = vec ? 4u : kTileN * 4u;   // bytes from one token row to the next
         for (int cb = half * 32; cb < m_valid; cb += 64) {
             uint32_t r[32];
             tmem_load_16(trow + cb, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
@@ -331,18 +359,33 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             tmem_load_wait();
             int owner = cb / rows_per;
             int lm = cb - owner * rows_per;
-            uint32_t addr = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
-                            static_cast<uint32_t>(lm) * (kTileN * 4u);
-            const int cnt = min(32, m_valid - cb);
+            uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
+                            static_cast<uint32_t>(lm) * row_step;
+            if (vec) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (i < cnt) {
-                    st_cluster_f32(addr, __uint_as_float(r[i]));
-                    addr += kTileN * 4u;
-                    if (++lm == rows_per) {
-                        lm = 0;
-                        ++owner;
-                        if (owner < S) addr = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                for (int i = 0; i < 32; i += 4) {
+                    if (cb + i < m_valid) {   // rows past M in this group of 4 carry padding, never stored
+                        st_cluster_v4(peer, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                        peer += 16u;
+                        lm += 4;
+                        if (lm == rows_per) {
+                            lm = 0;
+                            ++owner;
+                            if (owner < S) peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (cb + i < m_valid) {
+                        st_cluster_f32(peer, __uint_as_float(r[i]));
+                        peer += kTileN * 4u;
+                        if (++lm == rows_per) {
+                            lm = 0;
+                            ++owner;
+                            if (owner < S) peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                        }
                     }
                 }
             }
@@ -358,30 +401,56 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
     if (warp >= 2) {
-        // owner: rows r0 .. r1 of the tile, 4 output columns per thread per row
         const int et = threadIdx.x - 64;
-        const int nl4 = (et & 31) * 4;
-        const int n4 = n0 + nl4;
-        const bool vec = p.c_vec4 && n4 + 3 < p.N;
-        for (int lm = et >> 5; lm < r1 - r0; lm += kEpiWarps) {
-            float4 acc = *reinterpret_cast<const float4*>(sRecv + lm * kTileN + nl4);
-            for (int src = 1; src < S; ++src) {
-                const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * rows_per + lm) * kTileN + nl4);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
-            const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
-            if (vec) {
-                *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
-            } else {
-                const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                       static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+        const int nrows = r1 - r0;
+        if (vec) {
+            // owner, vector form: a thread sums 4 consecutive rows of one column
+            const int cn = et & (kTileN - 1);
+            const int nn = n0 + cn;
+            if (nn < p.N) {
+                for (int lm = (et / kTileN) * 4; lm < nrows; lm += 4 * (kEpiThreads / kTileN)) {
+                    float4 acc = *reinterpret_cast<const float4*>(sRecv + cn * stride + lm);
+                    for (int src = 1; src < S; ++src) {
+                        const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * kTileN + cn) * stride + lm);
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                        acc.w += v.w;
+                    }
+                    uint16_t* cp = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc + nn;
+                    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    if (n4 + t < p.N) crow[n4 + t] = h[t];
+                    for (int k = 0; k < 4; ++k) {
+                        if (lm + k < nrows) *cp = __bfloat16_as_ushort(__float2bfloat16_rn(vals[k]));
+                        cp += p.ldc;
+                    }
+                }
+            }
+        } else {
+            // owner, row form: a thread sums 4 consecutive columns of one row
+            const int nl4 = (et & 31) * 4;
+            const int n4 = n0 + nl4;
+            const bool v4 = p.c_vec4 && n4 + 3 < p.N;
+            for (int lm = et >> 5; lm < nrows; lm += kEpiWarps) {
+                float4 acc = *reinterpret_cast<const float4*>(sRecv + lm * kTileN + nl4);
+                for (int src = 1; src < S; ++src) {
+                    const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * rows_per + lm) * kTileN + nl4);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
+                const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
+                if (v4) {
+                    *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
+                } else {
+                    const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                           static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (n4 + t < p.N) crow[n4 + t] = h[t];
+                }
             }
         }
         if (et == 0) MXFP4_PHASE(11);

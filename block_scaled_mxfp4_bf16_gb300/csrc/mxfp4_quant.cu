@@ -12,10 +12,12 @@ __global__ void __launch_bounds__(256)
 quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                 uint8_t* __restrict__ q, uint8_t* __restrict__ scales) {
     pdl_launch_dependents();
-    pdl_wait_prior_grid();   // x may come from the previous kernel; q/scales may still be read by it
     const int64_t nblk = K / 32;
     const int64_t items = rows * nblk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (first < items) prefetch_l2(x + (first / nblk) * ld + (first % nblk) * 32);   // see prefetch_l2
+    pdl_wait_prior_grid();   // x may come from the previous kernel; q/scales may still be read by it
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
         const int64_t r = it / nblk;
         const int64_t kb = it - r * nblk;
@@ -34,10 +36,15 @@ __global__ void __launch_bounds__(256)
 quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
     pdl_launch_dependents();
-    pdl_wait_prior_grid();
     const int64_t nblk = K / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
+    {   // warm L2 with this thread's first block while the previous grid finishes (see prefetch_l2)
+        const int64_t it0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        const int64_t r = it0 / row_items, kbp = it0 - (it0 / row_items) * row_items;
+        if (it0 < items && r < rows && kbp < nblk) prefetch_l2(x + r * ld + kbp * 32);
+    }
+    pdl_wait_prior_grid();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int lane = threadIdx.x & 31;
     // the loop bound is uniform per warp (warps start at multiples of 32) so the shuffles below

@@ -207,9 +207,14 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t 
     return r;
 }
 
-// Posted store of one fp32 into (possibly another CTA's) shared memory of this cluster.
+// Posted stores into (possibly another CTA's) shared memory of this cluster.
 __device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool elect_one() {
@@ -220,6 +225,20 @@ __device__ __forceinline__ bool elect_one() {
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(pred));
     return pred != 0;
+}
+
+}  // namespace mxfp4
+
+namespace mxfp4 {
+
+// Warm L2 with a global range without touching shared memory or registers. Issued before the
+// wait on the previous grid it stays correct: nothing reads the prefetched bytes directly, and
+// later loads go through L2, which every write of the previous grid updates.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 }  // namespace mxfp4

@@ -138,7 +138,8 @@ typedef struct {
     int path;    /* 0 = automatic, 1 = A quantized inside the GEMM's producer warps (fused),
                     2 = standalone quantize kernel into the workspace, then the GEMM */
     int splits;  /* 0 = automatic, else the number of K slices per output tile (>= 1) */
-    int reserved[6];
+    int m_tile;  /* 0 = automatic, else tokens per tile: a multiple of 16 in [16, 256] */
+    int reserved[5];
 } mxfp4_gemm_options;
 
 /* mxfp4_gemm with an explicit plan. The workspace must be at least

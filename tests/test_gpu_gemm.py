@@ -130,3 +130,26 @@ def test_timeout_is_reported_not_hung():
     q, s = mx.mxfp4_quantize(x)
     torch.cuda.synchronize()
     assert int(s[0, 0].item()) == 125
+
+
+@pytest.mark.parametrize("M,N,K,m_tile", [(256, 384, 1024, 128), (100, 256, 768, 64), (64, 512, 512, 16)])
+def test_gemm_token_tile_override_vs_oracle(M, N, K, m_tile):
+    # several token tiles per weight tile (m_tiles > 1), with and without split-K, both paths
+    mx = _mx()
+    a = workloads.random_bf16(M, K, seed=M + m_tile)
+    b = workloads.random_bf16(N, K, seed=N + m_tile)
+    bq, bs = mx.mxfp4_quantize(b.cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    ref = oracle_c(a, to_np_u8(bq), to_np_u8(bs))
+    for path in (1, 2):
+        for splits in (1, 2):
+            try:
+                mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)
+            except mx.Mxfp4Error as e:
+                # a forced fused path whose staged A slice exceeds shared memory is refused
+                assert path == 1 and e.status == 2
+                continue
+            c = mx.mxfp4_gemm(a.cuda(), packed, N, path=path, splits=splits, m_tile=m_tile)
+            torch.cuda.synchronize()
+            assert mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)["m_tile"] == m_tile
+            check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} m_tile {m_tile} path {path} splits {splits}")
