@@ -1,0 +1,47 @@
+"""Host logic of the multi-process benchmark path, on CPU with gloo and two ranks: the job time
+is the slowest rank's, and each rank's workload is independent (no data-path collective)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    got = bench.max_over_ranks(float(10 + 5 * rank))
+    out[rank] = got
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_ranks_gloo():
+    world = 2
+    port = _free_port()
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_max_over_ranks_single_process_is_identity():
+    import bench
+    assert not dist.is_initialized()
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_traffic_is_dropped_when_kernel_sources_change(monkeypatch):
+    import bench
+    name = next(iter(bench.MEASURED_TRAFFIC))
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, bench.kernel_source_hash()))
+    assert bench.measured_traffic(name) == 123
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, "0000000000000000"))
+    assert bench.measured_traffic(name) is None
