@@ -16,7 +16,7 @@ Sources (the "amd-mxfp4-mm" leaderboard submissions):
 
 Pins (tests/test_oracle_pins.py): the e2m1 grid, an exhaustive fp32 cross-check against an
 independent nearest-value encoder, hand-worked blocks (tests/golden/hand_blocks.json), the
-spec scale formula evaluated literally for every bf16 amax, an error-bound invariant,
+scale formula as the method states it, evaluated literally for every bf16 amax, an error-bound invariant,
 exact closed-form GEMMs and brute-force tiny GEMMs. No oracle function is "parity unpinned".
 """
 from __future__ import annotations
