@@ -8,9 +8,9 @@
 namespace mxfp4 {
 
 constexpr int kMaxStages = 8;
-constexpr int kEpiWarps = 8;               // warps 2..9: A quantization (fused path) and the epilogue
+constexpr int kEpiWarps = 8;               // warps 3..10: A quantization (fused path) and the epilogue
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kGemmThreads = 64 + kEpiThreads;   // warp 0 copies, warp 1 MMA
+constexpr int kGemmThreads = 96 + kEpiThreads;   // warp 0 copies, warps 1-2 MMA
 constexpr int kTileN = 128;                // weight rows per MMA (the MMA's M)
 constexpr int kAtomK = 256;                // K elements per pipeline step (128-byte rows)
 constexpr int kMaxMTile = 256;             // tokens per tile (the MMA's N)
@@ -68,7 +68,9 @@ struct GemmPlan {
     int m_tiles, n_tiles;
     int k_atoms;       // ceil(K / 256)
     int atoms_max;     // most atoms any split gets
+    int raw_rows;      // fused path: token rows staged as bf16 (the real rows of a tile)
     int stages;
+    int issuers;       // MMA-issuing threads (1 or 2), one accumulator each
     int ctas;
     uint32_t a_block;  // bytes of one token block
     // shared-memory layout (bytes from a 1 KB-aligned base): weight stages at 0, token blocks
@@ -90,7 +92,7 @@ struct GemmArgs {
     int64_t ldc;
     uint32_t* status;      // device error word
     int M, N, K;
-    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages, atoms_max;
+    int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages, atoms_max, issuers;
     uint32_t a_block, off_a, off_araw, off_recv, off_bar;
     int recv_dedicated;
     uint32_t tmem_cols;

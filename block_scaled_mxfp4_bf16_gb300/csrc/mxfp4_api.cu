@@ -67,42 +67,55 @@ size_t packed_b_bytes(int64_t N, int64_t K) {
 
 // Shared-memory layout, tensor-memory columns and workspace of a plan whose tiling, path and
 // split count are set. MXFP4_ERR_SHAPE if it does not fit.
-static int plan_layout(GemmPlan& p) {
+static int plan_layout(GemmPlan& p, int max_stages) {
     p.atoms_max = static_cast<int>(cdiv(p.k_atoms, p.splits));
     const size_t bar_bytes = 256;
     const size_t budget = kSmemLimit - 1024 - bar_bytes;
-    // fused: every atom's token block and the whole bf16 A slice stay resident
-    const size_t raw_bytes = p.path == 1 ? static_cast<size_t>(p.m_tile) * p.atoms_max * kAtomK * 2 : 0;
+    // fused: every atom's token block and the bf16 A slice of the real rows stay resident
+    const size_t raw_bytes = p.path == 1 ? static_cast<size_t>(p.raw_rows) * p.atoms_max * kAtomK * 2 : 0;
     size_t fixed = raw_bytes, per_stage = kWBlock;
     if (p.path == 1) fixed += static_cast<size_t>(p.atoms_max) * p.a_block;
     else per_stage += p.a_block;
     if (fixed + per_stage > budget) return MXFP4_ERR_SHAPE;
-    p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(kMaxStages), static_cast<size_t>(p.atoms_max),
+    p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(max_stages), static_cast<size_t>(p.atoms_max),
                                                   (budget - fixed) / per_stage}));
     p.off_a = static_cast<uint32_t>(p.stages) * kWBlock;
     const int a_slots = p.path == 1 ? p.atoms_max : p.stages;
     p.off_araw = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
     size_t end = align_up(p.off_araw + raw_bytes, 1024);
+    // two MMA issuers (two accumulators) while their columns fit; a 256-token MMA keeps the
+    // tensor core busy from one issuer
+    p.issuers = (p.m_tile <= 128 && p.atoms_max >= 2) ? 2 : 1;
+    const uint32_t cols = static_cast<uint32_t>(p.issuers * p.m_tile) +
+                          static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc);
+    p.tmem_cols = 32;
+    while (p.tmem_cols < cols) p.tmem_cols <<= 1;
+    // CTAs of this kernel that may share an SM: as many as tensor memory holds without any
+    // allocation having to wait (at most 2). Shared memory then keeps more from landing on one SM.
+    const int per_sm = std::max(1, std::min(2, static_cast<int>(512u / p.tmem_cols)));
+    const size_t sm_smem = 233472;   // shared memory per SM; each CTA also reserves 1 KB
+    auto fits = [&](size_t end, int n) { return n * (end + bar_bytes + 1024 + 1024) <= sm_smem; };
     // reduction receive buffer: [source rank][weight row][padded run of owned rows] fp32
     const size_t recv_bytes = p.splits > 1 ? red_recv_floats(red_rows_per(p.m_tile, p.splits), p.splits) * sizeof(float)
                                            : static_cast<size_t>(p.m_tile) * kTileN * sizeof(float);
-    if (p.splits > 1 && end + recv_bytes <= budget) {
-        p.recv_dedicated = 1;
+    const size_t end_dedicated = align_up(end + recv_bytes, 1024);
+    const size_t end_shared = std::max(end, align_up(recv_bytes, 1024));
+    // a dedicated buffer saves a cluster barrier; giving up a co-resident CTA costs more
+    if (p.splits > 1 && end_dedicated <= budget && (fits(end_dedicated, per_sm) || !fits(end_shared, per_sm))) {
+        p.recv_dedicated = 1;       // peers may post while this CTA still runs MMAs
         p.off_recv = static_cast<uint32_t>(end);
-        end = align_up(end + recv_bytes, 1024);
+        end = end_dedicated;
     } else {
         p.recv_dedicated = 0;       // over the pipeline buffers, written once every MMA is done
         p.off_recv = 0;
-        end = std::max(end, align_up(recv_bytes, 1024));
+        end = end_shared;
     }
-    // at least ~half the shared memory, so one CTA runs per SM and tensor memory is never contended
-    end = std::max(end, align_up(120 * 1024 - bar_bytes - 1024, 1024));
+    // no more CTAs per SM than tensor memory serves: pad shared memory so a further one cannot fit
+    const size_t floor_bytes = sm_smem / (per_sm + 1) + 1;
+    if (end + bar_bytes + 1024 + 1024 < floor_bytes) end = align_up(floor_bytes - bar_bytes - 1024 - 1024, 1024);
     p.off_bar = static_cast<uint32_t>(end);
     p.smem_bytes = p.off_bar + bar_bytes + 1024;
     if (p.smem_bytes > kSmemLimit) return MXFP4_ERR_SHAPE;
-    const uint32_t cols = static_cast<uint32_t>(p.m_tile) + static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc);
-    p.tmem_cols = 32;
-    while (p.tmem_cols < cols) p.tmem_cols <<= 1;
     p.ctas = p.m_tiles * p.n_tiles * p.splits;
     p.ws_total = p.path == 2 ? static_cast<size_t>(p.m_tiles) * p.k_atoms * p.a_block : 0;
     return MXFP4_OK;
@@ -135,6 +148,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     p.n_tiles = static_cast<int>(cdiv(N, kTileN));
     p.k_atoms = static_cast<int>(cdiv(K, kAtomK));
     p.a_block = static_cast<uint32_t>(p.m_tile) * 128u + static_cast<uint32_t>(p.nmc) * 2u * kSfChunk;
+    p.raw_rows = static_cast<int>(std::min<int64_t>(M, p.m_tile));
     const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
     // Fused quantization puts A's load and quantization on the GEMM's critical path (behind the
@@ -144,11 +158,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     if (p.path != 1 && p.path != 2) return MXFP4_ERR_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    auto layout_once = [&](GemmPlan& q) { return plan_layout(q, kMaxStages); };
     auto layout = [&](GemmPlan& q) {
-        int st = plan_layout(q);
+        int st = layout_once(q);
         if (st != MXFP4_OK && q.path == 1 && path_req == 0) {   // fused slice too big: two-kernel path
             q.path = 2;
-            st = plan_layout(q);
+            st = layout_once(q);
         }
         return st;
     };
@@ -223,6 +238,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     g.k_atoms = plan.k_atoms;
     g.stages = plan.stages;
     g.atoms_max = plan.atoms_max;
+    g.issuers = plan.issuers;
     g.a_block = plan.a_block;
     g.off_a = plan.off_a;
     g.off_araw = plan.off_araw;

@@ -15,10 +15,11 @@
 //   warp 0    : copy producer -- weight blocks (17 KB) and, in the two-kernel path, token
 //               blocks. The first stages are requested before the CTA waits on the previous
 //               grid (the weights never depend on it).
-//   warp 1    : tensor-memory allocation and the single MMA-issuing thread: per 256-K step it
+//   warps 1-2 : tensor-memory allocation and two MMA-issuing threads (alternate 256-K steps, two
+//               accumulators): per 256-K step a thread
 //               copies the scale factors into tensor memory (tcgen05.cp) and issues four
 //               128 x N x 64 block-scaled MMAs.
-//   warps 2-9 : in the fused path they quantize the CTA's bf16 token slice (staged in shared
+//   warps 3-10: in the fused path they quantize the CTA's bf16 token slice (staged in shared
 //               memory by one bulk copy per row) into the token-block layout (the pages'
 //               in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`);
 //               then they move the accumulator out of tensor memory.
@@ -67,7 +68,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp == 2 && lane == 0; }
+__device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp == 3 && lane == 0; }
+
+// 32 accumulator columns of this thread's lane (the second 16 only if `upper`), plus the
+// matching columns of the second accumulator `acc2` columns further when `two`.
+__device__ __forceinline__ void load_acc32(uint32_t taddr, bool upper, bool two, uint32_t acc2, uint32_t (&r)[32]) {
+    tmem_load_16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+    if (upper) tmem_load_16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+    if (two) {
+        uint32_t q[32];
+        tmem_load_16(taddr + acc2, *reinterpret_cast<uint32_t(*)[16]>(&q[0]));
+        if (upper) tmem_load_16(taddr + acc2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&q[16]));
+        tmem_load_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(q[i]));
+    } else {
+        tmem_load_wait();
+    }
+}
 
 __device__ __forceinline__ void fail(const GemmArgs& p, volatile uint32_t* abort_flag) {
     atomicOr(p.status, 1u);
@@ -124,7 +142,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             mbar_init(&empty[s], 1);
         }
         mbar_init(a_full, kEpiThreads);
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
         mbar_init(a_raw, 1);
         flags[0] = 0u;
         fence_mbar_init();
@@ -180,23 +198,34 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
             if (p.fused) mbar_wait(a_raw, 0, lim);
         }
-    } else if (warp == 1) {
-        // -------------------------------------------------------------------- MMA issuer
-        // Columns are allocated only after the previous grid has finished, so a CTA of this
-        // grid never holds columns a CTA of the previous grid is still waiting for.
-        pdl_wait_prior_grid();
-        tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
-        tmem_relinquish();
-        tc_fence_before_sync();
-        named_barrier_arrive(1, 32 + kEpiThreads);   // publish the column base to the epilogue warps
+    } else if (warp <= 2) {
+        // ------------------------------------------------------------------- MMA issuers
+        // Warp 1 allocates tensor memory; warps 1 and 2 (one thread each) issue the MMAs of
+        // alternate 256-K steps into two accumulators, which halves the serial issue chain
+        // (the epilogue adds them). With one issuer warp 2 only waits.
+        const int issuer = warp - 1;
+        if (warp == 1) {
+            // Columns are allocated only after the previous grid has finished, so a CTA of this
+            // grid never holds columns a CTA of the previous grid is still waiting for.
+            pdl_wait_prior_grid();
+            tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
+            tmem_relinquish();
+            tc_fence_before_sync();
+            // publish the column base: to warp 2 now (barrier 3), to the epilogue warps once
+            // they are done with the A slice (barrier 1)
+            named_barrier_arrive(3, 64);
+            named_barrier_arrive(1, 32 + kEpiThreads);
+        } else {
+            named_barrier(3, 64);
+        }
         __syncwarp();
         tc_fence_after_sync();
         tmem_base = *tmem_slot;
-        if (lane == 0) {
+        if (lane == 0 && issuer < p.issuers) {
             // The issue loop is kept to integer adds: a shared-memory descriptor's start-address
             // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
-            const uint32_t t_acc = tmem_base;
-            const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.m_tile);
+            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
+            const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
             const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
             const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);      // columns per stage
             const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
@@ -209,12 +238,13 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             const bool two_chunks = p.nmc == 2;
             bool mok = true;
             if (p.fused) mok = mbar_wait(a_full, 0, lim);
-            MXFP4_PHASE(3);
+            if (issuer == 0) MXFP4_PHASE(3);
             tc_fence_after_sync();
-            int s = 0;
+            int s = issuer;
             uint32_t phase = 0;
+            while (s >= stages) { s -= stages; phase ^= 1u; }
 #pragma unroll 1
-            for (int j = 0; mok && j < na; ++j) {
+            for (int j = issuer; mok && j < na; j += p.issuers) {
                 if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
                 if (j == 0) MXFP4_PHASE(4);
                 if (j == na - 1) MXFP4_PHASE(5);
@@ -240,19 +270,20 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 }
                 const uint32_t sfa_g1 = sfa_cols + 4u * static_cast<uint32_t>(p.nmc);
                 // K step kk of the atom: +32 bytes in both operands (descriptor +2)
-                mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != 0);
+                mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != issuer);
                 mma_mxf4(t_acc, bd + 2, ad + 2, idesc1, sfb_cols, sfa_cols, 1);
                 mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
                 mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
                 tc_commit(&empty[s]);
-                if (++s == stages) { s = 0; phase ^= 1u; }
+                s += p.issuers;
+                while (s >= stages) { s -= stages; phase ^= 1u; }
             }
             if (!mok) fail(p, flags);
             tc_commit(acc_full);
         }
     } else {
-        // -------------------------------------------------------------------- warps 2..9
-        const int et = threadIdx.x - 64;
+        // -------------------------------------------------------------------- warps 3..10
+        const int et = threadIdx.x - 96;
         if (p.fused) {
             // Quantize the staged bf16 slice into token blocks in shared memory, one 1x32 block
             // per item; rows past M and K past the end become zeros.
@@ -260,30 +291,55 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             if (et == 0) MXFP4_PHASE(10);
             if (!got) fail(p, flags);
             const int nblk = na * (kAtomK / 32);
-            const int total = p.m_tile * nblk;
-            for (int idx = et; idx < total; idx += kEpiThreads) {
-                const int r = idx / nblk;
-                const int kb = idx - r * nblk;
-                uint32_t out[4] = {0u, 0u, 0u, 0u}, sbyte = 0u;
-                if (got && r < m_valid && kb * 32 < kslice) {
-                    uint32_t w[16];
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        reinterpret_cast<const uint8_t*>(sAraw) + r * raw_row + kb * 64);
+            const int kblk = (kslice + 31) / 32;            // blocks of this slice inside K
+            // real rows, two blocks per thread per pass so their arithmetic interleaves
+            const int total = got ? m_valid * nblk : 0;
+            for (int first = et; first < total; first += 2 * kEpiThreads) {
+                uint32_t w[2][16], out[2][4], sbyte[2];
+                int rr[2], kk[2];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 v = src[i];
-                        w[4 * i + 0] = v.x;
-                        w[4 * i + 1] = v.y;
-                        w[4 * i + 2] = v.z;
-                        w[4 * i + 3] = v.w;
+                for (int u = 0; u < 2; ++u) {
+                    const int idx = first + u * kEpiThreads;
+                    rr[u] = idx < total ? idx / nblk : 0;
+                    kk[u] = idx < total ? idx - rr[u] * nblk : kblk;     // kblk: nothing to read
+                    if (kk[u] < kblk) {
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            reinterpret_cast<const uint8_t*>(sAraw) + rr[u] * raw_row + kk[u] * 64);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 v = src[i];
+                            w[u][4 * i + 0] = v.x;
+                            w[u][4 * i + 1] = v.y;
+                            w[u][4 * i + 2] = v.z;
+                            w[u][4 * i + 3] = v.w;
+                        }
                     }
-                    sbyte = quantize_block32(w, out);
                 }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    out[u][0] = out[u][1] = out[u][2] = out[u][3] = 0u;
+                    sbyte[u] = kk[u] < kblk ? quantize_block32(w[u], out[u]) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (first + u * kEpiThreads >= total) continue;
+                    const uint32_t c = static_cast<uint32_t>(kk[u] & 7);
+                    uint8_t* blk = sA + (kk[u] >> 3) * a_block;
+                    *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(rr[u]), c)) =
+                        make_uint4(out[u][0], out[u][1], out[u][2], out[u][3]);
+                    blk[a_rows + block_sf_offset(static_cast<uint32_t>(rr[u]), c)] = static_cast<uint8_t>(sbyte[u]);
+                }
+            }
+            // rows past M (or all rows if the A slice never arrived): zero codes and scales
+            const int first_pad = got ? m_valid : 0;
+            const int pad_total = (p.m_tile - first_pad) * nblk;
+            for (int idx = et; idx < pad_total; idx += kEpiThreads) {
+                const int r = first_pad + idx / nblk;
+                const int kb = idx % nblk;
                 const uint32_t c = static_cast<uint32_t>(kb & 7);
                 uint8_t* blk = sA + (kb >> 3) * a_block;
-                *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(r), c)) =
-                    make_uint4(out[0], out[1], out[2], out[3]);
-                blk[a_rows + block_sf_offset(static_cast<uint32_t>(r), c)] = static_cast<uint8_t>(sbyte);
+                *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(r), c)) = make_uint4(0u, 0u, 0u, 0u);
+                blk[a_rows + block_sf_offset(static_cast<uint32_t>(r), c)] = 0;
             }
             fence_proxy_async_smem();
             mbar_arrive(a_full);
@@ -301,19 +357,19 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // ------------------------------------------------------------------------ output
     // Accumulator D = C^T: tensor-memory lane = weight row n, column = token m. Epilogue warp w
     // reads the lanes of quadrant w % 4 and every other 32-column chunk (two warps per quadrant).
-    const int half = ((warp - 2) >> 2) & 1;
+    const int half = ((warp - 3) >> 2) & 1;
+    const bool two_acc = p.issuers == 2 && na >= 2;     // the second accumulator holds data
+    const uint32_t acc2 = static_cast<uint32_t>(p.m_tile);
     const int nl = (warp & 3) * 32 + lane;
     const int n = n0 + nl;
     const uint32_t trow = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     __syncwarp();
     if (S == 1) {
         // one K slice: tensor memory -> bf16 C directly, one output column per thread
-        if (warp >= 2 && ok) {
+        if (warp >= 3 && ok) {
             for (int cb = half * 32; cb < m_valid; cb += 64) {
                 uint32_t r[32];
-                tmem_load_16(trow + cb, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-                if (cb + 16 < m_valid) tmem_load_16(trow + cb + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-                tmem_load_wait();
+                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
                 if (n < p.N) {
                     uint16_t* cp = p.c + static_cast<int64_t>(m0 + cb) * p.ldc + n;
                     const int cnt = min(32, m_valid - cb);
@@ -345,8 +401,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const bool vec = rows_per <= kRedVecMaxRows;
     const int stride = red_stride(rows_per);
     if (!p.recv_dedicated) cluster_sync();
-    if (threadIdx.x == 64) MXFP4_PHASE(7);
-    if (warp >= 2 && ok) {
+    if (threadIdx.x == 96) MXFP4_PHASE(7);
+    if (warp >= 3 && ok) {
         const uint32_t recv_addr = smem_addr(sRecv);
         // this source's slot in an owner: [n][stride] (vector form) or [row][n] (row form)
         const uint32_t own_off = vec ? static_cast<uint32_t>((split * kTileN + nl) * stride) * 4u
@@ -354,9 +410,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         const uint32_t row_step = vec ? 4u : kTileN * 4u;   // bytes from one token row to the next
         for (int cb = half * 32; cb < m_valid; cb += 64) {
             uint32_t r[32];
-            tmem_load_16(trow + cb, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-            if (cb + 16 < m_valid) tmem_load_16(trow + cb + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-            tmem_load_wait();
+            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
             int owner = cb / rows_per;
             int lm = cb - owner * rows_per;
             uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
@@ -391,17 +445,17 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             }
         }
     }
-    if (threadIdx.x == 64) MXFP4_PHASE(8);
+    if (threadIdx.x == 96) MXFP4_PHASE(8);
     __syncwarp();
     tc_fence_before_sync();
     cluster_sync();
-    if (threadIdx.x == 64) MXFP4_PHASE(9);
+    if (threadIdx.x == 96) MXFP4_PHASE(9);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
-    if (warp >= 2) {
-        const int et = threadIdx.x - 64;
+    if (warp >= 3) {
+        const int et = threadIdx.x - 96;
         const int nrows = r1 - r0;
         if (vec) {
             // owner, vector form: a thread sums 4 consecutive rows of one column
