@@ -51,6 +51,13 @@ __host__ __device__ inline size_t red_recv_floats(int rows_per, int splits) {
                                       : static_cast<size_t>(splits) * rows_per * 128;
 }
 
+// Fused path: bytes from one staged bf16 token row to the next. 16 bytes beyond the row's
+// atoms_max * 256 values move consecutive rows four banks apart, so eight threads reading the
+// same 1x32 block of eight consecutive rows hit distinct banks.
+__host__ __device__ inline uint32_t raw_pitch(int atoms_max) {
+    return static_cast<uint32_t>(atoms_max) * kAtomK * 2u + 16u;
+}
+
 __host__ __device__ inline uint32_t swz_chunk_offset(uint32_t r, uint32_t c) {
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }

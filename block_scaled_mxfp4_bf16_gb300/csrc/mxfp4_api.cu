@@ -72,7 +72,7 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     const size_t bar_bytes = 256;
     const size_t budget = kSmemLimit - 1024 - bar_bytes;
     // fused: every atom's token block and the bf16 A slice of the real rows stay resident
-    const size_t raw_bytes = p.path == 1 ? static_cast<size_t>(p.raw_rows) * p.atoms_max * kAtomK * 2 : 0;
+    const size_t raw_bytes = p.path == 1 ? static_cast<size_t>(p.raw_rows) * raw_pitch(p.atoms_max) : 0;
     size_t fixed = raw_bytes, per_stage = kWBlock;
     if (p.path == 1) fixed += static_cast<size_t>(p.atoms_max) * p.a_block;
     else per_stage += p.a_block;

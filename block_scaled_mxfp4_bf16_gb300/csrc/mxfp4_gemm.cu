@@ -15,14 +15,15 @@
 //   warp 0    : copy producer -- weight blocks (17 KB) and, in the two-kernel path, token
 //               blocks. The first stages are requested before the CTA waits on the previous
 //               grid (the weights never depend on it).
-//   warps 1-2 : tensor-memory allocation and two MMA-issuing threads (alternate 256-K steps, two
-//               accumulators): per 256-K step a thread
-//               copies the scale factors into tensor memory (tcgen05.cp) and issues four
-//               128 x N x 64 block-scaled MMAs.
-//   warps 3-10: in the fused path they quantize the CTA's bf16 token slice (staged in shared
-//               memory by one bulk copy per row) into the token-block layout (the pages'
-//               in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`);
-//               then they move the accumulator out of tensor memory.
+//   warps 1-2 : tensor-memory allocation (warp 1) and two MMA-issuing threads (alternate 256-K
+//               steps, two accumulators): per 256-K step a thread copies the scale factors into
+//               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs. In the
+//               fused path warp 2 first stages the CTA's bf16 token slice in shared memory (one
+//               bulk copy per row).
+//   warps 3-10: in the fused path they quantize that slice into the token-block layout (the
+//               pages' in-register A quantization, submission 711914
+//               `mxfp4_gemm_fused_k512_kernel`); then they move the accumulator out of tensor
+//               memory.
 // Reduction: each output row has an owner CTA in the cluster; the K slices post their fp32 rows
 // into the owner's shared memory, and after a cluster barrier the owner sums them in slice
 // order (run-to-run identical) and stores bf16 C.
@@ -133,15 +134,16 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const int r1 = min(m_valid, r0 + rows_per);
     // fused path: this CTA's bf16 A slice, rows of kslice elements
     const int kslice = min(na * kAtomK, p.K - a0 * kAtomK);
-    const uint32_t raw_row = static_cast<uint32_t>(p.atoms_max) * kAtomK * 2u;   // bytes per staged row
+    const uint32_t raw_row = raw_pitch(p.atoms_max);   // bytes from one staged row to the next
 
     if (threadIdx.x == 0) MXFP4_PHASE(0);
+    if (threadIdx.x == 0) MXFP4_TRACE_SM(12);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(a_full, kEpiThreads);
+        mbar_init(a_full, kEpiWarps);
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
         mbar_init(a_raw, 1);
         flags[0] = 0u;
@@ -165,21 +167,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
             }
-            if (p.fused)   // warm L2 with this CTA's A rows while the previous grid finishes
-                for (int r = 0; r < m_valid; ++r)
-                    prefetch_l2_bulk(p.a + static_cast<int64_t>(m0 + r) * p.lda + a0 * kAtomK,
-                                     static_cast<uint32_t>(kslice) * 2u);
             MXFP4_PHASE(1);
-            pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
-            MXFP4_PHASE(2);
-            if (p.fused) {
-                // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip
-                const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
-                mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
-                for (int r = 0; r < m_valid; ++r)
-                    bulk_load(smem + p.off_araw + r * raw_row,
-                              p.a + static_cast<int64_t>(m0 + r) * p.lda + a0 * kAtomK, row_bytes, a_raw, pol_a);
-            } else {
+            if (!p.fused) {
+                pdl_wait_prior_grid();   // the token blocks may be written by the previous grid
+                MXFP4_PHASE(2);
                 for (int j = 0; j < npro; ++j)
                     bulk_load(sA + j * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[j], pol_a);
             }
@@ -196,7 +187,6 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             // never leave copies in flight into shared memory that is about to be reused or freed
             for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
-            if (p.fused) mbar_wait(a_raw, 0, lim);
         }
     } else if (warp <= 2) {
         // ------------------------------------------------------------------- MMA issuers
@@ -216,6 +206,22 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             named_barrier_arrive(3, 64);
             named_barrier_arrive(1, 32 + kEpiThreads);
         } else {
+            if (p.fused && lane == 0) {
+                // The fused path's A slice, staged by this warp so that it is requested as soon
+                // as the previous grid is done, while warp 0 may still be issuing weight copies:
+                // warm L2 with the rows, wait for the previous grid (A may be its output), then
+                // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip.
+                const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
+                const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
+                for (int r = 0; r < m_valid; ++r) prefetch_l2_bulk(arow + r * p.lda, row_bytes);
+                pdl_wait_prior_grid();
+                MXFP4_PHASE(2);
+                mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
+                for (int r = 0; r < m_valid; ++r)
+                    bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw,
+                              policy_evict_last());
+            }
+            __syncwarp();
             named_barrier(3, 64);
         }
         __syncwarp();
@@ -281,12 +287,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             if (!mok) fail(p, flags);
             tc_commit(acc_full);
         }
+        // never leave the A copy in flight into shared memory that is about to be freed
+        if (warp == 2 && p.fused && lane == 0) mbar_wait(a_raw, 0, lim);
     } else {
         // -------------------------------------------------------------------- warps 3..10
         const int et = threadIdx.x - 96;
         if (p.fused) {
             // Quantize the staged bf16 slice into token blocks in shared memory, one 1x32 block
-            // per item; rows past M and K past the end become zeros.
+            // per item; K past the end becomes zero codes and scales.
             const bool got = mbar_wait(a_raw, 0, lim);
             if (et == 0) MXFP4_PHASE(10);
             if (!got) fail(p, flags);
@@ -299,9 +307,11 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 int rr[2], kk[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
+                    // rows run fastest: eight consecutive items read eight rows (distinct banks)
+                    // and write eight rows of one chunk column (distinct swizzled chunks)
                     const int idx = first + u * kEpiThreads;
-                    rr[u] = idx < total ? idx / nblk : 0;
-                    kk[u] = idx < total ? idx - rr[u] * nblk : kblk;     // kblk: nothing to read
+                    kk[u] = idx < total ? idx / m_valid : kblk;        // kblk: nothing to read
+                    rr[u] = idx < total ? idx - kk[u] * m_valid : 0;
                     if (kk[u] < kblk) {
                         const uint4* src = reinterpret_cast<const uint4*>(
                             reinterpret_cast<const uint8_t*>(sAraw) + rr[u] * raw_row + kk[u] * 64);
@@ -330,19 +340,12 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                     blk[a_rows + block_sf_offset(static_cast<uint32_t>(rr[u]), c)] = static_cast<uint8_t>(sbyte[u]);
                 }
             }
-            // rows past M (or all rows if the A slice never arrived): zero codes and scales
-            const int first_pad = got ? m_valid : 0;
-            const int pad_total = (p.m_tile - first_pad) * nblk;
-            for (int idx = et; idx < pad_total; idx += kEpiThreads) {
-                const int r = first_pad + idx / nblk;
-                const int kb = idx % nblk;
-                const uint32_t c = static_cast<uint32_t>(kb & 7);
-                uint8_t* blk = sA + (kb >> 3) * a_block;
-                *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(r), c)) = make_uint4(0u, 0u, 0u, 0u);
-                blk[a_rows + block_sf_offset(static_cast<uint32_t>(r), c)] = 0;
-            }
+            // Rows past M are left as they are: a token row only feeds its own accumulator column,
+            // and columns past M are never stored.
+            if (et == 0) MXFP4_PHASE(13);
             fence_proxy_async_smem();
-            mbar_arrive(a_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);   // one arrival per warp
         }
         const bool waited = mbar_wait(acc_full, 0, lim);
         if (et == 0) MXFP4_PHASE(6);

@@ -10,8 +10,10 @@
 // compiles to nothing.
 #ifdef MXFP4_TRACE
 #define MXFP4_PHASE(slot) (::mxfp4::trace_buffer[blockIdx.x % 4096][(slot)] = ::mxfp4::global_timer_ns())
+#define MXFP4_TRACE_SM(slot) (::mxfp4::trace_buffer[blockIdx.x % 4096][(slot)] = ::mxfp4::sm_id())
 #else
 #define MXFP4_PHASE(slot) ((void)0)
+#define MXFP4_TRACE_SM(slot) ((void)0)
 #endif
 
 namespace mxfp4 {
@@ -22,6 +24,12 @@ static __device__ unsigned long long trace_buffer[4096][16];
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
