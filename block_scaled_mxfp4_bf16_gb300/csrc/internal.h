@@ -85,6 +85,10 @@ struct GemmPlan {
     // off_recv (over the pipeline buffers unless recv_dedicated), barriers at off_bar
     uint32_t off_a, off_araw, off_recv, off_bar;
     int recv_dedicated;
+    // split-K by bulk copies: each CTA stages its fp32 tile [row][n] at off_stage (inside the
+    // pipeline buffers, clear of the receive buffer) and copies each owner's rows in one piece
+    int red_bulk;
+    uint32_t off_stage;
     size_t smem_bytes;
     uint32_t tmem_cols;
     size_t ws_total;   // workspace: the two-kernel path's token blocks [m_tiles][k_atoms][a_block]
@@ -102,6 +106,8 @@ struct GemmArgs {
     int m_tile, nmc, m_tiles, n_tiles, splits, k_atoms, stages, atoms_max, issuers;
     uint32_t a_block, off_a, off_araw, off_recv, off_bar;
     int recv_dedicated;
+    int red_bulk;
+    uint32_t off_stage;
     uint32_t tmem_cols;
     int fused;
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)

@@ -101,6 +101,7 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     const size_t end_dedicated = align_up(end + recv_bytes, 1024);
     const size_t end_shared = std::max(end, align_up(recv_bytes, 1024));
     // a dedicated buffer saves a cluster barrier; giving up a co-resident CTA costs more
+    const size_t pipe_end = end;   // pipeline buffers (and the fused path's A) end here
     if (p.splits > 1 && end_dedicated <= budget && (fits(end_dedicated, per_sm) || !fits(end_shared, per_sm))) {
         p.recv_dedicated = 1;       // peers may post while this CTA still runs MMAs
         p.off_recv = static_cast<uint32_t>(end);
@@ -109,6 +110,19 @@ static int plan_layout(GemmPlan& p, int max_stages) {
         p.recv_dedicated = 0;       // over the pipeline buffers, written once every MMA is done
         p.off_recv = 0;
         end = end_shared;
+    }
+    // Long runs of owned rows (the row form) go as one bulk copy per owner from a staged tile;
+    // the tile [m_tile][128] fp32 sits in the pipeline buffers, after the receive buffer when
+    // that shares them.
+    p.red_bulk = 0;
+    p.off_stage = 0;
+    if (p.splits > 1 && red_rows_per(p.m_tile, p.splits) > kRedVecMaxRows) {
+        const size_t stage_bytes = static_cast<size_t>(p.m_tile) * kTileN * sizeof(float);
+        const size_t at = p.recv_dedicated ? 0 : align_up(recv_bytes, 1024);
+        if (at + stage_bytes <= pipe_end) {
+            p.red_bulk = 1;
+            p.off_stage = static_cast<uint32_t>(at);
+        }
     }
     // no more CTAs per SM than tensor memory serves: pad shared memory so a further one cannot fit
     const size_t floor_bytes = sm_smem / (per_sm + 1) + 1;
@@ -177,10 +191,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     // Automatic: as many K slices as fill the SMs (within the portable cluster size), fewer if
     // that many clusters would not all be resident at once.
     // A split must buy more than its reduction costs: with few output tiles (under a quarter of
-    // the SMs) each slice keeps at least two 256-K steps, otherwise at least eight (measured on
-    // the 32x4096x512, 64x7168x2048 and 256x4096x7168 workloads).
+    // the SMs) each slice keeps at least two 256-K steps; up to a third of the SMs at least
+    // eight; with more tiles than that the SMs a split would add do not pay for the reduction
+    // (measured on the 32x4096x512, 64x7168x2048 and 256x4096x7168 workloads).
     const int64_t fill = std::max<int64_t>(1, sm_count / std::max<int64_t>(1, units));
-    const int64_t by_atoms = units * 4 < sm_count ? p.k_atoms / 2 : p.k_atoms / 8;
+    const int64_t by_atoms = units * 4 < sm_count ? p.k_atoms / 2 : (units * 3 <= sm_count ? p.k_atoms / 8 : 1);
     const int s_max = static_cast<int>(std::min<int64_t>({fill, std::max<int64_t>(1, by_atoms),
                                                           static_cast<int64_t>(kAutoMaxSplits)}));
     for (int s = s_max; s >= 1; --s) {
@@ -242,6 +257,8 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     g.a_block = plan.a_block;
     g.off_a = plan.off_a;
     g.off_araw = plan.off_araw;
+    g.red_bulk = plan.red_bulk;
+    g.off_stage = plan.off_stage;
     g.off_recv = plan.off_recv;
     g.recv_dedicated = plan.recv_dedicated;
     g.off_bar = plan.off_bar;

@@ -24,9 +24,10 @@
 //               pages' in-register A quantization, submission 711914
 //               `mxfp4_gemm_fused_k512_kernel`); then they move the accumulator out of tensor
 //               memory.
-// Reduction: each output row has an owner CTA in the cluster; the K slices post their fp32 rows
-// into the owner's shared memory, and after a cluster barrier the owner sums them in slice
-// order (run-to-run identical) and stores bf16 C.
+// Reduction: each output row has an owner CTA in the cluster; the K slices send their fp32 rows
+// into the owner's shared memory -- short runs as posted remote stores followed by a cluster
+// barrier, long runs as one bulk copy per owner counted on the owner's mbarrier -- and the
+// owner sums them in slice order (run-to-run identical) and stores bf16 C.
 // Every wait on an mbarrier is bounded; on timeout the kernel records an error in the device
 // status word and unwinds (outputs undefined, no hang, tensor memory released).
 #include <cuda_bf16.h>
@@ -106,7 +107,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint64_t* a_full = empty + kMaxStages;
     uint64_t* acc_full = a_full + 1;
     uint64_t* a_raw = acc_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_raw + 1);
+    uint64_t* red_bar = a_raw + 1;                // bulk split-K: the peers' rows have landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
     volatile uint32_t* flags = tmem_slot + 1;    // [0] abort
 
     const int warp = threadIdx.x >> 5;
@@ -146,10 +148,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         mbar_init(a_full, kEpiWarps);
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
         mbar_init(a_raw, 1);
+        mbar_init(red_bar, 1);
+        if (S > 1 && p.red_bulk && r1 > r0)   // (S - 1) peers x owned rows x 512 bytes
+            mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * (r1 - r0)) * kTileN * 4u);
         flags[0] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
+    if (S > 1 && p.red_bulk) cluster_arrive_relaxed();   // waited for before the first copy to a peer
     pdl_launch_dependents();
     uint32_t tmem_base = 0;
     bool ok = true;
@@ -401,6 +407,91 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // sources in rank order (run-to-run identical) and stores bf16.
     // Without a dedicated receive buffer a first barrier makes sure every peer's MMAs are done
     // before its pipeline buffers are overwritten.
+    if (p.red_bulk) {
+        // Long runs: every CTA stages its fp32 tile [row][n] in its own shared memory, then one
+        // bulk copy per owner moves that owner's rows into the owner's receive buffer, counted
+        // on the owner's red_bar. An owner sums its own staged rows and the received ones in
+        // rank order; a last cluster barrier (reached by owners only once their rows are in)
+        // keeps every CTA resident until no copy reads or writes its shared memory.
+        float* sStage = reinterpret_cast<float*>(smem + p.off_stage);
+        if (threadIdx.x == 96) MXFP4_PHASE(7);
+        if (warp >= 3 && ok) {
+            for (int cb = half * 32; cb < m_valid; cb += 64) {
+                uint32_t r[32];
+                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                const int cnt = min(32, m_valid - cb);
+                float* dst = sStage + cb * kTileN + nl;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < cnt) dst[i * kTileN] = __uint_as_float(r[i]);
+            }
+            fence_proxy_async_smem();   // the copies read the staged tile through the async proxy
+        }
+        if (threadIdx.x == 96) MXFP4_PHASE(8);
+        __syncwarp();
+        cluster_wait();                            // every peer has initialized its red_bar
+        if (!p.recv_dedicated) cluster_sync();     // and is done with the buffers it receives in
+        tc_fence_before_sync();
+        __syncthreads();                           // the staged tile is complete; TMEM reads done
+        if (warp == 1) {
+            tc_fence_after_sync();
+            tmem_dealloc(tmem_base, p.tmem_cols);
+        }
+        if (threadIdx.x == 96 && ok) {
+            const uint32_t slot_off = smem_addr(sRecv) + static_cast<uint32_t>(split * rows_per) * kTileN * 4u;
+            for (int o = 0; o < S; ++o) {
+                const int o0 = min(m_valid, o * rows_per), o1 = min(m_valid, o0 + rows_per);
+                if (o == split || o1 <= o0) continue;
+                bulk_copy_to_peer(map_to_rank(slot_off, static_cast<uint32_t>(o)), sStage + o0 * kTileN,
+                                  static_cast<uint32_t>(o1 - o0) * kTileN * 4u,
+                                  map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(o)));
+            }
+        }
+        const bool owner = warp >= 3 && r1 > r0;
+        if (owner && !mbar_wait_cluster(red_bar, 0, lim)) fail(p, flags);
+        __syncwarp();
+        cluster_arrive();
+        if (threadIdx.x == 96) MXFP4_PHASE(9);
+        if (owner) {
+            const int et = threadIdx.x - 96;
+            const int nrows = r1 - r0;
+            const int nl4 = (et & 31) * 4;
+            const int n4 = n0 + nl4;
+            const bool v4 = p.c_vec4 && n4 + 3 < p.N;
+            for (int lm = et >> 5; lm < nrows; lm += kEpiWarps) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int src = 0; src < S; ++src) {
+                    const float* row = src == split ? sStage + (r0 + lm) * kTileN
+                                                    : sRecv + (src * rows_per + lm) * kTileN;
+                    const float4 v = *reinterpret_cast<const float4*>(row + nl4);
+                    if (src == 0) {
+                        acc = v;
+                    } else {
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                        acc.w += v.w;
+                    }
+                }
+                uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
+                const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
+                if (v4) {
+                    *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
+                } else {
+                    const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                           static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (n4 + t < p.N) crow[n4 + t] = h[t];
+                }
+            }
+            if (et == 0) MXFP4_PHASE(11);
+        }
+        __syncwarp();
+        cluster_wait();
+        return;
+    }
+
     const bool vec = rows_per <= kRedVecMaxRows;
     const int stride = red_stride(rows_per);
     if (!p.recv_dedicated) cluster_sync();

@@ -84,18 +84,21 @@ def test_gemm_outlier_workload_full_oracle_both_paths():
         check_tolerance(c, oracle_c(a, bq, bs), f"{w.name} path {path}")
 
 
-def test_gemm_run_to_run_identical():
+@pytest.mark.parametrize("name,path,splits", [("M8_N2112_K7168", 0, 0), ("M256_N4096_K7168", 2, 2)])
+def test_gemm_run_to_run_identical(name, path, splits):
+    # split-K sums in a fixed order: short runs (posted stores) and long runs (bulk copies)
     mx = _mx()
-    w = workloads.by_name("M8_N2112_K7168")
+    w = workloads.by_name(name)
     a, b = workloads.make_inputs(w, seed=4)
     a, b = a.cuda(), b.cuda()
     bq, bs = mx.mxfp4_quantize(b)
     packed = mx.mxfp4_prepack_b(bq, bs)
-    c1 = mx.mxfp4_gemm(a, packed, w.N).clone()
-    c2 = mx.mxfp4_gemm(a, packed, w.N).clone()
+    c1 = mx.mxfp4_gemm(a, packed, w.N, path=path, splits=splits).clone()
+    c2 = mx.mxfp4_gemm(a, packed, w.N, path=path, splits=splits).clone()
     torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
-    assert mx.mxfp4_gemm_plan(w.M, w.N, w.K)["splits"] > 1
+    assert mx.mxfp4_gemm_plan(w.M, w.N, w.K, path, splits)["splits"] > 1
 
 
 def test_gemm_empty_and_errors():
