@@ -20,10 +20,10 @@
 //               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs. In the
 //               fused path warp 2 first stages the CTA's bf16 token slice in shared memory (one
 //               bulk copy per row).
-//   warps 3-10: in the fused path they quantize that slice into the token-block layout (the
-//               pages' in-register A quantization, submission 711914
-//               `mxfp4_gemm_fused_k512_kernel`); then they move the accumulator out of tensor
-//               memory.
+//   warps 3-10: the epilogue: they move the accumulator out of tensor memory.
+// In the fused path every warp first quantizes the staged slice into the token-block layout (the
+// pages' in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`): the copy
+// and MMA warps have nothing else to do until those blocks exist.
 // Reduction: each output row has an owner CTA in the cluster; the K slices send their fp32 rows
 // into the owner's shared memory -- short runs as posted remote stores followed by a cluster
 // barrier, long runs as one bulk copy per owner counted on the owner's mbarrier -- and the
@@ -94,13 +94,81 @@ __device__ __forceinline__ void fail(const GemmArgs& p, volatile uint32_t* abort
     *abort_flag = 1u;
 }
 
+// Fused path: what the CTA's threads need to quantize its staged bf16 A slice.
+struct QuantSlice {
+    const uint8_t* raw;    // staged rows, raw_row bytes apart
+    uint8_t* blocks;       // token blocks, one per 256-K step
+    uint32_t raw_row, a_block, a_rows;
+    int m_valid, nblk, kblk;
+    uint64_t* a_raw;       // the staged rows have landed
+    uint64_t* a_full;      // the token blocks are written (one arrival per warp)
+    uint64_t lim;
+};
+
+// Every thread of the CTA takes part (the copy and MMA warps have nothing else to do until the
+// token blocks exist): one 1x32 block per item, items dealt round-robin over the CTA, two per
+// thread per pass so their arithmetic interleaves; K past the end becomes zero codes and scales.
+// Rows past M are left as they are: a token row only feeds its own accumulator column, and
+// columns past M are never stored.
+__device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, const GemmArgs& p,
+                                               volatile uint32_t* abort_flag) {
+    const int warp = qt >> 5, lane = qt & 31;
+    const bool got = mbar_wait(q.a_raw, 0, q.lim);
+    if (qt == 96) MXFP4_PHASE(10);
+    if (lane == 0 && warp >= 3) MXFP4_PHASE(16 + warp - 3);
+    if (!got) fail(p, abort_flag);
+    const int total = got ? q.m_valid * q.nblk : 0;
+    constexpr int nq = kGemmThreads;
+    for (int first = qt; first < total; first += 2 * nq) {
+        uint32_t w[2][16], out[2][4], sbyte[2];
+        int rr[2], kk[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            // rows run fastest: eight consecutive items read eight rows (distinct banks) and
+            // write eight rows of one chunk column (distinct swizzled chunks)
+            const int idx = first + u * nq;
+            kk[u] = idx < total ? idx / q.m_valid : q.kblk;        // kblk: nothing to read
+            rr[u] = idx < total ? idx - kk[u] * q.m_valid : 0;
+            if (kk[u] < q.kblk) {
+                const uint4* src = reinterpret_cast<const uint4*>(q.raw + rr[u] * q.raw_row + kk[u] * 64);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = src[i];
+                    w[u][4 * i + 0] = v.x;
+                    w[u][4 * i + 1] = v.y;
+                    w[u][4 * i + 2] = v.z;
+                    w[u][4 * i + 3] = v.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            out[u][0] = out[u][1] = out[u][2] = out[u][3] = 0u;
+            sbyte[u] = kk[u] < q.kblk ? quantize_block32(w[u], out[u]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (first + u * nq >= total) continue;
+            const uint32_t c = static_cast<uint32_t>(kk[u] & 7);
+            uint8_t* blk = q.blocks + (kk[u] >> 3) * q.a_block;
+            *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(rr[u]), c)) =
+                make_uint4(out[u][0], out[u][1], out[u][2], out[u][3]);
+            blk[q.a_rows + block_sf_offset(static_cast<uint32_t>(rr[u]), c)] = static_cast<uint8_t>(sbyte[u]);
+        }
+    }
+    if (qt == 96) MXFP4_PHASE(13);
+    if (lane == 0 && warp >= 3) MXFP4_PHASE(24 + warp - 3);
+    fence_proxy_async_smem();   // the MMAs read the token blocks through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q.a_full);   // one arrival per warp
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mxfp4_gemm_kernel(const GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* sB = smem;                           // stages x kWBlock
     uint8_t* sA = smem + p.off_a;                 // token blocks: stages (two-kernel) or atoms (fused)
-    const uint16_t* sAraw = reinterpret_cast<const uint16_t*>(smem + p.off_araw);   // fused: bf16 A slice
     float* sRecv = reinterpret_cast<float*>(smem + p.off_recv);   // fp32 rows this CTA reduces / stages
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + kMaxStages;
@@ -137,6 +205,18 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // fused path: this CTA's bf16 A slice, rows of kslice elements
     const int kslice = min(na * kAtomK, p.K - a0 * kAtomK);
     const uint32_t raw_row = raw_pitch(p.atoms_max);   // bytes from one staged row to the next
+    QuantSlice qs;
+    qs.raw = smem + p.off_araw;
+    qs.blocks = sA;
+    qs.raw_row = raw_row;
+    qs.a_block = a_block;
+    qs.a_rows = a_rows;
+    qs.m_valid = m_valid;
+    qs.nblk = na * (kAtomK / 32);
+    qs.kblk = (kslice + 31) / 32;            // blocks of this slice inside K
+    qs.a_raw = a_raw;
+    qs.a_full = a_full;
+    qs.lim = lim;
 
     if (threadIdx.x == 0) MXFP4_PHASE(0);
     if (threadIdx.x == 0) MXFP4_TRACE_SM(12);
@@ -145,7 +225,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(a_full, kEpiWarps);
+        mbar_init(a_full, kGemmThreads / 32);
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
         mbar_init(a_raw, 1);
         mbar_init(red_bar, 1);
@@ -160,15 +240,15 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint32_t tmem_base = 0;
     bool ok = true;
 
+    const uint8_t* bsrc = p.bblk + (static_cast<size_t>(nt) * p.k_atoms + a0) * kWBlock;
+    const uint8_t* asrc = p.ablk + (static_cast<size_t>(mt) * p.k_atoms + a0) * a_block;
+    const uint32_t tx_bytes = kWBlock + (p.fused ? 0u : a_block);
+    const int npro = na < stages ? na : stages;
+    // ------------------------------------------------------------------------ set-up
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------------------------------------------------------- producer
-            const uint8_t* bsrc = p.bblk + (static_cast<size_t>(nt) * p.k_atoms + a0) * kWBlock;
-            const uint8_t* asrc = p.ablk + (static_cast<size_t>(mt) * p.k_atoms + a0) * a_block;
-            const uint32_t tx_bytes = kWBlock + (p.fused ? 0u : a_block);
+            // the first stages of the weight ring
             const uint64_t pol_b = policy_evict_first();
-            const uint64_t pol_a = policy_evict_last();
-            const int npro = na < stages ? na : stages;
             for (int j = 0; j < npro; ++j) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
@@ -178,8 +258,49 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 pdl_wait_prior_grid();   // the token blocks may be written by the previous grid
                 MXFP4_PHASE(2);
                 for (int j = 0; j < npro; ++j)
-                    bulk_load(sA + j * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[j], pol_a);
+                    bulk_load(sA + j * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[j],
+                              policy_evict_last());
             }
+        }
+    } else if (warp == 1) {
+        // Columns are allocated only after the previous grid has finished, so a CTA of this
+        // grid never holds columns a CTA of the previous grid is still waiting for.
+        pdl_wait_prior_grid();
+        tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+        // publish the column base: to warp 2 now (barrier 3), to the epilogue warps once they
+        // are done with the A slice (barrier 1)
+        named_barrier_arrive(3, 64);
+        named_barrier_arrive(1, 32 + kEpiThreads);
+    } else if (warp == 2) {
+        if (p.fused && lane == 0) {
+            // The fused path's A slice, staged by this warp so that it is requested as soon as
+            // the previous grid is done, while warp 0 may still be issuing weight copies: warm L2
+            // with the rows, wait for the previous grid (A may be its output), then the whole
+            // bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip.
+            const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
+            const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
+            for (int r = 0; r < m_valid; ++r) prefetch_l2_bulk(arow + r * p.lda, row_bytes);
+            pdl_wait_prior_grid();
+            MXFP4_PHASE(2);
+            mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
+            for (int r = 0; r < m_valid; ++r)
+                bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw,
+                          policy_evict_last());
+        }
+        __syncwarp();
+        named_barrier(3, 64);
+    }
+    __syncwarp();
+    // Fused path: every warp quantizes (one call site, so the quantizer is inlined once).
+    if (p.fused) quantize_slice(qs, threadIdx.x, p, flags);
+
+    if (warp == 0) {
+        // -------------------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol_b = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
             int issued = npro;
             for (int j = npro; j < na; ++j) {
                 const int s = j % stages;
@@ -200,37 +321,6 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         // alternate 256-K steps into two accumulators, which halves the serial issue chain
         // (the epilogue adds them). With one issuer warp 2 only waits.
         const int issuer = warp - 1;
-        if (warp == 1) {
-            // Columns are allocated only after the previous grid has finished, so a CTA of this
-            // grid never holds columns a CTA of the previous grid is still waiting for.
-            pdl_wait_prior_grid();
-            tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
-            tmem_relinquish();
-            tc_fence_before_sync();
-            // publish the column base: to warp 2 now (barrier 3), to the epilogue warps once
-            // they are done with the A slice (barrier 1)
-            named_barrier_arrive(3, 64);
-            named_barrier_arrive(1, 32 + kEpiThreads);
-        } else {
-            if (p.fused && lane == 0) {
-                // The fused path's A slice, staged by this warp so that it is requested as soon
-                // as the previous grid is done, while warp 0 may still be issuing weight copies:
-                // warm L2 with the rows, wait for the previous grid (A may be its output), then
-                // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip.
-                const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
-                const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
-                for (int r = 0; r < m_valid; ++r) prefetch_l2_bulk(arow + r * p.lda, row_bytes);
-                pdl_wait_prior_grid();
-                MXFP4_PHASE(2);
-                mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
-                for (int r = 0; r < m_valid; ++r)
-                    bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw,
-                              policy_evict_last());
-            }
-            __syncwarp();
-            named_barrier(3, 64);
-        }
-        __syncwarp();
         tc_fence_after_sync();
         tmem_base = *tmem_slot;
         if (lane == 0 && issuer < p.issuers) {
@@ -298,63 +388,9 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     } else {
         // -------------------------------------------------------------------- warps 3..10
         const int et = threadIdx.x - 96;
-        if (p.fused) {
-            // Quantize the staged bf16 slice into token blocks in shared memory, one 1x32 block
-            // per item; K past the end becomes zero codes and scales.
-            const bool got = mbar_wait(a_raw, 0, lim);
-            if (et == 0) MXFP4_PHASE(10);
-            if (!got) fail(p, flags);
-            const int nblk = na * (kAtomK / 32);
-            const int kblk = (kslice + 31) / 32;            // blocks of this slice inside K
-            // real rows, two blocks per thread per pass so their arithmetic interleaves
-            const int total = got ? m_valid * nblk : 0;
-            for (int first = et; first < total; first += 2 * kEpiThreads) {
-                uint32_t w[2][16], out[2][4], sbyte[2];
-                int rr[2], kk[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    // rows run fastest: eight consecutive items read eight rows (distinct banks)
-                    // and write eight rows of one chunk column (distinct swizzled chunks)
-                    const int idx = first + u * kEpiThreads;
-                    kk[u] = idx < total ? idx / m_valid : kblk;        // kblk: nothing to read
-                    rr[u] = idx < total ? idx - kk[u] * m_valid : 0;
-                    if (kk[u] < kblk) {
-                        const uint4* src = reinterpret_cast<const uint4*>(
-                            reinterpret_cast<const uint8_t*>(sAraw) + rr[u] * raw_row + kk[u] * 64);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 v = src[i];
-                            w[u][4 * i + 0] = v.x;
-                            w[u][4 * i + 1] = v.y;
-                            w[u][4 * i + 2] = v.z;
-                            w[u][4 * i + 3] = v.w;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    out[u][0] = out[u][1] = out[u][2] = out[u][3] = 0u;
-                    sbyte[u] = kk[u] < kblk ? quantize_block32(w[u], out[u]) : 0u;
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (first + u * kEpiThreads >= total) continue;
-                    const uint32_t c = static_cast<uint32_t>(kk[u] & 7);
-                    uint8_t* blk = sA + (kk[u] >> 3) * a_block;
-                    *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(rr[u]), c)) =
-                        make_uint4(out[u][0], out[u][1], out[u][2], out[u][3]);
-                    blk[a_rows + block_sf_offset(static_cast<uint32_t>(rr[u]), c)] = static_cast<uint8_t>(sbyte[u]);
-                }
-            }
-            // Rows past M are left as they are: a token row only feeds its own accumulator column,
-            // and columns past M are never stored.
-            if (et == 0) MXFP4_PHASE(13);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_full);   // one arrival per warp
-        }
         const bool waited = mbar_wait(acc_full, 0, lim);
         if (et == 0) MXFP4_PHASE(6);
+        if (lane == 0) MXFP4_PHASE(32 + warp - 3);
         named_barrier(1, 32 + kEpiThreads);       // the column base from warp 1
         tc_fence_after_sync();
         tmem_base = *tmem_slot;
@@ -540,6 +576,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         }
     }
     if (threadIdx.x == 96) MXFP4_PHASE(8);
+    if (warp >= 3 && lane == 0) MXFP4_PHASE(40 + warp - 3);
     __syncwarp();
     tc_fence_before_sync();
     cluster_sync();
