@@ -12,14 +12,13 @@
 //
 // One CTA = one (weight tile of 128 rows, token tile, K slice); the K slices of one output tile
 // form one thread-block cluster. Warp roles:
-//   warp 0    : copy producer -- weight blocks (17 KB) and, in the two-kernel path, token
-//               blocks. The first stages are requested before the CTA waits on the previous
-//               grid (the weights never depend on it).
+//   warp 0    : copy producer -- weight blocks (17 KB), the fused path's bf16 A slice (one
+//               bulk copy per row) or the two-kernel path's token blocks. The first weight
+//               stages are requested before the CTA waits on the previous grid (the weights never
+//               depend on it).
 //   warps 1-2 : tensor-memory allocation (warp 1) and two MMA-issuing threads (alternate 256-K
 //               steps, two accumulators): per 256-K step a thread copies the scale factors into
-//               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs. In the
-//               fused path warp 2 first stages the CTA's bf16 token slice in shared memory (one
-//               bulk copy per row).
+//               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs.
 //   warps 3-10: the epilogue: they move the accumulator out of tensor memory.
 // In the fused path every warp first quantizes the staged slice into the token-block layout (the
 // pages' in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`): the copy
@@ -48,20 +47,6 @@ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t n_mma) {
          | ((n_mma >> 3) << 17)             // N / 8
          | (1u << 23)                       // scale factor type UE8M0
          | ((uint32_t(kTileN) >> 4) << 24); // M / 16
-}
-
-// OR of a predicate over the epilogue warps (named barrier 2).
-__device__ __forceinline__ bool any_of_epilogue(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred p, 2, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "n"(kEpiThreads)
-        : "memory");
-    return r != 0;
 }
 
 // Two fp32 -> two bf16 (round to nearest even) in one word, `lo` in the low half.
@@ -247,16 +232,31 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // ------------------------------------------------------------------------ set-up
     if (warp == 0) {
         if (lane == 0) {
-            // the first stages of the weight ring
+            // The weight ring's first stages go before the dependency wait (the weights never
+            // depend on the previous grid). In the fused path only two: the A slice is the first
+            // thing the CTA needs once the wait returns, and copies leave in issue order.
             const uint64_t pol_b = policy_evict_first();
-            for (int j = 0; j < npro; ++j) {
+            const int nfirst = p.fused ? min(npro, 2) : npro;
+            for (int j = 0; j < nfirst; ++j) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
             }
             MXFP4_PHASE(1);
-            if (!p.fused) {
-                pdl_wait_prior_grid();   // the token blocks may be written by the previous grid
-                MXFP4_PHASE(2);
+            pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
+            MXFP4_PHASE(2);
+            if (p.fused) {
+                // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip
+                const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
+                const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
+                mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
+                for (int r = 0; r < m_valid; ++r)
+                    bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw,
+                              policy_evict_last());
+                for (int j = nfirst; j < npro; ++j) {
+                    mbar_arrive_expect_tx(&full[j], tx_bytes);
+                    bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
+                }
+            } else {
                 for (int j = 0; j < npro; ++j)
                     bulk_load(sA + j * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[j],
                               policy_evict_last());
@@ -274,23 +274,16 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         named_barrier_arrive(3, 64);
         named_barrier_arrive(1, 32 + kEpiThreads);
     } else if (warp == 2) {
-        if (p.fused && lane == 0) {
-            // The fused path's A slice, staged by this warp so that it is requested as soon as
-            // the previous grid is done, while warp 0 may still be issuing weight copies: warm L2
-            // with the rows, wait for the previous grid (A may be its output), then the whole
-            // bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip.
-            const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
-            const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
-            for (int r = 0; r < m_valid; ++r) prefetch_l2_bulk(arow + r * p.lda, row_bytes);
-            pdl_wait_prior_grid();
-            MXFP4_PHASE(2);
-            mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
-            for (int r = 0; r < m_valid; ++r)
-                bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw,
-                          policy_evict_last());
-        }
-        __syncwarp();
         named_barrier(3, 64);
+    } else if (p.fused) {
+        // Warm L2 with the CTA's A rows while the previous grid finishes (plain prefetches from
+        // the idle epilogue warps: they do not queue in front of the bulk copies).
+        const int lines = (kslice * 2 + 127) / 128;
+        const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
+        for (int i = threadIdx.x - 96; i < m_valid * lines; i += kEpiThreads) {
+            const int r = i / lines;
+            prefetch_l2(arow + static_cast<int64_t>(r) * p.lda + (i - r * lines) * 64);
+        }
     }
     __syncwarp();
     // Fused path: every warp quantizes (one call site, so the quantizer is inlined once).
@@ -314,6 +307,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             // never leave copies in flight into shared memory that is about to be reused or freed
             for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
+            if (p.fused) mbar_wait(a_raw, 0, lim);
         }
     } else if (warp <= 2) {
         // ------------------------------------------------------------------- MMA issuers
@@ -383,20 +377,18 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             if (!mok) fail(p, flags);
             tc_commit(acc_full);
         }
-        // never leave the A copy in flight into shared memory that is about to be freed
-        if (warp == 2 && p.fused && lane == 0) mbar_wait(a_raw, 0, lim);
     } else {
         // -------------------------------------------------------------------- warps 3..10
         const int et = threadIdx.x - 96;
+        named_barrier(1, 32 + kEpiThreads);       // the column base, published by warp 1 long ago
+        tmem_base = *tmem_slot;
         const bool waited = mbar_wait(acc_full, 0, lim);
+        tc_fence_after_sync();
         if (et == 0) MXFP4_PHASE(6);
         if (lane == 0) MXFP4_PHASE(32 + warp - 3);
-        named_barrier(1, 32 + kEpiThreads);       // the column base from warp 1
-        tc_fence_after_sync();
-        tmem_base = *tmem_slot;
         if (!waited) fail(p, flags);
-        // one decision for all epilogue threads (tcgen05.ld is warp-collective)
-        ok = !any_of_epilogue(!waited || flags[0] != 0u);
+        // one decision per warp (tcgen05.ld is warp-collective)
+        ok = !__any_sync(0xffffffffu, !waited || flags[0] != 0u);
     }
 
     // ------------------------------------------------------------------------ output
