@@ -164,7 +164,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
     volatile uint32_t* flags = tmem_slot + 1;    // [0] abort
 
-    const int warp = threadIdx.x >> 5;
+    // The warp index broadcast from lane 0, so the compiler treats it (and the MMA operands
+    // derived from it) as warp-uniform: tcgen05 instructions take their operands from uniform
+    // registers, and operands it cannot prove uniform cost extra instructions at every issue.
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
 
     // ---- work unit: (token tile, weight tile, K slice)
@@ -218,8 +221,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * (r1 - r0)) * kTileN * 4u);
         flags[0] = 0u;
         fence_mbar_init();
+        MXFP4_PHASE(52);
     }
     __syncthreads();
+    if (threadIdx.x == 0) MXFP4_PHASE(53);
     if (S > 1 && p.red_bulk) cluster_arrive_relaxed();   // waited for before the first copy to a peer
     pdl_launch_dependents();
     uint32_t tmem_base = 0;
@@ -371,10 +376,12 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
                 mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
                 tc_commit(&empty[s]);
+                if (j == issuer) MXFP4_PHASE(48 + 2 * issuer);
                 s += p.issuers;
                 while (s >= stages) { s -= stages; phase ^= 1u; }
             }
             if (!mok) fail(p, flags);
+            MXFP4_PHASE(49 + 2 * issuer);
             tc_commit(acc_full);
         }
     } else {

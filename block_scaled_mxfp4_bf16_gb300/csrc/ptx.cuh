@@ -19,7 +19,7 @@
 namespace mxfp4 {
 
 #ifdef MXFP4_TRACE
-static __device__ unsigned long long trace_buffer[4096][48];
+static __device__ unsigned long long trace_buffer[4096][64];
 #endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
