@@ -190,6 +190,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const int rows_per = red_rows_per(m_valid, S);   // multiple of 4
     const int r0 = min(m_valid, split * rows_per);
     const int r1 = min(m_valid, r0 + rows_per);
+    const bool vec = rows_per <= kRedVecMaxRows;   // short runs: 16-byte stores of four tokens
     // fused path: this CTA's bf16 A slice, rows of kslice elements
     const int kslice = min(na * kAtomK, p.K - a0 * kAtomK);
     const uint32_t raw_row = raw_pitch(p.atoms_max);   // bytes from one staged row to the next
@@ -219,13 +220,15 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         mbar_init(red_bar, 1);
         if (S > 1 && p.red_bulk && r1 > r0)   // (S - 1) peers x owned rows x 512 bytes
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * (r1 - r0)) * kTileN * 4u);
+        else if (S > 1 && vec && r1 > r0)     // (S - 1) peers x 128 weight rows x 16 bytes per 4 rows
+            mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * ((r1 - r0 + 3) / 4)) * kTileN * 16u);
         flags[0] = 0u;
         fence_mbar_init();
         MXFP4_PHASE(52);
     }
     __syncthreads();
     if (threadIdx.x == 0) MXFP4_PHASE(53);
-    if (S > 1 && p.red_bulk) cluster_arrive_relaxed();   // waited for before the first copy to a peer
+    if (S > 1 && (p.red_bulk || vec)) cluster_arrive_relaxed();   // waited for before the first post to a peer
     pdl_launch_dependents();
     uint32_t tmem_base = 0;
     bool ok = true;
@@ -527,68 +530,61 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         return;
     }
 
-    const bool vec = rows_per <= kRedVecMaxRows;
     const int stride = red_stride(rows_per);
-    if (!p.recv_dedicated) cluster_sync();
-    if (threadIdx.x == 96) MXFP4_PHASE(7);
-    if (warp >= 3 && ok) {
-        const uint32_t recv_addr = smem_addr(sRecv);
-        // this source's slot in an owner: [n][stride] (vector form) or [row][n] (row form)
-        const uint32_t own_off = vec ? static_cast<uint32_t>((split * kTileN + nl) * stride) * 4u
-                                     : static_cast<uint32_t>(split * rows_per * kTileN + nl) * 4u;
-        const uint32_t row_step = vec ? 4u : kTileN * 4u;   // bytes from one token row to the next
-        for (int cb = half * 32; cb < m_valid; cb += 64) {
-            uint32_t r[32];
-            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
-            int owner = cb / rows_per;
-            int lm = cb - owner * rows_per;
-            uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
-                            static_cast<uint32_t>(lm) * row_step;
-            if (vec) {
+    if (vec) {
+        // Short runs: each source posts its rows as 16-byte st.async stores into the owners'
+        // transposed receive buffers ([source][n][stride]), counted on the owner's red_bar (its
+        // own rows as plain stores). An owner sums as soon as all its bytes are in; no CTA waits
+        // for the others to finish, since only owners receive and they wait for every byte.
+        cluster_wait();                            // every peer has initialized its red_bar
+        if (!p.recv_dedicated) cluster_sync();     // and is done with the buffers it receives in
+        if (threadIdx.x == 96) MXFP4_PHASE(7);
+        if (warp >= 3 && ok) {
+            const uint32_t recv_addr = smem_addr(sRecv);
+            const uint32_t bar_addr = smem_addr(red_bar);
+            const uint32_t own_off = static_cast<uint32_t>((split * kTileN + nl) * stride) * 4u;
+            for (int cb = half * 32; cb < m_valid; cb += 64) {
+                uint32_t r[32];
+                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                int owner = cb / rows_per;
+                int lm = cb - owner * rows_per;
+                uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
+                                static_cast<uint32_t>(lm) * 4u;
+                uint32_t peer_bar = map_to_rank(bar_addr, static_cast<uint32_t>(owner));
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     if (cb + i < m_valid) {   // rows past M in this group of 4 carry padding, never stored
-                        st_cluster_v4(peer, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                        if (owner == split) st_cluster_v4(peer, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                        else st_async_v4(peer, r[i], r[i + 1], r[i + 2], r[i + 3], peer_bar);
                         peer += 16u;
                         lm += 4;
                         if (lm == rows_per) {
                             lm = 0;
                             ++owner;
-                            if (owner < S) peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (cb + i < m_valid) {
-                        st_cluster_f32(peer, __uint_as_float(r[i]));
-                        peer += kTileN * 4u;
-                        if (++lm == rows_per) {
-                            lm = 0;
-                            ++owner;
-                            if (owner < S) peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                            if (owner < S) {
+                                peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                                peer_bar = map_to_rank(bar_addr, static_cast<uint32_t>(owner));
+                            }
                         }
                     }
                 }
             }
         }
-    }
-    if (threadIdx.x == 96) MXFP4_PHASE(8);
-    if (warp >= 3 && lane == 0) MXFP4_PHASE(40 + warp - 3);
-    __syncwarp();
-    tc_fence_before_sync();
-    cluster_sync();
-    if (threadIdx.x == 96) MXFP4_PHASE(9);
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem_base, p.tmem_cols);
-    }
-    if (warp >= 3) {
-        const int et = threadIdx.x - 96;
-        const int nrows = r1 - r0;
-        if (vec) {
-            // owner, vector form: a thread sums 4 consecutive rows of one column
+        if (threadIdx.x == 96) MXFP4_PHASE(8);
+        if (warp >= 3 && lane == 0) MXFP4_PHASE(40 + warp - 3);
+        __syncwarp();
+        tc_fence_before_sync();
+        __syncthreads();                           // own rows visible; TMEM reads done
+        if (warp == 1) {
+            tc_fence_after_sync();
+            tmem_dealloc(tmem_base, p.tmem_cols);
+        }
+        if (warp >= 3 && r1 > r0) {
+            if (!mbar_wait_cluster(red_bar, 0, lim)) fail(p, flags);
+            if (threadIdx.x == 96) MXFP4_PHASE(9);
+            // owner: a thread sums 4 consecutive rows of one column over the sources in rank order
+            const int et = threadIdx.x - 96;
+            const int nrows = r1 - r0;
             const int cn = et & (kTileN - 1);
             const int nn = n0 + cn;
             if (nn < p.N) {
@@ -610,31 +606,74 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                     }
                 }
             }
-        } else {
-            // owner, row form: a thread sums 4 consecutive columns of one row
-            const int nl4 = (et & 31) * 4;
-            const int n4 = n0 + nl4;
-            const bool v4 = p.c_vec4 && n4 + 3 < p.N;
-            for (int lm = et >> 5; lm < nrows; lm += kEpiWarps) {
-                float4 acc = *reinterpret_cast<const float4*>(sRecv + lm * kTileN + nl4);
-                for (int src = 1; src < S; ++src) {
-                    const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * rows_per + lm) * kTileN + nl4);
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-                uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
-                const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
-                if (v4) {
-                    *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
-                } else {
-                    const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                           static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+            if (et == 0) MXFP4_PHASE(11);
+        }
+        return;
+    }
+
+    // Long runs that the bulk form could not stage: posted 4-byte stores along contiguous rows
+    // ([source][row][n], one 128-byte segment per warp store), then one cluster barrier.
+    if (!p.recv_dedicated) cluster_sync();
+    if (threadIdx.x == 96) MXFP4_PHASE(7);
+    if (warp >= 3 && ok) {
+        const uint32_t recv_addr = smem_addr(sRecv);
+        const uint32_t own_off = static_cast<uint32_t>(split * rows_per * kTileN + nl) * 4u;
+        for (int cb = half * 32; cb < m_valid; cb += 64) {
+            uint32_t r[32];
+            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+            int owner = cb / rows_per;
+            int lm = cb - owner * rows_per;
+            uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
+                            static_cast<uint32_t>(lm) * kTileN * 4u;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (n4 + t < p.N) crow[n4 + t] = h[t];
+            for (int i = 0; i < 32; ++i) {
+                if (cb + i < m_valid) {
+                    st_cluster_f32(peer, __uint_as_float(r[i]));
+                    peer += kTileN * 4u;
+                    if (++lm == rows_per) {
+                        lm = 0;
+                        ++owner;
+                        if (owner < S) peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off;
+                    }
                 }
+            }
+        }
+    }
+    if (threadIdx.x == 96) MXFP4_PHASE(8);
+    __syncwarp();
+    tc_fence_before_sync();
+    cluster_sync();
+    if (threadIdx.x == 96) MXFP4_PHASE(9);
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+    if (warp >= 3) {
+        // owner: a thread sums 4 consecutive columns of one row over the sources in rank order
+        const int et = threadIdx.x - 96;
+        const int nrows = r1 - r0;
+        const int nl4 = (et & 31) * 4;
+        const int n4 = n0 + nl4;
+        const bool v4 = p.c_vec4 && n4 + 3 < p.N;
+        for (int lm = et >> 5; lm < nrows; lm += kEpiWarps) {
+            float4 acc = *reinterpret_cast<const float4*>(sRecv + lm * kTileN + nl4);
+            for (int src = 1; src < S; ++src) {
+                const float4 v = *reinterpret_cast<const float4*>(sRecv + (src * rows_per + lm) * kTileN + nl4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            uint16_t* crow = p.c + static_cast<int64_t>(m0 + r0 + lm) * p.ldc;
+            const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
+            if (v4) {
+                *reinterpret_cast<uint2*>(crow + n4) = make_uint2(lo, hi);
+            } else {
+                const uint16_t h[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                       static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (n4 + t < p.N) crow[n4 + t] = h[t];
             }
         }
         if (et == 0) MXFP4_PHASE(11);

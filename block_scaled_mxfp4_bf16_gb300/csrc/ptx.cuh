@@ -238,6 +238,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
 }
 
+// A 16-byte store into another CTA's shared memory that counts its bytes on an mbarrier of
+// that CTA (both addresses from map_to_rank). The stored values come from registers, so the
+// issuing CTA need not stay resident until the store lands.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
 // Bulk copy from this CTA's shared memory into (another CTA's) shared memory of the cluster,
 // counted on an mbarrier of the destination CTA. Addresses 16-byte aligned, bytes % 16 == 0;
 // `dst` and `bar` are map_to_rank addresses.
