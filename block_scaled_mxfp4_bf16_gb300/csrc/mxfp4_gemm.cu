@@ -228,7 +228,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     }
     __syncthreads();
     if (threadIdx.x == 0) MXFP4_PHASE(53);
-    if (S > 1 && (p.red_bulk || vec)) cluster_arrive_relaxed();   // waited for before the first post to a peer
+    // Split-K by st.async or bulk copies: every CTA arrives here once its barriers exist, and each
+    // warp waits (cluster_wait) at a point of its own off the critical path, before any post.
+    const bool cluster_posts = S > 1 && (p.red_bulk || vec);
+    if (cluster_posts) cluster_arrive_relaxed();
     pdl_launch_dependents();
     uint32_t tmem_base = 0;
     bool ok = true;
@@ -317,6 +320,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
             if (p.fused) mbar_wait(a_raw, 0, lim);
         }
+        __syncwarp();
+        if (cluster_posts) cluster_wait();
     } else if (warp <= 2) {
         // ------------------------------------------------------------------- MMA issuers
         // Warp 1 allocates tensor memory; warps 1 and 2 (one thread each) issue the MMAs of
@@ -387,11 +392,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             MXFP4_PHASE(49 + 2 * issuer);
             tc_commit(acc_full);
         }
+        __syncwarp();
+        if (cluster_posts) cluster_wait();
     } else {
         // -------------------------------------------------------------------- warps 3..10
         const int et = threadIdx.x - 96;
         named_barrier(1, 32 + kEpiThreads);       // the column base, published by warp 1 long ago
         tmem_base = *tmem_slot;
+        if (cluster_posts) cluster_wait();         // every peer's red_bar exists (long since)
         const bool waited = mbar_wait(acc_full, 0, lim);
         tc_fence_after_sync();
         if (et == 0) MXFP4_PHASE(6);
@@ -467,8 +475,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         }
         if (threadIdx.x == 96) MXFP4_PHASE(8);
         __syncwarp();
-        cluster_wait();                            // every peer has initialized its red_bar
-        if (!p.recv_dedicated) cluster_sync();     // and is done with the buffers it receives in
+        if (!p.recv_dedicated) cluster_sync();     // every peer is done with the buffers it receives in
         tc_fence_before_sync();
         __syncthreads();                           // the staged tile is complete; TMEM reads done
         if (warp == 1) {
@@ -536,8 +543,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         // transposed receive buffers ([source][n][stride]), counted on the owner's red_bar (its
         // own rows as plain stores). An owner sums as soon as all its bytes are in; no CTA waits
         // for the others to finish, since only owners receive and they wait for every byte.
-        cluster_wait();                            // every peer has initialized its red_bar
-        if (!p.recv_dedicated) cluster_sync();     // and is done with the buffers it receives in
+        if (!p.recv_dedicated) cluster_sync();     // every peer is done with the buffers it receives in
         if (threadIdx.x == 96) MXFP4_PHASE(7);
         if (warp >= 3 && ok) {
             const uint32_t recv_addr = smem_addr(sRecv);
