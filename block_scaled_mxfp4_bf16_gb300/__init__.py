@@ -80,6 +80,8 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_gemm_ex.restype = _int
             L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options)] + [ctypes.POINTER(_int)] * 5
             L.mxfp4_gemm_plan.restype = _int
+            L.mxfp4_gemm_plan_info.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
+            L.mxfp4_gemm_plan_info.restype = _int
             L.mxfp4_device_status.argtypes = [_vp]
             L.mxfp4_device_status.restype = _int
             L.mxfp4_selftest_timeout.argtypes = [_int, _vp]
@@ -201,12 +203,20 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     return c
 
 
+_PLAN_FIELDS = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated",
+                "smem_bytes", "tmem_cols")
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in _PLAN_FIELDS] + [("reserved", ctypes.c_int * 6)]
+
+
 def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> dict:
+    """The plan mxfp4_gemm would run, as a dict of the mxfp4_plan_info fields."""
     L = load_library()
-    out = [ctypes.c_int() for _ in range(5)]
-    _check(L.mxfp4_gemm_plan(M, N, K, _opts(path, splits, m_tile), *[ctypes.byref(o) for o in out]),
-           "mxfp4_gemm_plan")
-    return dict(zip(["path", "splits", "m_tile", "ctas", "stages"], [o.value for o in out]))
+    info = _PlanInfo()
+    _check(L.mxfp4_gemm_plan_info(M, N, K, _opts(path, splits, m_tile), ctypes.byref(info)), "mxfp4_gemm_plan_info")
+    return {name: getattr(info, name) for name in _PLAN_FIELDS}
 
 
 def mxfp4_device_status(stream=None) -> int:

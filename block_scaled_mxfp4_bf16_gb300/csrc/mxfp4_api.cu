@@ -368,6 +368,35 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
     return MXFP4_OK;
 }
 
+int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts, mxfp4_plan_info* info) {
+    if (!info) return MXFP4_ERR_ARG;
+    if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
+    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    DeviceInfo di;
+    int st = device_info(&di);
+    if (st != MXFP4_OK) return st;
+    GemmPlan plan;
+    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
+    if (st != MXFP4_OK) return st;
+    mxfp4_plan_info out = {};
+    out.path = plan.path;
+    out.splits = plan.splits;
+    out.m_tile = plan.m_tile;
+    out.ctas = plan.ctas;
+    out.stages = plan.stages;
+    out.issuers = plan.issuers;
+    // the form every CTA of a full token tile uses (a ragged last tile may post short runs)
+    out.reduction = plan.splits == 1 ? 0
+                    : plan.red_bulk ? 3
+                    : (red_rows_per(plan.m_tile, plan.splits) <= kRedVecMaxRows ? 2 : 1);
+    out.recv_dedicated = plan.splits > 1 ? plan.recv_dedicated : 0;
+    out.smem_bytes = static_cast<int>(plan.smem_bytes);
+    out.tmem_cols = static_cast<int>(plan.tmem_cols);
+    *info = out;
+    return MXFP4_OK;
+}
+
 int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
                   int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts, void* stream) {
     if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;

@@ -156,6 +156,28 @@ size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4
 int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts,
                     int *path, int *splits, int *m_tile, int *ctas, int *stages);
 
+/* Everything the planner decided for one call. */
+typedef struct mxfp4_plan_info {
+    int path;            /* 1: A quantized inside the GEMM; 2: standalone quantize, then the GEMM */
+    int splits;          /* K slices per output tile (= thread-block cluster size) */
+    int m_tile;          /* tokens per tile (the MMA's N) */
+    int ctas;            /* CTAs of the GEMM launch */
+    int stages;          /* weight pipeline stages per CTA */
+    int issuers;         /* MMA-issuing threads per CTA, one tensor-memory accumulator each */
+    int reduction;       /* split-K form: 0 none (one slice); 1 posted 4-byte rows + cluster
+                            barrier; 2 16-byte st.async posts counted on the owner's mbarrier;
+                            3 one bulk shared-memory copy per owner */
+    int recv_dedicated;  /* 1: the receive buffer has shared memory of its own; 0: it lies over
+                            the pipeline buffers (one more cluster barrier before the posts) */
+    int smem_bytes;      /* dynamic shared memory per CTA */
+    int tmem_cols;       /* tensor-memory columns allocated per CTA */
+    int reserved[6];
+} mxfp4_plan_info;
+
+/* The full plan mxfp4_gemm_ex would run (superset of mxfp4_gemm_plan). `info` must not be
+ * NULL. Returns MXFP4_OK or an argument / shape error. */
+int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts, mxfp4_plan_info *info);
+
 /*
  * mxfp4_device_status -- synchronize `stream`, then read and clear the library's device
  * error word for the current device: MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel gave up a

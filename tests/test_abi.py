@@ -62,3 +62,14 @@ def test_no_cpu_fallback_when_cuda_missing(lib):
     buf = ctypes.create_string_buffer(256)
     p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
     assert lib.mxfp4_quantize(p, 1, 32, 32, p, p, None) != 0
+
+
+def test_plan_info_layout_and_null_check(lib):
+    # the binding's struct mirrors mxfp4_plan_info: ten ints and six reserved (64 bytes)
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    assert ctypes.sizeof(mx._PlanInfo) == 64
+    lib.mxfp4_gemm_plan_info.restype = ctypes.c_int
+    lib.mxfp4_gemm_plan_info.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_void_p]
+    assert lib.mxfp4_gemm_plan_info(8, 2112, 7168, None, None) == 1      # MXFP4_ERR_ARG, no device needed
+

@@ -156,3 +156,34 @@ def test_gemm_token_tile_override_vs_oracle(M, N, K, m_tile):
             torch.cuda.synchronize()
             assert mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)["m_tile"] == m_tile
             check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} m_tile {m_tile} path {path} splits {splits}")
+
+
+# One case per split-K form the planner can pick (mxfp4_plan_info.reduction: 1 posted rows,
+# 2 st.async short runs, 3 bulk copies), with and without a dedicated receive buffer, for
+# both paths; the expected form is asserted so a planner change cannot silently drop one.
+REDUCTION_CASES = [
+    # M, N, K, path, splits, (reduction, recv_dedicated)
+    (100, 200, 512, 1, 2, (1, 0)),
+    (100, 200, 768, 2, 2, (1, 0)),
+    (64, 200, 512, 2, 2, (1, 1)),
+    (1, 200, 4096, 1, 12, (2, 0)),
+    (5, 200, 4096, 2, 12, (2, 0)),
+    (1, 200, 512, 1, 2, (2, 1)),
+    (7, 200, 512, 2, 2, (2, 1)),
+    (33, 200, 4096, 1, 2, (3, 0)),
+    (33, 200, 2048, 2, 2, (3, 0)),
+    (33, 200, 512, 1, 2, (3, 1)),
+    (40, 200, 512, 2, 2, (3, 1)),
+]
+
+
+@pytest.mark.parametrize("M,N,K,path,splits,form", REDUCTION_CASES)
+def test_every_split_k_form_vs_oracle(M, N, K, path, splits, form):
+    mx = _mx()
+    plan = mx.mxfp4_gemm_plan(M, N, K, path, splits)
+    assert (plan["reduction"], plan["recv_dedicated"]) == form, plan
+    assert plan["path"] == path and plan["splits"] == splits
+    a = workloads.random_bf16(M, K, seed=M * 31 + K)
+    b = workloads.random_bf16(N, K, seed=N * 37 + K, scale=0.5)
+    c, bq, bs = run_gemm(a, b, path=path, splits=splits, ldc_pad=5)
+    check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} path {path} splits {splits} form {form}")
