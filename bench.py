@@ -31,29 +31,38 @@ sys.path.insert(0, ROOT)
 from block_scaled_mxfp4_bf16_gb300 import workloads  # noqa: E402
 
 METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor roofline"
-# DRAM bytes (read + write) per GEMM launch from one ncu capture (profiles/), valid only for the
-# kernel sources it was taken on: keyed by a hash of csrc/, reported as null once they change.
-MEASURED_TRAFFIC = {"M8_N2112_K7168": (8470272, "8c1650cb5d9d4a15")}
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM launch from one ncu
+# capture (profiles/), valid only for the device code and the launch plan it was taken with (both
+# checked at run time; reported as null otherwise).
+MEASURED_TRAFFIC = {"M8_N2112_K7168": (8470272, "bc3d3336e881e953",
+                                      "path=1,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=2,recv_dedicated=1")}
 HEADLINE = "M8_N2112_K7168"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES_DEFAULT = 126 * 1024 * 1024
 
 
+DEVICE_SOURCES = ("mxfp4_gemm.cu", "mxfp4_quant.cu", "ptx.cuh", "quant_device.cuh", "internal.h")
+
+
 def kernel_source_hash() -> str:
-    import glob
+    """Hash of the device code (the kernels and what they include)."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "block_scaled_mxfp4_bf16_gb300", "csrc", "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(f).encode())
-            with open(f, "rb") as fh:
-                h.update(fh.read())
+    for name in DEVICE_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "block_scaled_mxfp4_bf16_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(name: str):
+def plan_signature(plan: dict) -> str:
+    keys = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated")
+    return ",".join(f"{k}={plan[k]}" for k in keys)
+
+
+def measured_traffic(name: str, plan: dict):
     entry = MEASURED_TRAFFIC.get(name)
-    if entry is None or entry[1] != kernel_source_hash():
+    if entry is None or entry[1] != kernel_source_hash() or entry[2] != plan_signature(plan):
         return None
     return entry[0]
 
@@ -331,7 +340,7 @@ def main():
                    "ctas": main_res["plan"]["ctas"]},
         "tflops": round(w.flops / (t_us * 1e-6) / 1e12, 3),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "traffic": measured_traffic(w.name), "peak_kind": peak_kind,
+                     "frac": round(gbs / peak, 4), "traffic": measured_traffic(w.name, main_res["plan"]), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": w.algorithmic_bytes},
         "e2e": {"value": round(main_res["e2e_us_per_call"], 3), "unit": "us/call",
                 "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},

@@ -79,15 +79,26 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     if (fixed + per_stage > budget) return MXFP4_ERR_SHAPE;
     p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(max_stages), static_cast<size_t>(p.atoms_max),
                                                   (budget - fixed) / per_stage}));
+    // two MMA issuers (one accumulator each) while their columns fit; a 256-token MMA keeps the
+    // tensor core busy from one issuer
+    p.issuers = p.m_tile <= 128 ? std::min(2, p.atoms_max) : 1;
+    auto sf_cols = [&]() { return static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc); };
+    while (p.issuers > 1 && static_cast<uint32_t>(p.issuers * p.m_tile) + sf_cols() > 512u) --p.issuers;
+    // An issuer tells a stage's fills apart only by the parity of its full barrier, so it must
+    // never wait for a stage's next fill before the previous fill of that stage has landed. That
+    // holds when each stage has a single consumer (stages a multiple of the issuers, each issuer
+    // taking every issuers-th step) or when no stage is refilled. Otherwise drop stages to a
+    // multiple of the issuers, or issuers to a divisor of the stages.
+    if (p.atoms_max > p.stages && p.stages % p.issuers != 0) {
+        if (p.stages >= 2 * p.issuers) p.stages -= p.stages % p.issuers;
+        else
+            while (p.stages % p.issuers != 0) --p.issuers;
+    }
     p.off_a = static_cast<uint32_t>(p.stages) * kWBlock;
     const int a_slots = p.path == 1 ? p.atoms_max : p.stages;
     p.off_araw = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
     size_t end = align_up(p.off_araw + raw_bytes, 1024);
-    // two MMA issuers (two accumulators) while their columns fit; a 256-token MMA keeps the
-    // tensor core busy from one issuer
-    p.issuers = (p.m_tile <= 128 && p.atoms_max >= 2) ? 2 : 1;
-    const uint32_t cols = static_cast<uint32_t>(p.issuers * p.m_tile) +
-                          static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc);
+    const uint32_t cols = static_cast<uint32_t>(p.issuers * p.m_tile) + sf_cols();
     p.tmem_cols = 32;
     while (p.tmem_cols < cols) p.tmem_cols <<= 1;
     // CTAs of this kernel that may share an SM: as many as tensor memory holds without any

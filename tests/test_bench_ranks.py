@@ -38,10 +38,14 @@ def test_max_over_ranks_single_process_is_identity():
     assert bench.max_over_ranks(3.5) == 3.5
 
 
-def test_traffic_is_dropped_when_kernel_sources_change(monkeypatch):
+def test_traffic_is_dropped_when_kernel_sources_or_plan_change(monkeypatch):
     import bench
     name = next(iter(bench.MEASURED_TRAFFIC))
-    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, bench.kernel_source_hash()))
-    assert bench.measured_traffic(name) == 123
-    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, "0000000000000000"))
-    assert bench.measured_traffic(name) is None
+    plan = {"path": 1, "splits": 6, "m_tile": 16, "ctas": 102, "stages": 5, "issuers": 2, "reduction": 2,
+            "recv_dedicated": 1}
+    sig = bench.plan_signature(plan)
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, bench.kernel_source_hash(), sig))
+    assert bench.measured_traffic(name, plan) == 123
+    assert bench.measured_traffic(name, dict(plan, splits=5)) is None          # another launch plan
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, "0000000000000000", sig))
+    assert bench.measured_traffic(name, plan) is None                          # other device code

@@ -187,3 +187,28 @@ def test_every_split_k_form_vs_oracle(M, N, K, path, splits, form):
     b = workloads.random_bf16(N, K, seed=N * 37 + K, scale=0.5)
     c, bq, bs = run_gemm(a, b, path=path, splits=splits, ldc_pad=5)
     check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} path {path} splits {splits} form {form}")
+
+
+def test_plan_invariants_over_a_shape_grid():
+    # Planner invariants the kernel relies on, over tiny to large shapes and every option:
+    # a refilled stage has a single MMA issuer (stages % issuers == 0), tensor memory fits one
+    # power-of-two allocation, shared memory fits the opt-in limit.
+    mx = _mx()
+    checked = 0
+    for M in (1, 8, 16, 33, 64, 100, 200, 256, 1000):
+        for K in (256, 1280, 4096, 7168, 16384):
+            for path in (0, 1, 2):
+                for splits in (0, 1, 2, 3, 5):
+                    try:
+                        pl = mx.mxfp4_gemm_plan(M, 2112, K, path, splits)
+                    except Exception:
+                        continue
+                    checked += 1
+                    steps = -(-(-(-K // 256)) // pl["splits"])      # 256-K steps of the longest slice
+                    assert 1 <= pl["issuers"] <= 2, pl
+                    if steps > pl["stages"]:
+                        assert pl["stages"] % pl["issuers"] == 0, (M, K, path, splits, pl)
+                    t = pl["tmem_cols"]
+                    assert 32 <= t <= 512 and t & (t - 1) == 0, pl
+                    assert pl["smem_bytes"] <= 227 * 1024, pl
+    assert checked > 200
