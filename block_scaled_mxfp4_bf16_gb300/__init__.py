@@ -80,6 +80,8 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_gemm_ex.restype = _int
             L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options)] + [ctypes.POINTER(_int)] * 5
             L.mxfp4_gemm_plan.restype = _int
+            L.mxfp4_gemm_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
+            L.mxfp4_gemm_host.restype = _int
             L.mxfp4_gemm_plan_info.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
             L.mxfp4_gemm_plan_info.restype = _int
             L.mxfp4_device_status.argtypes = [_vp]
@@ -201,6 +203,36 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     _check(L.mxfp4_gemm_ex(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
                            ws_ptr, ws_bytes, _opts(path, splits, m_tile), st), "mxfp4_gemm")
     return c
+
+
+def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host: torch.Tensor,
+                    a_dev: torch.Tensor, c_dev: torch.Tensor, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """mxfp4_gemm_host: A and C in (preferably pinned) host memory, device staging buffers a_dev
+    [M, K] and c_dev [M, N] from the caller; asynchronous on `stream`. Returns c_host."""
+    L = load_library()
+    if a_host.is_cuda or c_host.is_cuda:
+        raise ValueError("a_host and c_host must be host tensors")
+    for t, name in ((a_host, "a_host"), (c_host, "c_host"), (a_dev, "a_dev"), (c_dev, "c_dev")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be a 2-D bf16 tensor with unit column stride")
+    _dev(a_dev, "a_dev")
+    _dev(c_dev, "c_dev")
+    M, K = a_host.shape
+    if tuple(a_dev.shape) != (M, K) or a_dev.stride(0) != K or tuple(c_dev.shape) != (M, N) or c_dev.stride(0) != N:
+        raise ValueError("a_dev must be a packed [M, K] and c_dev a packed [M, N] tensor")
+    if tuple(c_host.shape) != (M, N):
+        raise ValueError("c_host must be [M, N]")
+    st = _stream(stream)
+    need = mxfp4_gemm_workspace_size(M, N, K) if M and N else 0
+    if workspace is None:
+        workspace = _workspace(a_dev.device, need, stream)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(L.mxfp4_gemm_host(a_host.data_ptr(), M, K, a_host.stride(0), packed_b.data_ptr(), N, c_host.data_ptr(),
+                             c_host.stride(0), a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st),
+           "mxfp4_gemm_host")
+    return c_host
 
 
 _PLAN_FIELDS = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated",

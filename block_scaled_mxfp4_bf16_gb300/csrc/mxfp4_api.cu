@@ -432,6 +432,35 @@ int mxfp4_gemm(const void* a, int64_t M, int64_t K, int64_t lda, const void* pac
     return mxfp4_gemm_ex(a, M, K, lda, packed_b, N, c, ldc, workspace, ws_bytes, nullptr, stream);
 }
 
+int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
+                    void* c_host, int64_t ldc, void* a_dev, void* c_dev, void* workspace, size_t ws_bytes,
+                    void* stream) {
+    // everything the device-side call checks is checked first, so nothing is copied on an error
+    int st = check_gemm_args(a_dev, M, K, K, packed_b, N, c_dev, N);
+    if (st != MXFP4_OK || M == 0 || N == 0) return st;
+    if (!a_host || !c_host) return MXFP4_ERR_ARG;
+    if (lda < K || ldc < N) return MXFP4_ERR_SHAPE;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MXFP4_OK) return st;
+    GemmPlan plan;
+    st = make_plan(M, N, K, 0, 0, 0, di.sm_count, &plan);
+    if (st != MXFP4_OK) return st;
+    if (plan.ws_total > 0) {
+        if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpy2DAsync(a_dev, static_cast<size_t>(K) * 2, a_host, static_cast<size_t>(lda) * 2,
+                                      static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_dev, N, static_cast<uint8_t*>(workspace), s);
+    if (st != MXFP4_OK) return st;
+    e = cudaMemcpy2DAsync(c_host, static_cast<size_t>(ldc) * 2, c_dev, static_cast<size_t>(N) * 2,
+                          static_cast<size_t>(N) * 2, static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+}
+
 int mxfp4_device_status(void* stream) {
     DeviceInfo di;
     int st = device_info(&di);

@@ -156,6 +156,22 @@ size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4
 int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts,
                     int *path, int *splits, int *m_tile, int *ctas, int *stages);
 
+/*
+ * mxfp4_gemm_host -- mxfp4_gemm for A and C in host memory: on `stream`, copy A (rows of K
+ * elements, row stride lda) into the caller's device buffer a_dev, run mxfp4_gemm into the
+ * caller's device buffer c_dev, and copy C back into c_host (row stride ldc). The call is
+ * asynchronous like mxfp4_gemm: c_host is valid once `stream` has completed, and a_host /
+ * c_host must stay valid until then (page-locked host memory lets the copies overlap other
+ * work; pageable memory works but the copies then block the host).
+ *   a_host : bf16 [M, K], row stride lda (lda >= K); a_dev: device bf16 [M, K] packed
+ *            (row stride K), 16-byte aligned; c_dev: device bf16 [M, N] packed (row stride N);
+ *   packed_b, workspace: as for mxfp4_gemm.
+ * Errors: as mxfp4_gemm, checked before any copy; MXFP4_ERR_CUDA if a copy fails to enqueue.
+ */
+int mxfp4_gemm_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const void *packed_b, int64_t N,
+                    void *c_host, int64_t ldc, void *a_dev, void *c_dev, void *workspace, size_t ws_bytes,
+                    void *stream);
+
 /* Everything the planner decided for one call. */
 typedef struct mxfp4_plan_info {
     int path;            /* 1: A quantized inside the GEMM; 2: standalone quantize, then the GEMM */

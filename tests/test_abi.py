@@ -62,6 +62,17 @@ def test_no_cpu_fallback_when_cuda_missing(lib):
     buf = ctypes.create_string_buffer(256)
     p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
     assert lib.mxfp4_quantize(p, 1, 32, 32, p, p, None) != 0
+    # the host-buffer GEMM refuses too (no device to plan for), before touching any buffer
+    big = ctypes.create_string_buffer(8192)
+    q = ctypes.addressof(big) + (-ctypes.addressof(big)) % 1024
+    lib.mxfp4_gemm_host.restype = ctypes.c_int
+    lib.mxfp4_gemm_host.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_void_p]
+    before = big.raw
+    assert lib.mxfp4_gemm_host(q, 1, 64, 64, q, 16, q + 2048, 16, q + 4096, q + 6144, None, 0, None) != 0
+    assert big.raw == before
 
 
 def test_plan_info_layout_and_null_check(lib):

@@ -212,3 +212,40 @@ def test_plan_invariants_over_a_shape_grid():
                     assert 32 <= t <= 512 and t & (t - 1) == 0, pl
                     assert pl["smem_bytes"] <= 227 * 1024, pl
     assert checked > 200
+
+
+def test_gemm_host_buffers_match_device_call():
+    # mxfp4_gemm_host: strided pinned host A in, strided pinned host C out, bit-identical to the
+    # device call; an undersized workspace is refused before anything is copied.
+    mx = _mx()
+    for M, N, K in ((8, 2112, 7168), (40, 300, 512)):
+        a = workloads.random_bf16(M, K, seed=M + 7)
+        b = workloads.random_bf16(N, K, seed=N + 7)
+        bq, bs = mx.mxfp4_quantize(b.cuda())
+        packed = mx.mxfp4_prepack_b(bq, bs)
+        want = mx.mxfp4_gemm(a.cuda(), packed, N)
+        a_store = torch.zeros(M, K + 64, dtype=torch.bfloat16).pin_memory()
+        a_store[:, :K] = a
+        c_store = torch.full((M, N + 3), 5.0, dtype=torch.bfloat16).pin_memory()
+        a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+        c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        mx.mxfp4_gemm_host(a_store[:, :K], packed, N, c_store[:, :N], a_dev, c_dev)
+        torch.cuda.synchronize()
+        assert mx.mxfp4_device_status() == 0
+        assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16))
+        assert torch.all(c_store[:, N:] == 5.0)
+    # M = 300 needs a workspace (two-kernel path): a one-byte one is refused, C untouched
+    M, N, K = 300, 256, 256
+    need = mx.mxfp4_gemm_workspace_size(M, N, K)
+    assert need > 0
+    a_host = workloads.random_bf16(M, K, seed=3).pin_memory()
+    c_host = torch.full((M, N), 5.0, dtype=torch.bfloat16).pin_memory()
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=4).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    tiny = torch.empty(1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, workspace=tiny)
+    torch.cuda.synchronize()
+    assert torch.all(c_host == 5.0)
