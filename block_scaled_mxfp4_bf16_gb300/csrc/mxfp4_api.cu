@@ -202,11 +202,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     // Automatic: as many K slices as fill the SMs (within the portable cluster size), fewer if
     // that many clusters would not all be resident at once.
     // A split must buy more than its reduction costs: with few output tiles (under a quarter of
-    // the SMs) each slice keeps at least two 256-K steps; up to a third of the SMs at least
-    // eight; with more tiles than that the SMs a split would add do not pay for the reduction
-    // (measured on the 32x4096x512, 64x7168x2048 and 256x4096x7168 workloads).
+    // the SMs) each slice keeps at least two 256-K steps, otherwise at least eight (measured on
+    // the 32x4096x512, 64x7168x2048 and 256x4096x7168 workloads).
     const int64_t fill = std::max<int64_t>(1, sm_count / std::max<int64_t>(1, units));
-    const int64_t by_atoms = units * 4 < sm_count ? p.k_atoms / 2 : (units * 3 <= sm_count ? p.k_atoms / 8 : 1);
+    const int64_t by_atoms = units * 4 < sm_count ? p.k_atoms / 2 : p.k_atoms / 8;
     const int s_max = static_cast<int>(std::min<int64_t>({fill, std::max<int64_t>(1, by_atoms),
                                                           static_cast<int64_t>(kAutoMaxSplits)}));
     for (int s = s_max; s >= 1; --s) {
@@ -451,13 +450,17 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
         if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpy2DAsync(a_dev, static_cast<size_t>(K) * 2, a_host, static_cast<size_t>(lda) * 2,
-                                      static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+    // one linear copy when the host rows are contiguous, a strided one otherwise
+    const size_t a_row = static_cast<size_t>(K) * 2, c_row = static_cast<size_t>(N) * 2;
+    cudaError_t e = lda == K ? cudaMemcpyAsync(a_dev, a_host, a_row * M, cudaMemcpyHostToDevice, s)
+                             : cudaMemcpy2DAsync(a_dev, a_row, a_host, static_cast<size_t>(lda) * 2, a_row,
+                                                 static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
     st = run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_dev, N, static_cast<uint8_t*>(workspace), s);
     if (st != MXFP4_OK) return st;
-    e = cudaMemcpy2DAsync(c_host, static_cast<size_t>(ldc) * 2, c_dev, static_cast<size_t>(N) * 2,
-                          static_cast<size_t>(N) * 2, static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
+    e = ldc == N ? cudaMemcpyAsync(c_host, c_dev, c_row * M, cudaMemcpyDeviceToHost, s)
+                 : cudaMemcpy2DAsync(c_host, static_cast<size_t>(ldc) * 2, c_dev, c_row, c_row,
+                                     static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
 }
 
