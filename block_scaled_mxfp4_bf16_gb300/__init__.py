@@ -82,6 +82,9 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_gemm_plan.restype = _int
             L.mxfp4_gemm_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
             L.mxfp4_gemm_host.restype = _int
+            L.mxfp4_gemm_plan_model.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options), _int,
+                                                ctypes.POINTER(_int), ctypes.POINTER(_PlanInfo)]
+            L.mxfp4_gemm_plan_model.restype = _int
             L.mxfp4_gemm_plan_info.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
             L.mxfp4_gemm_plan_info.restype = _int
             L.mxfp4_device_status.argtypes = [_vp]
@@ -248,6 +251,20 @@ def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_ti
     L = load_library()
     info = _PlanInfo()
     _check(L.mxfp4_gemm_plan_info(M, N, K, _opts(path, splits, m_tile), ctypes.byref(info)), "mxfp4_gemm_plan_info")
+    return {name: getattr(info, name) for name in _PLAN_FIELDS}
+
+
+def mxfp4_gemm_plan_model(M: int, N: int, K: int, sm_count: int, cluster_caps=None, path: int = 0,
+                          splits: int = 0, m_tile: int = 0) -> dict:
+    """The planner alone for a described device (no GPU needed): `cluster_caps` lists, for cluster
+    sizes 1..16, how many clusters can be resident at once (None: no limit)."""
+    L = load_library()
+    info = _PlanInfo()
+    caps = None
+    if cluster_caps is not None:
+        caps = (ctypes.c_int * 17)(0, *[int(c) for c in cluster_caps])
+    _check(L.mxfp4_gemm_plan_model(M, N, K, _opts(path, splits, m_tile), sm_count, caps, ctypes.byref(info)),
+           "mxfp4_gemm_plan_model")
     return {name: getattr(info, name) for name in _PLAN_FIELDS}
 
 

@@ -124,8 +124,10 @@ struct DeviceInfo {
 };
 
 int device_info(DeviceInfo* out);   // MXFP4_OK or an error status
+// cluster_caps: if not null, cluster_caps[s] (s = 1..kMaxSplits) is how many clusters of s CTAs
+// can be resident at once, used instead of asking the current device (no CUDA call is made).
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
-              GemmPlan* plan);
+              GemmPlan* plan, const int* cluster_caps = nullptr);
 size_t packed_b_bytes(int64_t N, int64_t K);
 
 // Kernel launchers (return cudaError_t).

@@ -160,7 +160,7 @@ static int active_clusters(int device, int size, size_t smem) {
 }
 
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
-              GemmPlan* P) {
+              GemmPlan* P, const int* cluster_caps) {
     GemmPlan p = {};
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_SHAPE;
     if (mtile_req < 0 || mtile_req > kMaxMTile || mtile_req % 16 != 0) return MXFP4_ERR_ARG;
@@ -182,7 +182,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     p.path = path_req ? path_req : (M <= 16 ? 1 : 2);
     if (p.path != 1 && p.path != 2) return MXFP4_ERR_ARG;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (!cluster_caps && cudaGetDevice(&dev) != cudaSuccess) dev = 0;
     auto layout_once = [&](GemmPlan& q) { return plan_layout(q, kMaxStages); };
     auto layout = [&](GemmPlan& q) {
         int st = layout_once(q);
@@ -213,7 +213,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
         q.splits = s;
         const int st = layout(q);
         if (st != MXFP4_OK) return st;
-        if (s == 1 || units <= active_clusters(dev, s, q.smem_bytes)) {
+        const int resident = cluster_caps ? cluster_caps[s] : active_clusters(dev, s, q.smem_bytes);
+        if (s == 1 || units <= resident) {
             *P = q;
             return MXFP4_OK;
         }
@@ -285,6 +286,26 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
 using namespace mxfp4;
 
 // ====================================================================== C ABI
+
+// The planner's decisions as the public mxfp4_plan_info.
+static void fill_plan_info(const mxfp4::GemmPlan& plan, mxfp4_plan_info* info) {
+    using namespace mxfp4;
+    mxfp4_plan_info out = {};
+    out.path = plan.path;
+    out.splits = plan.splits;
+    out.m_tile = plan.m_tile;
+    out.ctas = plan.ctas;
+    out.stages = plan.stages;
+    out.issuers = plan.issuers;
+    // the form every CTA of a full token tile uses (a ragged last tile may post short runs)
+    out.reduction = plan.splits == 1 ? 0
+                    : plan.red_bulk ? 3
+                    : (red_rows_per(plan.m_tile, plan.splits) <= kRedVecMaxRows ? 2 : 1);
+    out.recv_dedicated = plan.splits > 1 ? plan.recv_dedicated : 0;
+    out.smem_bytes = static_cast<int>(plan.smem_bytes);
+    out.tmem_cols = static_cast<int>(plan.tmem_cols);
+    *info = out;
+}
 
 extern "C" {
 
@@ -389,21 +410,23 @@ int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_optio
     GemmPlan plan;
     st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
     if (st != MXFP4_OK) return st;
-    mxfp4_plan_info out = {};
-    out.path = plan.path;
-    out.splits = plan.splits;
-    out.m_tile = plan.m_tile;
-    out.ctas = plan.ctas;
-    out.stages = plan.stages;
-    out.issuers = plan.issuers;
-    // the form every CTA of a full token tile uses (a ragged last tile may post short runs)
-    out.reduction = plan.splits == 1 ? 0
-                    : plan.red_bulk ? 3
-                    : (red_rows_per(plan.m_tile, plan.splits) <= kRedVecMaxRows ? 2 : 1);
-    out.recv_dedicated = plan.splits > 1 ? plan.recv_dedicated : 0;
-    out.smem_bytes = static_cast<int>(plan.smem_bytes);
-    out.tmem_cols = static_cast<int>(plan.tmem_cols);
-    *info = out;
+    fill_plan_info(plan, info);
+    return MXFP4_OK;
+}
+
+int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts, int sm_count,
+                          const int* cluster_caps, mxfp4_plan_info* info) {
+    if (!info || sm_count < 1) return MXFP4_ERR_ARG;
+    if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
+    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    int caps[kMaxSplits + 1];
+    for (int s = 0; s <= kMaxSplits; ++s) caps[s] = cluster_caps ? cluster_caps[s] : (1 << 30);
+    GemmPlan plan;
+    const int st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0,
+                             sm_count, &plan, caps);
+    if (st != MXFP4_OK) return st;
+    fill_plan_info(plan, info);
     return MXFP4_OK;
 }
 

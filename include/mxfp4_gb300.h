@@ -195,6 +195,17 @@ typedef struct mxfp4_plan_info {
 int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts, mxfp4_plan_info *info);
 
 /*
+ * mxfp4_gemm_plan_model -- the planner alone, for a device described by its SM count and, for
+ * every cluster size s = 1..16, how many clusters of s CTAs can be resident at once
+ * (cluster_caps[s]; cluster_caps[0] is ignored; NULL means no limit). Makes no CUDA call, so it
+ * works without a GPU. On a device with those properties the plan equals mxfp4_gemm_plan_info's
+ * (the device query there also accounts for each plan's shared memory; on sm_103a the count did
+ * not depend on it). Returns MXFP4_OK or an argument / shape error.
+ */
+int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts, int sm_count,
+                          const int *cluster_caps, mxfp4_plan_info *info);
+
+/*
  * mxfp4_device_status -- synchronize `stream`, then read and clear the library's device
  * error word for the current device: MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel gave up a
  * bounded wait (the kernel then skipped its remaining work and released its resources;

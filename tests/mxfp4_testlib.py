@@ -79,3 +79,22 @@ def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: in
 def oracle_c(a_cpu: torch.Tensor, bq: np.ndarray, bs: np.ndarray) -> np.ndarray:
     aq, as_ = oracle.quantize(workloads.bf16_bits(a_cpu))
     return oracle.mxfp4_gemm_ref(aq, as_, bq, bs)
+
+
+# One case per split-K form the planner can pick (mxfp4_plan_info.reduction: 1 posted rows,
+# 2 st.async short runs, 3 bulk copies), with and without a dedicated receive buffer, for
+# both paths; the expected form is asserted so a planner change cannot silently drop one.
+REDUCTION_CASES = [
+    # M, N, K, path, splits, (reduction, recv_dedicated)
+    (100, 200, 512, 1, 2, (1, 0)),
+    (100, 200, 768, 2, 2, (1, 0)),
+    (64, 200, 512, 2, 2, (1, 1)),
+    (1, 200, 4096, 1, 12, (2, 0)),
+    (5, 200, 4096, 2, 12, (2, 0)),
+    (1, 200, 512, 1, 2, (2, 1)),
+    (7, 200, 512, 2, 2, (2, 1)),
+    (33, 200, 4096, 1, 2, (3, 0)),
+    (33, 200, 2048, 2, 2, (3, 0)),
+    (33, 200, 512, 1, 2, (3, 1)),
+    (40, 200, 512, 2, 2, (3, 1)),
+]

@@ -6,7 +6,8 @@ import torch
 
 import oracle
 from block_scaled_mxfp4_bf16_gb300 import workloads
-from mxfp4_testlib import assert_bytes_equal, bf16_to_f64, check_tolerance, oracle_c, run_gemm, to_np_u8
+from mxfp4_testlib import (REDUCTION_CASES, assert_bytes_equal, bf16_to_f64, check_tolerance, oracle_c,
+                           run_gemm, to_np_u8)
 
 pytestmark = pytest.mark.gpu
 
@@ -156,25 +157,6 @@ def test_gemm_token_tile_override_vs_oracle(M, N, K, m_tile):
             torch.cuda.synchronize()
             assert mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)["m_tile"] == m_tile
             check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} m_tile {m_tile} path {path} splits {splits}")
-
-
-# One case per split-K form the planner can pick (mxfp4_plan_info.reduction: 1 posted rows,
-# 2 st.async short runs, 3 bulk copies), with and without a dedicated receive buffer, for
-# both paths; the expected form is asserted so a planner change cannot silently drop one.
-REDUCTION_CASES = [
-    # M, N, K, path, splits, (reduction, recv_dedicated)
-    (100, 200, 512, 1, 2, (1, 0)),
-    (100, 200, 768, 2, 2, (1, 0)),
-    (64, 200, 512, 2, 2, (1, 1)),
-    (1, 200, 4096, 1, 12, (2, 0)),
-    (5, 200, 4096, 2, 12, (2, 0)),
-    (1, 200, 512, 1, 2, (2, 1)),
-    (7, 200, 512, 2, 2, (2, 1)),
-    (33, 200, 4096, 1, 2, (3, 0)),
-    (33, 200, 2048, 2, 2, (3, 0)),
-    (33, 200, 512, 1, 2, (3, 1)),
-    (40, 200, 512, 2, 2, (3, 1)),
-]
 
 
 @pytest.mark.parametrize("M,N,K,path,splits,form", REDUCTION_CASES)

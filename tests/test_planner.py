@@ -1,0 +1,94 @@
+"""CPU tests of the host planner through mxfp4_gemm_plan_model (no GPU, no CUDA call): the
+plans it picks for the five workloads on a GB300-like device, the invariants the GEMM kernel
+relies on, the split-K form of every case the GPU tests run, and the cluster-residency limit."""
+import pytest
+
+from mxfp4_testlib import REDUCTION_CASES
+
+# GB300: 152 SMs; clusters of s CTAs resident at once, s = 1..16 (cudaOccupancyMaxActiveClusters
+# on the GEMM kernel, the same for 90 KB, 130 KB and 210 KB of shared memory per CTA)
+SM_COUNT = 152
+CLUSTER_CAPS = [152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import block_scaled_mxfp4_bf16_gb300 as m
+    m.load_library()
+    return m
+
+
+def plan(mx, M, N, K, **kw):
+    return mx.mxfp4_gemm_plan_model(M, N, K, SM_COUNT, CLUSTER_CAPS, **kw)
+
+
+@pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
+    (16, 3072, 1536, 1, 3, 16),      # fused A quantization, 72 CTAs
+    (8, 2112, 7168, 1, 6, 16),       # fused, 6-slice clusters, 102 CTAs
+    (32, 4096, 512, 2, 1, 32),       # standalone quantize + GEMM
+    (64, 7168, 2048, 2, 1, 64),
+    (256, 4096, 7168, 2, 2, 128),    # 128-token tiles, 2 slices (bulk split-K)
+])
+def test_workload_plans(mx, M, N, K, path, splits, m_tile):
+    p = plan(mx, M, N, K)
+    assert (p["path"], p["splits"], p["m_tile"]) == (path, splits, m_tile), p
+    m_tiles = -(-M // p["m_tile"])
+    assert p["ctas"] == m_tiles * -(-N // 128) * p["splits"]
+
+
+def test_invariants_over_a_grid(mx):
+    checked = 0
+    for M in (1, 5, 8, 16, 17, 33, 64, 100, 128, 200, 256, 300, 512, 1000, 4096):
+        for N in (128, 2112, 7168):
+            for K in (64, 256, 1280, 4096, 7168, 16384, 65536):
+                for path in (0, 1, 2):
+                    for splits in (0, 1, 2, 3, 5, 8, 16):
+                        try:
+                            p = plan(mx, M, N, K, path=path, splits=splits)
+                        except Exception:
+                            continue
+                        checked += 1
+                        steps = -(-(-(-K // 256)) // p["splits"])     # 256-K steps of the longest slice
+                        assert 1 <= p["issuers"] <= 2 and 1 <= p["stages"] <= 8, p
+                        if steps > p["stages"]:   # refilled stages: one MMA thread per stage
+                            assert p["stages"] % p["issuers"] == 0, (M, N, K, path, splits, p)
+                        t = p["tmem_cols"]
+                        assert 32 <= t <= 512 and t & (t - 1) == 0, p
+                        assert p["smem_bytes"] <= 227 * 1024, p
+                        assert p["m_tile"] % 16 == 0 and 16 <= p["m_tile"] <= 256
+                        assert p["splits"] <= min(16, -(-K // 256))
+                        if splits:
+                            assert p["splits"] == min(splits, -(-K // 256), 16)
+                        if path:
+                            assert p["path"] == path
+                        if p["splits"] == 1:
+                            assert p["reduction"] == 0
+    assert checked > 1500
+
+
+@pytest.mark.parametrize("M,N,K,path,splits,form", REDUCTION_CASES)
+def test_split_k_forms(mx, M, N, K, path, splits, form):
+    p = plan(mx, M, N, K, path=path, splits=splits)
+    assert (p["reduction"], p["recv_dedicated"]) == form, p
+
+
+def test_cluster_residency_limits_the_split(mx):
+    # the headline shape has 17 output tiles: 6-CTA clusters need 17 resident at once
+    caps = list(CLUSTER_CAPS)
+    assert mx.mxfp4_gemm_plan_model(8, 2112, 7168, SM_COUNT, caps)["splits"] == 6
+    caps[5] = 16                     # only 16 clusters of 6 fit: fall back to 5 slices
+    assert mx.mxfp4_gemm_plan_model(8, 2112, 7168, SM_COUNT, caps)["splits"] == 5
+    # without a limit the automatic plan still stays within portable cluster sizes (<= 8)
+    assert mx.mxfp4_gemm_plan_model(1, 128, 65536, SM_COUNT, None)["splits"] <= 8
+
+
+def test_errors(mx):
+    import block_scaled_mxfp4_bf16_gb300 as m
+    with pytest.raises(m.Mxfp4Error):
+        plan(mx, 8, 2112, 7200)          # K not a multiple of 64
+    with pytest.raises(m.Mxfp4Error):
+        plan(mx, 0, 2112, 7168)
+    with pytest.raises(m.Mxfp4Error):
+        mx.mxfp4_gemm_plan_model(8, 2112, 7168, 0, CLUSTER_CAPS)
+    with pytest.raises(m.Mxfp4Error):
+        plan(mx, 8, 2112, 7168, m_tile=24)   # token tile must be a multiple of 16
