@@ -29,7 +29,8 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t
     }
 }
 
-// Token blocks (layout in internal.h): block (mt, j) at (mt * k_atoms + j) * a_block. Items run
+// Token blocks, one lane per 1x32 block (layout in internal.h): block (mt, j) at
+// (mt * k_atoms + j) * a_block. Items run
 // over every (row, block) of the padded [m_tiles*m_tile, k_atoms*256] matrix, so padding rows and
 // the K tail are written as zeros. Four consecutive lanes own the four blocks of one scale word.
 __global__ void __launch_bounds__(256)
@@ -76,6 +77,65 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
     }
 }
 
+// Token blocks (layout in internal.h): block (mt, j) at (mt * k_atoms + j) * a_block; items run
+// over every (row, block) of the padded [m_tiles*m_tile, k_atoms*256] matrix, so padding rows and
+// the K tail are written as zeros. Four lanes per 1x32 block: lane part p of a block loads
+// elements 8p..8p+7 (16 bytes; a warp reads eight consecutive blocks, 512 contiguous bytes), the
+// block's amax is combined over the four lanes, and each lane writes its 4 bytes of codes. The
+// eight blocks of a warp are two scale words (four consecutive blocks of one row each),
+// assembled by shuffles. Shorter per-thread chains than one lane per block: the kernel sits
+// between two GEMMs on the critical path, so its latency is what counts.
+__global__ void __launch_bounds__(256)
+quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
+                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
+    pdl_launch_dependents();
+    const int64_t nblk = K / 32;
+    const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
+    const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
+    const int lane = threadIdx.x & 31;
+    const int part = lane & 3;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    {   // warm L2 with this lane's first 16 bytes while the previous grid finishes (see prefetch_l2)
+        const int64_t it0 = warp_id * 8 + (lane >> 2);
+        const int64_t r = it0 / row_items, kbp = it0 - (it0 / row_items) * row_items;
+        if (it0 < items && r < rows && kbp < nblk) prefetch_l2(x + r * ld + kbp * 32 + part * 8);
+    }
+    pdl_wait_prior_grid();
+    // the loop bound is uniform per warp, so the shuffles below always see all 32 lanes
+    for (int64_t base = warp_id * 8; base < items; base += warps * 8) {
+        const int64_t it = base + (lane >> 2);
+        const int64_t r = it / row_items;
+        const int64_t kbp = it - r * row_items;          // block index within the padded row
+        const bool live = r < rows && kbp < nblk;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (live) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + r * ld + kbp * 32 + part * 8));
+            w[0] = v.x;
+            w[1] = v.y;
+            w[2] = v.z;
+            w[3] = v.w;
+        }
+        uint32_t amax = amax_quarter(w);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int s = scale_exponent(amax << 16);
+        const uint32_t codes = live ? quantize_quarter(w, inv_scale(s)) : 0u;
+        const uint32_t byte = live ? static_cast<uint32_t>(s + 127) : 0u;
+        // scale word of four consecutive blocks: the part-0 lanes 0, 4, 8, 12 (and 16..28)
+        uint32_t word = part == 0 ? byte << (8 * ((lane >> 2) & 3)) : 0u;
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        word |= __shfl_xor_sync(0xffffffffu, word, 8);
+        const int mt = static_cast<int>(r / m_tile);
+        const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
+        const uint32_t c = static_cast<uint32_t>(kbp & 7);
+        uint8_t* blk = blocks + (static_cast<size_t>(mt) * k_atoms + static_cast<size_t>(kbp >> 3)) * a_block;
+        *reinterpret_cast<uint32_t*>(blk + swz_chunk_offset(rr, c) + part * 4) = codes;
+        if ((lane & 15) == 0)
+            *reinterpret_cast<uint32_t*>(blk + static_cast<uint32_t>(m_tile) * 128u + block_sf_offset(rr, c)) = word;
+    }
+}
+
 // Weight prepack: one thread per (row, block) of the padded [n_tiles*128, k_atoms*256] matrix;
 // copies 16 bytes of e2m1 into the swizzled rows and the scale byte into its chunk.
 __global__ void __launch_bounds__(256)
@@ -103,6 +163,8 @@ prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, i
     }
 }
 
+constexpr int64_t kQuantFourLaneMaxBlocks = 16384;
+
 static int grid_for(int64_t items, int threads) {
     int64_t blocks = (items + threads - 1) / threads;
     if (blocks > 65535) blocks = 65535;   // grid-stride loops cover the rest
@@ -121,6 +183,11 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
                                    int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s) {
     const int threads = 256;
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * 8 * k_atoms;
+    // few blocks: four lanes each (shorter chains, the launch is latency-bound); many blocks: one
+    // lane each (less total work; measured faster for 256x7168 and slower for 64x2048)
+    if (items <= kQuantFourLaneMaxBlocks)
+        return launch_pdl(quantize_blocks4_kernel, dim3(grid_for(items * 4, threads)), dim3(threads), 0, s, x, rows,
+                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block);
     return launch_pdl(quantize_blocks_kernel, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K, ld,
                       blocks, m_tile, m_tiles, k_atoms, a_block);
 }

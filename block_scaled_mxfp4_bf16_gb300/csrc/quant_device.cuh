@@ -79,6 +79,27 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&w)[16], ui
     return static_cast<uint32_t>(s + 127);
 }
 
+// A quarter of a 1x32 block: 8 bf16 as 4 words, quantized with the block's scale multiplier m
+// (inv_scale of the block's exponent); returns 4 bytes of packed codes (element 2i in the low
+// nibble of byte i). Same arithmetic per element as quantize_block32.
+__device__ __forceinline__ uint32_t quantize_quarter(const uint32_t (&w)[4], float m) {
+    uint32_t packed = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float even = __fmul_rn(__uint_as_float(w[i] << 16), m);
+        const float odd = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), m);
+        packed |= e2m1x2(even, odd) << (8 * i);
+    }
+    return packed;
+}
+
+// Max |x| bit pattern (as a bf16 in the low half) over 4 words of bf16 pairs.
+__device__ __forceinline__ uint32_t amax_quarter(const uint32_t (&w)[4]) {
+    const uint32_t m = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
+}
+
 // Load 32 consecutive bf16 (64 bytes, 16-byte aligned) as 16 words.
 __device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[16]) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
