@@ -24,9 +24,9 @@
 // pages' in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`): the copy
 // and MMA warps have nothing else to do until those blocks exist.
 // Reduction: each output row has an owner CTA in the cluster; the K slices send their fp32 rows
-// into the owner's shared memory -- short runs as posted remote stores followed by a cluster
-// barrier, long runs as one bulk copy per owner counted on the owner's mbarrier -- and the
-// owner sums them in slice order (run-to-run identical) and stores bf16 C.
+// into the owner's shared memory -- short runs as st.async stores, long runs as one bulk copy per
+// owner, both counted on the owner's mbarrier (where neither fits, posted stores and a cluster
+// barrier) -- and the owner sums them in slice order (run-to-run identical) and stores bf16 C.
 // Every wait on an mbarrier is bounded; on timeout the kernel records an error in the device
 // status word and unwinds (outputs undefined, no hang, tensor memory released).
 #include <cuda_bf16.h>
@@ -97,10 +97,9 @@ struct QuantSlice {
 // columns past M are never stored.
 __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, const GemmArgs& p,
                                                volatile uint32_t* abort_flag) {
-    const int warp = qt >> 5, lane = qt & 31;
+    const int lane = qt & 31;
     const bool got = mbar_wait(q.a_raw, 0, q.lim);
     if (qt == 96) MXFP4_PHASE(10);
-    if (lane == 0 && warp >= 3) MXFP4_PHASE(16 + warp - 3);
     if (!got) fail(p, abort_flag);
     const int total = got ? q.m_valid * q.nblk : 0;
     constexpr int nq = kGemmThreads;
@@ -142,7 +141,6 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
         }
     }
     if (qt == 96) MXFP4_PHASE(13);
-    if (lane == 0 && warp >= 3) MXFP4_PHASE(24 + warp - 3);
     fence_proxy_async_smem();   // the MMAs read the token blocks through the async proxy
     __syncwarp();
     if (lane == 0) mbar_arrive(q.a_full);   // one arrival per warp
@@ -160,7 +158,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint64_t* a_full = empty + kMaxStages;
     uint64_t* acc_full = a_full + 1;
     uint64_t* a_raw = acc_full + 1;
-    uint64_t* red_bar = a_raw + 1;                // bulk split-K: the peers' rows have landed
+    uint64_t* red_bar = a_raw + 1;                // split-K: the peers' rows have landed here
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
     volatile uint32_t* flags = tmem_slot + 1;    // [0] abort
 
@@ -224,10 +222,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * ((r1 - r0 + 3) / 4)) * kTileN * 16u);
         flags[0] = 0u;
         fence_mbar_init();
-        MXFP4_PHASE(52);
     }
     __syncthreads();
-    if (threadIdx.x == 0) MXFP4_PHASE(53);
     // Split-K by st.async or bulk copies: every CTA arrives here once its barriers exist, and each
     // warp waits (cluster_wait) at a point of its own off the critical path, before any post.
     const bool cluster_posts = S > 1 && (p.red_bulk || vec);
@@ -384,12 +380,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
                 mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
                 tc_commit(&empty[s]);
-                if (j == issuer) MXFP4_PHASE(48 + 2 * issuer);
                 s += p.issuers;
                 while (s >= stages) { s -= stages; phase ^= 1u; }
             }
             if (!mok) fail(p, flags);
-            MXFP4_PHASE(49 + 2 * issuer);
             tc_commit(acc_full);
         }
         __syncwarp();
@@ -403,7 +397,6 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         const bool waited = mbar_wait(acc_full, 0, lim);
         tc_fence_after_sync();
         if (et == 0) MXFP4_PHASE(6);
-        if (lane == 0) MXFP4_PHASE(32 + warp - 3);
         if (!waited) fail(p, flags);
         // one decision per warp (tcgen05.ld is warp-collective)
         ok = !__any_sync(0xffffffffu, !waited || flags[0] != 0u);
@@ -446,13 +439,12 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         return;
     }
 
-    // K slices > 1. Runs of rows_per rows of the tile belong to successive CTAs of the cluster.
-    // Every CTA posts its fp32 accumulator straight from tensor memory into the owners' receive
-    // buffers (slot = source rank): short runs as 16-byte stores of four tokens, long runs as
-    // contiguous 128-byte rows. After one cluster barrier each owner sums its rows over the
-    // sources in rank order (run-to-run identical) and stores bf16.
-    // Without a dedicated receive buffer a first barrier makes sure every peer's MMAs are done
-    // before its pipeline buffers are overwritten.
+    // K slices > 1. Runs of rows_per rows of the tile belong to successive CTAs of the cluster
+    // (the owners); every CTA sends its fp32 accumulator rows to their owners' receive buffers
+    // (slot = source rank) in one of three forms below, and each owner sums its rows over the
+    // sources in rank order (run-to-run identical) and stores bf16. Without a dedicated receive
+    // buffer a cluster barrier first makes sure every peer's MMAs are done before its pipeline
+    // buffers are overwritten.
     if (p.red_bulk) {
         // Long runs: every CTA stages its fp32 tile [row][n] in its own shared memory, then one
         // bulk copy per owner moves that owner's rows into the owner's receive buffer, counted
@@ -577,7 +569,6 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             }
         }
         if (threadIdx.x == 96) MXFP4_PHASE(8);
-        if (warp >= 3 && lane == 0) MXFP4_PHASE(40 + warp - 3);
         __syncwarp();
         tc_fence_before_sync();
         __syncthreads();                           // own rows visible; TMEM reads done

@@ -19,7 +19,7 @@
 namespace mxfp4 {
 
 #ifdef MXFP4_TRACE
-static __device__ unsigned long long trace_buffer[4096][64];
+static __device__ unsigned long long trace_buffer[4096][16];
 #endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -274,26 +274,9 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a,
                  : "memory");
 }
 
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
-}  // namespace mxfp4
-
-namespace mxfp4 {
-
-// Warm L2 with a global range without touching shared memory or registers. Issued before the
+// Warm L2 with a global line without touching shared memory or registers. Issued before the
 // wait on the previous grid it stays correct: nothing reads the prefetched bytes directly, and
 // later loads go through L2, which every write of the previous grid updates.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
