@@ -234,6 +234,42 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
     return res
 
 
+def bench_quantizer(mx, rows: int, K: int, steps: int, warmup: int, l2_bytes: int) -> dict:
+    """The standalone quantizer on a large activation: `steps` mxfp4_quantize calls of a bf16
+    [rows, K] matrix in a CUDA graph, rotating over enough copies (> 3x L2) that every call reads
+    from HBM. Algorithmic bytes: the bf16 read, the e2m1 and e8m0 writes."""
+    dev = torch.device("cuda")
+    x0 = workloads.random_bf16(rows, K, seed=11).to(dev)
+    per_copy = rows * K * 2 + rows * K // 2 + rows * K // 32
+    copies = max(2, -(-3 * l2_bytes // per_copy))
+    xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+    qs = [torch.empty(rows, K // 2, dtype=torch.uint8, device=dev) for _ in range(copies)]
+    ss = [torch.empty(rows, K // 32, dtype=torch.uint8, device=dev) for _ in range(copies)]
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        for i in range(max(warmup, copies)):
+            mx.mxfp4_quantize(xs[i % copies], qs[i % copies], ss[i % copies], stream=side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(steps):
+            mx.mxfp4_quantize(xs[i % copies], qs[i % copies], ss[i % copies], stream=side)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    with torch.cuda.stream(side):
+        e0.record(side)
+        g.replay()
+        e1.record(side)
+    e1.synchronize()
+    us = 1000.0 * e0.elapsed_time(e1) / steps
+    status = mx.mxfp4_device_status()
+    del xs, qs, ss, g
+    torch.cuda.empty_cache()
+    return {"rows": rows, "K": K, "us_per_call": round(us, 3), "algorithmic_bytes": per_copy,
+            "gbs": round(per_copy / (us * 1e-6) / 1e9, 1), "status": status}
+
+
 def fp4_peak_tflops():
     """Dense FP4 peak: the measured bf16 burst figure times the nominal fp4 / bf16 ratio (13.5 / 2.25
     PFLOP/s), else the nominal 13.5 PFLOP/s. Returns (TFLOP/s, kind)."""
@@ -322,7 +358,7 @@ def main():
     per_shape = {}
     if not args.no_shapes:
         fp4_peak, _ = fp4_peak_tflops()
-        for ws_ in workloads.WORKLOADS:
+        for ws_ in workloads.WORKLOADS + workloads.EXTRA_WORKLOADS:
             r = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2)
             rw = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2, warm=True)
             gbs = ws_.algorithmic_bytes / (r["us_per_call"] * 1e-6) / 1e9
@@ -337,6 +373,11 @@ def main():
                                    "warm_l2_fp4_frac": round(tf_warm / fp4_peak, 4),
                                    "path": r["plan"]["path"], "splits": r["plan"]["splits"],
                                    "ctas": r["plan"]["ctas"], "status": max(r["status"], rw["status"])}
+
+    quantizer = None
+    if not args.no_shapes:
+        quantizer = bench_quantizer(mx, 4096, 7168, 50, args.warmup, l2)
+        quantizer["hbm_frac"] = round(quantizer["gbs"] / peak, 4)
 
     if rank != 0:
         if world > 1:
@@ -368,6 +409,7 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "per_shape": per_shape,
+        "quantizer": quantizer,
         "device_status": main_res["status"],
     }
     print(json.dumps(line))
