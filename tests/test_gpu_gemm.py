@@ -231,3 +231,21 @@ def test_gemm_host_buffers_match_device_call():
         mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, workspace=tiny)
     torch.cuda.synchronize()
     assert torch.all(c_host == 5.0)
+
+
+@pytest.mark.parametrize("M,N,K,splits,m_tile", [(600, 200, 512, 1, 0), (600, 200, 1024, 2, 0), (300, 384, 768, 1, 256)])
+def test_gemm_256_token_tiles_vs_oracle(M, N, K, splits, m_tile):
+    # 256-token tiles (M > 512 by default, or forced): two 128-row scale chunks per token block,
+    # four token-scale copies per step, one MMA issuer; ragged last tile
+    mx = _mx()
+    plan = mx.mxfp4_gemm_plan(M, N, K, 2, splits, m_tile)
+    assert plan["m_tile"] == 256 and plan["issuers"] == 1, plan
+    a = workloads.random_bf16(M, K, seed=M + K + 256)
+    b = workloads.random_bf16(N, K, seed=N + K + 256, scale=0.5)
+    bq, bs = mx.mxfp4_quantize(b.cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c = mx.mxfp4_gemm(a.cuda(), packed, N, path=2, splits=splits, m_tile=m_tile)
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0
+    ref = oracle_c(a, to_np_u8(bq), to_np_u8(bs))
+    check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} splits {splits} m_tile 256")
