@@ -249,3 +249,23 @@ def test_gemm_256_token_tiles_vs_oracle(M, N, K, splits, m_tile):
     assert mx.mxfp4_device_status() == 0
     ref = oracle_c(a, to_np_u8(bq), to_np_u8(bs))
     check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} splits {splits} m_tile 256")
+
+
+@pytest.mark.parametrize("M,K,path,splits", [(8, 512, 1, 1), (16, 1536, 1, 3), (5, 1280, 1, 2), (13, 2048, 1, 4),
+                                              (40, 768, 2, 1), (8, 1024, 2, 2)])
+def test_quantized_a_read_back_through_one_hot_b(M, K, path, splits):
+    # With B one-hot (B[n, n] = 1, all else 0: exactly representable, so its quantization is the
+    # identity), C[m, n] is dequant(quantized A)[m, n] exactly: C shows the codes and scales the
+    # call's own A quantization produced -- inside the GEMM on the fused path -- and must equal the
+    # oracle's bit for bit, not just within the GEMM tolerance.
+    N = K
+    a = workloads.random_bf16(M, K, seed=M * 13 + K)
+    b = torch.zeros(N, K, dtype=torch.bfloat16)
+    idx = torch.arange(N)
+    b[idx, idx] = 1.0
+    c, bq, bs = run_gemm(a, b, path=path, splits=splits)
+    aq, as_ = oracle.quantize(workloads.bf16_bits(a))
+    want = oracle.bf16_to_f64(oracle.to_bf16(oracle.mxfp4_gemm_ref(aq, as_, bq, bs)))
+    assert np.array_equal(want, oracle.dequantize(aq, as_)), "one-hot B must read A back"
+    bad = np.argwhere(c != want)
+    assert bad.size == 0, f"{len(bad)} entries differ, first at {tuple(bad[0])}: got {c[tuple(bad[0])]!r} want {want[tuple(bad[0])]!r}"
