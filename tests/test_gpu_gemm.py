@@ -208,14 +208,17 @@ def test_gemm_host_buffers_match_device_call():
         want = mx.mxfp4_gemm(a.cuda(), packed, N)
         a_store = torch.zeros(M, K + 64, dtype=torch.bfloat16).pin_memory()
         a_store[:, :K] = a
-        c_store = torch.full((M, N + 3), 5.0, dtype=torch.bfloat16).pin_memory()
-        a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-        c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-        mx.mxfp4_gemm_host(a_store[:, :K], packed, N, c_store[:, :N], a_dev, c_dev)
-        torch.cuda.synchronize()
-        assert mx.mxfp4_device_status() == 0
-        assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16))
-        assert torch.all(c_store[:, N:] == 5.0)
+        for pinned in (True, False):   # mapped page-locked C (written by the GEMM) or a copy
+            c_store = torch.full((M, N + 3), 5.0, dtype=torch.bfloat16)
+            if pinned:
+                c_store = c_store.pin_memory()
+            a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+            c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            mx.mxfp4_gemm_host(a_store[:, :K], packed, N, c_store[:, :N], a_dev, c_dev)
+            torch.cuda.synchronize()
+            assert mx.mxfp4_device_status() == 0
+            assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16)), pinned
+            assert torch.all(c_store[:, N:] == 5.0)
     # M = 300 needs a workspace (two-kernel path): a one-byte one is refused, C untouched
     M, N, K = 300, 256, 256
     need = mx.mxfp4_gemm_workspace_size(M, N, K)
