@@ -8,9 +8,12 @@
 //   code   = e2m1(x * 2^-s): nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to even,
 //            saturating at 6, sign in bit 3 even when the magnitude rounds to 0;
 //   byte   = code(even element) | code(odd element) << 4.
-// Here amax is taken on the integer bit patterns (|x| of a finite float orders like its
-// bit pattern), floor(log2) is read off the exponent field, and the element rounding uses
-// the sm_100+ conversion cvt.rn.satfinite.e2m1x2.f32 on the exactly scaled fp32 value.
+// Here amax is a depth-4 tree of max.xorsign.abs.bf16x2 over the block's bf16 pairs (the
+// magnitude of the larger |x|, exactly; inputs are finite by contract), floor(log2) is read off
+// the exponent field, the scaling is one fp32 multiply per element (exact for a power of two)
+// and the element rounding uses the sm_100+ conversion cvt.rn.satfinite.e2m1x2.f32. (Measured
+// against a chain of integer maxima, and against f32x2 multiplies with prmt packing: the tree
+// with scalar multiplies was the fastest inside the fused GEMM and the quantize kernels.)
 #pragma once
 #include <cstdint>
 
@@ -54,35 +57,15 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
 #endif
 }
 
-// Quantize one 1x32 block held as 16 words of bf16 pairs (element 2i in the low half of
-// word i). Writes 4 words of packed codes (element 2i in the low nibble of its byte) and
-// returns the e8m0 byte.
-__device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&w)[16], uint32_t (&out)[4]) {
-    uint32_t mx = 0u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
-    const uint32_t amax_bits = max(mx & 0xFFFFu, mx >> 16) << 16;
-    const int s = scale_exponent(amax_bits);
-    const float m = inv_scale(s);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t packed = 0u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t word = w[4 * j + i];
-            const float even = __fmul_rn(__uint_as_float(word << 16), m);
-            const float odd = __fmul_rn(__uint_as_float(word & 0xFFFF0000u), m);
-            packed |= e2m1x2(even, odd) << (8 * i);
-        }
-        out[j] = packed;
-    }
-    return static_cast<uint32_t>(s + 127);
+// max(|a|, |b|) per bf16 half (the sign bit of each half is junk: mask it off).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// A quarter of a 1x32 block: 8 bf16 as 4 words, quantized with the block's scale multiplier m
-// (inv_scale of the block's exponent); returns 4 bytes of packed codes (element 2i in the low
-// nibble of byte i). Same arithmetic per element as quantize_block32.
-__device__ __forceinline__ uint32_t quantize_quarter(const uint32_t (&w)[4], float m) {
+// Codes of 8 elements (4 words) scaled by m: 4 bytes, element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t encode_words4(const uint32_t* w, float m) {
     uint32_t packed = 0u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -93,11 +76,35 @@ __device__ __forceinline__ uint32_t quantize_quarter(const uint32_t (&w)[4], flo
     return packed;
 }
 
+// Quantize one 1x32 block held as 16 words of bf16 pairs (element 2i in the low half of
+// word i). Writes 4 words of packed codes (element 2i in the low nibble of its byte) and
+// returns the e8m0 byte.
+__device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&w)[16], uint32_t (&out)[4]) {
+    uint32_t m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m8[i] = absmax_bf16x2(m8[2 * i], m8[2 * i + 1]);
+    const uint32_t mx = absmax_bf16x2(absmax_bf16x2(m8[0], m8[1]), absmax_bf16x2(m8[2], m8[3]));
+    const uint32_t amax_bits = max(mx & 0x7FFFu, (mx >> 16) & 0x7FFFu) << 16;
+    const int s = scale_exponent(amax_bits);
+    const float m = inv_scale(s);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = encode_words4(&w[4 * j], m);
+    return static_cast<uint32_t>(s + 127);
+}
+
+// A quarter of a 1x32 block: 8 bf16 as 4 words, quantized with the block's scale multiplier m
+// (inv_scale of the block's exponent); returns 4 bytes of packed codes (element 2i in the low
+// nibble of byte i). Same arithmetic per element as quantize_block32.
+__device__ __forceinline__ uint32_t quantize_quarter(const uint32_t (&w)[4], float m) {
+    return encode_words4(w, m);
+}
+
 // Max |x| bit pattern (as a bf16 in the low half) over 4 words of bf16 pairs.
 __device__ __forceinline__ uint32_t amax_quarter(const uint32_t (&w)[4]) {
-    const uint32_t m = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-    return max(m & 0xFFFFu, m >> 16);
+    const uint32_t m = absmax_bf16x2(absmax_bf16x2(w[0], w[1]), absmax_bf16x2(w[2], w[3]));
+    return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
 }
 
 // Load 32 consecutive bf16 (64 bytes, 16-byte aligned) as 16 words.
