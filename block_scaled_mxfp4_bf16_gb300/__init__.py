@@ -123,16 +123,18 @@ def mxfp4_version() -> int:
 
 def mxfp4_quantize(x: torch.Tensor, q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
                    stream=None) -> tuple[torch.Tensor, torch.Tensor]:
-    """bf16 [rows, K] (row stride may exceed K) -> (e2m1 uint8 [rows, K/2], e8m0 uint8 [rows, K/32])."""
+    """bf16 [rows, K] (row stride may exceed K, K % 8 == 0) -> (e2m1 uint8 [rows, nblk*16],
+    e8m0 uint8 [rows, nblk]) with nblk = ceil(K/32); codes past K are zero."""
     L = load_library()
     _dev(x, "x")
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a 2-D bf16 tensor with unit column stride")
     rows, K = x.shape
+    nblk = (K + 31) // 32
     if q is None:
-        q = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+        q = torch.empty(rows, nblk * 16, dtype=torch.uint8, device=x.device)
     if scales is None:
-        scales = torch.empty(rows, K // 32, dtype=torch.uint8, device=x.device)
+        scales = torch.empty(rows, nblk, dtype=torch.uint8, device=x.device)
     _check(L.mxfp4_quantize(x.data_ptr(), rows, K, x.stride(0), q.data_ptr(), scales.data_ptr(), _stream(stream)),
            "mxfp4_quantize")
     return q, scales
@@ -144,12 +146,13 @@ def mxfp4_prepack_b_size(N: int, K: int) -> int:
 
 def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | None = None,
                     stream=None) -> torch.Tensor:
-    """Pre-quantized B (e2m1 [N, K/2], e8m0 [N, K/32]) -> packed uint8 buffer for mxfp4_gemm."""
+    """Pre-quantized B (e2m1 [N, nblk*16], e8m0 [N, nblk], the layout mxfp4_quantize writes) ->
+    packed uint8 buffer for mxfp4_gemm with any K in (32*(nblk-1), 32*nblk]."""
     L = load_library()
     _dev(bq, "bq")
     N, K = bq.shape[0], bq.shape[1] * 2
     if bs.shape != (N, K // 32) or not bq.is_contiguous() or not bs.is_contiguous():
-        raise ValueError("bq [N, K/2] and bs [N, K/32] must be contiguous and consistent")
+        raise ValueError("bq [N, nblk*16] and bs [N, nblk] must be contiguous and consistent")
     size = mxfp4_prepack_b_size(N, K)
     if size == 0:
         raise Mxfp4Error(2, "mxfp4_prepack_b_size")

@@ -131,7 +131,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
 size_t packed_b_bytes(int64_t N, int64_t K);
 
 // Kernel launchers (return cudaError_t).
-// Natural layout: q [rows, K/2], scales [rows, K/32].
+// Natural layout: q [rows, nblk*16], scales [rows, nblk], nblk = ceil(K/32) (K % 8 == 0).
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q,
                             uint8_t* scales, cudaStream_t s);
 // Token blocks for the GEMM, [m_tiles][k_atoms][a_block]; rows past `rows` and K past `K` zeroed.

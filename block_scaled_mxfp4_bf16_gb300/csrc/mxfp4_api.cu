@@ -228,7 +228,7 @@ static uint64_t g_wait_limit_ns = 1000000000ull;   // 1 s per bounded wait
 static int check_gemm_args(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
                            const void* c, int64_t ldc) {
     if (M < 0 || N < 0 || K < 0) return MXFP4_ERR_ARG;
-    if (K == 0 || K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (K == 0 || K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (M == 0 || N == 0) return MXFP4_OK;
     if (lda < K || ldc < N) return MXFP4_ERR_SHAPE;
     if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 30)) return MXFP4_ERR_SHAPE;
@@ -329,7 +329,7 @@ int mxfp4_version(void) { return 200; }
 
 int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, void* scales, void* stream) {
     if (rows < 0 || K < 0) return MXFP4_ERR_ARG;
-    if (K % 32 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (rows == 0 || K == 0) return MXFP4_OK;
     if (ld < K) return MXFP4_ERR_SHAPE;
     if (!x || !q || !scales) return MXFP4_ERR_ARG;
@@ -343,13 +343,13 @@ int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, 
 }
 
 size_t mxfp4_prepack_b_size(int64_t N, int64_t K) {
-    if (N <= 0 || K <= 0 || K % 64 != 0) return 0;
+    if (N <= 0 || K <= 0 || K % 8 != 0) return 0;
     return packed_b_bytes(N, K);
 }
 
 int mxfp4_prepack_b(const void* bq, const void* bs, int64_t N, int64_t K, void* packed, void* stream) {
     if (N <= 0 || K <= 0) return MXFP4_ERR_ARG;
-    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (!bq || !bs || !packed) return MXFP4_ERR_ARG;
     if (!aligned(bq, 16) || !aligned(packed, 1024)) return MXFP4_ERR_ALIGN;
     DeviceInfo di;
@@ -361,7 +361,7 @@ int mxfp4_prepack_b(const void* bq, const void* bs, int64_t N, int64_t K, void* 
 }
 
 size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts) {
-    if (M <= 0 || N <= 0 || K <= 0 || K % 64 != 0) return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0) return 0;
     DeviceInfo di;
     if (device_info(&di) != MXFP4_OK) return 0;
     GemmPlan plan;
@@ -383,7 +383,7 @@ int mxfp4_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
 int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts, int* path, int* splits,
                     int* m_tile, int* ctas, int* stages) {
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
-    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
@@ -402,7 +402,7 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
 int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts, mxfp4_plan_info* info) {
     if (!info) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
-    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
@@ -418,7 +418,7 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
                           const int* cluster_caps, mxfp4_plan_info* info) {
     if (!info || sm_count < 1) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
-    if (K % 64 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
     if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     int caps[kMaxSplits + 1];
     for (int s = 0; s <= kMaxSplits; ++s) caps[s] = cluster_caps ? cluster_caps[s] : (1 << 30);

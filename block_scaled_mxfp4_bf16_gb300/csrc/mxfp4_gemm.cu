@@ -93,6 +93,7 @@ struct QuantSlice {
 // Every thread of the CTA takes part (the copy and MMA warps have nothing else to do until the
 // token blocks exist): one 1x32 block per item, items dealt round-robin over the CTA, two per
 // thread per pass so their arithmetic interleaves; K past the end becomes zero codes and scales.
+// (In a last block cut by K the epilogue warps have zeroed the staged bytes past K.)
 // Rows past M are left as they are: a token row only feeds its own accumulator column, and
 // columns past M are never stored.
 __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, const GemmArgs& p,
@@ -214,7 +215,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         }
         mbar_init(a_full, kGemmThreads / 32);
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
-        mbar_init(a_raw, 1);
+        mbar_init(a_raw, 1 + kEpiWarps);   // the copy thread + the epilogue warps (tail zeroing)
         mbar_init(red_bar, 1);
         if (S > 1 && p.red_bulk && r1 > r0)   // (S - 1) peers x owned rows x 512 bytes
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * (r1 - r0)) * kTileN * 4u);
@@ -291,6 +292,21 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             const int r = i / lines;
             prefetch_l2(arow + static_cast<int64_t>(r) * p.lda + (i - r * lines) * 64);
         }
+        // K cuts the slice's last 1x32 block when kslice % 32 != 0: the copies stop at K, so the
+        // rest of that block in every staged row is zeroed here (elements past K count as zeros).
+        // Disjoint from the bytes the copies write; published by each warp's arrival on a_raw,
+        // which the quantizing threads acquire with the copies. (Placed here, in warps that are
+        // idle until then, it measured free; in the copy thread it slowed the fused path.)
+        const uint32_t from = static_cast<uint32_t>(kslice) * 2u;
+        const uint32_t end = static_cast<uint32_t>((kslice + 31) / 32) * 64u;
+        const int per_row = static_cast<int>((end - from) / 16u);
+        for (int i = threadIdx.x - 96; i < m_valid * per_row; i += kEpiThreads) {
+            const int r = i / per_row;
+            *reinterpret_cast<uint4*>(smem + p.off_araw + r * raw_row + from + (i - r * per_row) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_raw);
     }
     __syncwarp();
     // Fused path: every warp quantizes (one call site, so the quantizer is inlined once).

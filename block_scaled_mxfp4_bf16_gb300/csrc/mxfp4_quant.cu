@@ -1,18 +1,22 @@
 // Standalone MXFP4 quantizer (natural layout and the GEMM's token blocks) and the weight
 // prepack. One thread per 1x32 block: 64 bytes of bf16 in (four 16-byte loads in flight),
 // 16 bytes of packed e2m1 and one e8m0 byte out.
+// K is a multiple of 8. A row has ceil(K/32) blocks; in the last one the elements past K count
+// as zeros (submission 711914 `_standalone_quant_kernel` loads A under the mask offs_k < K with
+// 0 as the fill value), so they give zero codes and do not change the block's scale. The
+// 16-byte pieces past K are never read.
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_device.cuh"
 
 namespace mxfp4 {
 
-// Natural layout: q [rows, K/2], scales [rows, K/32].
+// Natural layout: q [rows, nblk*16], scales [rows, nblk], nblk = ceil(K/32).
 __global__ void __launch_bounds__(256)
 quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                 uint8_t* __restrict__ q, uint8_t* __restrict__ scales) {
     pdl_launch_dependents();
-    const int64_t nblk = K / 32;
+    const int64_t nblk = (K + 31) / 32;
     const int64_t items = rows * nblk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -22,9 +26,9 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t
         const int64_t r = it / nblk;
         const int64_t kb = it - r * nblk;
         uint32_t w[16], out[4];
-        load_block32(x + r * ld + kb * 32, w);
+        load_block32_upto(x + r * ld + kb * 32, K - kb * 32, w);
         const uint32_t byte = quantize_block32(w, out);
-        *reinterpret_cast<uint4*>(q + r * (K / 2) + kb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(q + r * (nblk * 16) + kb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
         scales[it] = static_cast<uint8_t>(byte);
     }
 }
@@ -37,7 +41,7 @@ __global__ void __launch_bounds__(256)
 quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
     pdl_launch_dependents();
-    const int64_t nblk = K / 32;
+    const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
     {   // warm L2 with this thread's first block while the previous grid finishes (see prefetch_l2)
@@ -59,7 +63,7 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
         const bool live = in_range && r < rows && kbp < nblk;
         uint32_t w[16], out[4] = {0u, 0u, 0u, 0u}, byte = 0u;
         if (live) {
-            load_block32(x + r * ld + kbp * 32, w);
+            load_block32_upto(x + r * ld + kbp * 32, K - kbp * 32, w);
             byte = quantize_block32(w, out);
         }
         uint32_t word = byte << (8 * (lane & 3));
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(256)
 quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                         uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
     pdl_launch_dependents();
-    const int64_t nblk = K / 32;
+    const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
     const int lane = threadIdx.x & 31;
@@ -99,7 +103,7 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
     {   // warm L2 with this lane's first 16 bytes while the previous grid finishes (see prefetch_l2)
         const int64_t it0 = warp_id * 8 + (lane >> 2);
         const int64_t r = it0 / row_items, kbp = it0 - (it0 / row_items) * row_items;
-        if (it0 < items && r < rows && kbp < nblk) prefetch_l2(x + r * ld + kbp * 32 + part * 8);
+        if (it0 < items && r < rows && kbp * 32 + part * 8 < K) prefetch_l2(x + r * ld + kbp * 32 + part * 8);
     }
     pdl_wait_prior_grid();
     // the loop bound is uniform per warp, so the shuffles below always see all 32 lanes
@@ -109,7 +113,7 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
         const int64_t kbp = it - r * row_items;          // block index within the padded row
         const bool live = r < rows && kbp < nblk;
         uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (live) {
+        if (live && kbp * 32 + part * 8 < K) {   // a piece past K in the last block stays zero
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + r * ld + kbp * 32 + part * 8));
             w[0] = v.x;
             w[1] = v.y;
@@ -137,11 +141,12 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
 }
 
 // Weight prepack: one thread per (row, block) of the padded [n_tiles*128, k_atoms*256] matrix;
-// copies 16 bytes of e2m1 into the swizzled rows and the scale byte into its chunk.
+// copies 16 bytes of e2m1 into the swizzled rows and the scale byte into its chunk. Input rows
+// are the natural layout: nblk = ceil(K/32) blocks of 16 code bytes and one scale byte each.
 __global__ void __launch_bounds__(256)
 prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, int64_t N, int64_t K,
                uint8_t* __restrict__ out, int k_atoms) {
-    const int64_t nblk = K / 32;
+    const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
     const int64_t rows_cover = (N + kTileN - 1) / kTileN * kTileN;
     const int64_t items = rows_cover * row_items;
@@ -155,7 +160,7 @@ prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, i
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         uint8_t sc = 0;
         if (r < N && kbp < nblk) {
-            v = __ldg(reinterpret_cast<const uint4*>(bq + r * (K / 2) + kbp * 16));
+            v = __ldg(reinterpret_cast<const uint4*>(bq + r * (nblk * 16) + kbp * 16));
             sc = bs[r * nblk + kbp];
         }
         *reinterpret_cast<uint4*>(blk + swz_chunk_offset(rr, c)) = v;
@@ -175,7 +180,7 @@ static int grid_for(int64_t items, int threads) {
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q, uint8_t* scales,
                             cudaStream_t s) {
     const int threads = 256;
-    return launch_pdl(quantize_kernel, dim3(grid_for(rows * (K / 32), threads)), dim3(threads), 0, s, x, rows, K,
+    return launch_pdl(quantize_kernel, dim3(grid_for(rows * ((K + 31) / 32), threads)), dim3(threads), 0, s, x, rows, K,
                       ld, q, scales);
 }
 

@@ -120,4 +120,22 @@ __device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[
     }
 }
 
+// The block starting at src when only `avail` elements remain in the row (avail > 0, a
+// multiple of 8): the 16-byte pieces at or past the row's end are not read and count as zeros.
+__device__ __forceinline__ void load_block32_upto(const uint16_t* src, int64_t avail, uint32_t (&w)[16]) {
+    if (avail >= 32) {
+        load_block32(src, w);
+        return;
+    }
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = 8 * i < avail ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i + 0] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+}
+
 }  // namespace mxfp4

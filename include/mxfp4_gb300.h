@@ -23,6 +23,12 @@
  *     mxfp4_device_status.
  *   - Inputs must be finite; NaN or Inf in A or B gives unspecified (but memory-safe)
  *     results. Scale bytes of 255 (e8m0 NaN) in B likewise.
+ *   - K is a positive multiple of 8 (bf16 rows move in 16-byte pieces). A row has
+ *     nblk = ceil(K/32) blocks; when K % 32 != 0 the last block is cut by K and its elements
+ *     past K count as zeros, as submission 711914's `_standalone_quant_kernel` loads A under
+ *     the mask offs_k < K with 0 as the fill value: they do not change the block's scale and
+ *     are stored as zero codes. The natural packed layout keeps whole blocks: codes
+ *     [rows, nblk*16] bytes, scales [rows, nblk] bytes.
  *   - The library targets compute capability 10.3 (GB300) only; other devices give
  *     MXFP4_ERR_ARCH.
  */
@@ -39,7 +45,7 @@ extern "C" {
 typedef enum {
     MXFP4_OK = 0,
     MXFP4_ERR_ARG = 1,       /* null pointer, negative size, bad option value */
-    MXFP4_ERR_SHAPE = 2,     /* K not a positive multiple of 64, ld smaller than K, too large */
+    MXFP4_ERR_SHAPE = 2,     /* K not a positive multiple of 8, ld smaller than K, too large */
     MXFP4_ERR_ALIGN = 3,     /* pointer or leading dimension misaligned (see each call) */
     MXFP4_ERR_ARCH = 4,      /* current device is not compute capability 10.3 */
     MXFP4_ERR_CUDA = 5,      /* a CUDA runtime/driver call or a launch failed */
@@ -65,9 +71,10 @@ int mxfp4_version(void);
  * x * 2^-s is rounded to the nearest e2m1 value (ties to even, saturating at 6, the sign
  * kept even when the value rounds to zero) and packed even-low / odd-high.
  *   x       : bf16 [rows, K], row stride `ld` elements (ld >= K). 16-byte aligned, ld % 8 == 0.
- *   q       : out, uint8 [rows, K/2], row stride K/2 bytes. 16-byte aligned.
- *   scales  : out, uint8 [rows, K/32], row stride K/32 bytes (no alignment requirement).
- *   K       : multiple of 32.  rows == 0 or K == 0 is a no-op.
+ *   q       : out, uint8 [rows, nblk*16] (nblk = ceil(K/32)), row stride nblk*16 bytes
+ *             (K/2 when K % 32 == 0). 16-byte aligned. Codes past K are zero.
+ *   scales  : out, uint8 [rows, nblk], row stride nblk bytes (no alignment requirement).
+ *   K       : multiple of 8.  rows == 0 or K == 0 is a no-op.
  * Bytes are bit-identical to the CPU oracle.
  */
 int mxfp4_quantize(const void *x, int64_t rows, int64_t K, int64_t ld,
@@ -89,9 +96,11 @@ size_t mxfp4_prepack_b_size(int64_t N, int64_t K);
  * for the MFMA layout, submission 608632 `_new_generate_input`); here every (128-row tile,
  * 256-K step) becomes one contiguous block that is the exact shared-memory image the tcgen05
  * block-scaled MMA reads, so the GEMM streams the weights with one bulk copy per step.
- *   bq     : uint8 [N, K/2] packed e2m1 (even element low nibble). 16-byte aligned.
- *   bs     : uint8 [N, K/32] e8m0 scales (as written by mxfp4_quantize).
- *   K      : positive multiple of 64.  N >= 1.
+ *   bq     : uint8 [N, nblk*16] packed e2m1 (even element low nibble), nblk = ceil(K/32),
+ *            row stride nblk*16 bytes (the layout mxfp4_quantize writes). 16-byte aligned.
+ *            Codes past K only ever meet A's zero codes, so their value does not matter.
+ *   bs     : uint8 [N, nblk] e8m0 scales (as written by mxfp4_quantize).
+ *   K      : positive multiple of 8.  N >= 1. K and ceil(K/32)*32 give the same buffer.
  *   packed : out, mxfp4_prepack_b_size(N, K) bytes, 1024-byte aligned. Must not overlap
  *            bq or bs.
  */
@@ -122,7 +131,7 @@ int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  *   workspace: ws_bytes >= mxfp4_gemm_workspace_size(M, N, K), 256-byte aligned; may be
  *              NULL when that size is 0. Calls sharing a workspace must be ordered (same
  *              stream, or synchronized); overlapping calls on one workspace race.
- *   K        : positive multiple of 64.  M == 0 or N == 0 is a no-op.
+ *   K        : positive multiple of 8.  M == 0 or N == 0 is a no-op.
  * A is quantized exactly like mxfp4_quantize (bit-identical codes and scales). With split-K
  * the K slices of an output tile run as one thread-block cluster and their fp32 partial
  * sums are added in slice order through distributed shared memory, so results are

@@ -99,11 +99,21 @@ def num_threads() -> int:
 
 
 def quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    """bf16 bit patterns [rows, K] (uint16) -> (q uint8 [rows, K/2], scales uint8 [rows, K/32])."""
+    """bf16 bit patterns [rows, K] (uint16) -> (q uint8 [rows, nblk*16], scales uint8 [rows, nblk]),
+    nblk = ceil(K/32).
+
+    When K is not a multiple of 32 the row is first widened to 32*nblk elements with zeros:
+    submission 711914's `_standalone_quant_kernel` loads A under the mask offs_k < K with 0.0
+    as the fill value, so the missing elements of the last block are zeros to the block
+    maximum and to the encoder (zero codes). K must be a multiple of 8 (the library's bf16
+    rows move in 16-byte pieces)."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     rows, K = x.shape
+    if K % 8:
+        raise ValueError("K must be a multiple of 8")
     if K % 32:
-        raise ValueError("K must be a multiple of 32")
+        x = np.concatenate([x, np.zeros((rows, 32 - K % 32), np.uint16)], axis=1)
+        K = x.shape[1]
     q = np.empty((rows, K // 2), np.uint8)
     s = np.empty((rows, K // 32), np.uint8)
     if rows and K:
@@ -112,7 +122,8 @@ def quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 
 
 def dequantize(q: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """Packed e2m1 [rows, K/2] + e8m0 [rows, K/32] -> fp64 [rows, K]."""
+    """Packed e2m1 [rows, K/2] + e8m0 [rows, K/32] -> fp64 [rows, K] (K = 32 * whole blocks; a
+    K-tail matrix comes back with its zero padding)."""
     q = np.ascontiguousarray(q, np.uint8)
     scales = np.ascontiguousarray(scales, np.uint8)
     rows, K = q.shape[0], q.shape[1] * 2

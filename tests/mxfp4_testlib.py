@@ -61,7 +61,8 @@ def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: in
     b = b_cpu.cuda()
     bq, bs = mx.mxfp4_quantize(b)
     packed = mx.mxfp4_prepack_b(bq, bs)
-    a_store = torch.zeros(M, K + lda_pad, dtype=torch.bfloat16, device="cuda")
+    # the row padding past K holds huge values: reading any of it would show in C
+    a_store = torch.full((M, K + lda_pad), 1.0e30, dtype=torch.bfloat16, device="cuda")
     a_store[:, :K] = a_cpu.cuda()
     a = a_store[:, :K]
     c_store = torch.full((M + 1, N + ldc_pad), canary, dtype=torch.bfloat16, device="cuda")

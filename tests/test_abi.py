@@ -48,7 +48,9 @@ def test_prepack_size_is_pure_host_arithmetic(lib):
     # and 256-element K step
     assert lib.mxfp4_prepack_b_size(2112, 7168) == 17 * 28 * 17408
     assert lib.mxfp4_prepack_b_size(100, 64) == 1 * 1 * 17408
-    assert lib.mxfp4_prepack_b_size(100, 96) == 0     # K must be a multiple of 64
+    assert lib.mxfp4_prepack_b_size(100, 96) == 1 * 1 * 17408   # K tails are zero padding
+    assert lib.mxfp4_prepack_b_size(100, 8) == 1 * 1 * 17408
+    assert lib.mxfp4_prepack_b_size(100, 100) == 0    # K must be a multiple of 8
     assert lib.mxfp4_prepack_b_size(0, 64) == 0
 
 

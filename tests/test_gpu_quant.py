@@ -76,6 +76,35 @@ def test_quantize_strided_rows_and_small_shapes():
         assert_bytes_equal(s, rs, f"scales {rows}x{K}")
 
 
+@pytest.mark.parametrize("rows,K", [(1, 8), (3, 40), (5, 72), (64, 200), (129, 7176), (4096, 7176)])
+def test_quantize_k_tail_bit_exact(rows, K):
+    # K % 32 != 0: the last block is cut by K and its missing elements count as zeros; the row
+    # padding past K holds huge values, which would change the last block's scale if read
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    x = workloads.random_bf16(rows, K, seed=rows + 3 * K, scale=2.0)
+    store = torch.full((rows, K + 40), 1.0e30, dtype=torch.bfloat16)
+    store[:, :K] = x
+    q, s = mx.mxfp4_quantize(store.cuda()[:, :K])
+    rq, rs = oracle.quantize(workloads.bf16_bits(x))
+    torch.cuda.synchronize()
+    nblk = (K + 31) // 32
+    assert tuple(q.shape) == (rows, nblk * 16) and tuple(s.shape) == (rows, nblk)
+    assert_bytes_equal(to_np_u8(q), rq, f"e2m1 {rows}x{K}")
+    assert_bytes_equal(to_np_u8(s), rs, f"scales {rows}x{K}")
+
+
+def test_quantize_tail_rows_hand_worked():
+    # the hand-derived rows of tests/golden/tail_blocks.json, on the GPU
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    from test_oracle_pins import _load_tail_rows, tail_row_input
+    for row in _load_tail_rows():
+        x = torch.from_numpy(tail_row_input(row).view(np.int16)).view(torch.bfloat16)
+        q, s = mx.mxfp4_quantize(x.cuda())
+        torch.cuda.synchronize()
+        assert [int(v) for v in to_np_u8(s)[0]] == row["scale_bytes"], row["name"]
+        assert bytes(to_np_u8(q)[0]).hex() == row["packed_hex"], row["name"]
+
+
 def test_quantize_rejects_bad_arguments():
     import block_scaled_mxfp4_bf16_gb300 as mx
     L = mx.load_library()
@@ -83,7 +112,7 @@ def test_quantize_rejects_bad_arguments():
     q = torch.empty(4, 32, dtype=torch.uint8, device="cuda")
     s = torch.empty(4, 2, dtype=torch.uint8, device="cuda")
     st = torch.cuda.current_stream().cuda_stream
-    assert L.mxfp4_quantize(x.data_ptr(), 4, 48, 64, q.data_ptr(), s.data_ptr(), st) == 2    # K % 32
+    assert L.mxfp4_quantize(x.data_ptr(), 4, 44, 64, q.data_ptr(), s.data_ptr(), st) == 2    # K % 8
     assert L.mxfp4_quantize(x.data_ptr(), 4, 64, 60, q.data_ptr(), s.data_ptr(), st) == 2    # ld < K
     assert L.mxfp4_quantize(x.data_ptr() + 2, 4, 64, 64, q.data_ptr(), s.data_ptr(), st) == 3  # misaligned
     assert L.mxfp4_quantize(None, 4, 64, 64, q.data_ptr(), s.data_ptr(), st) == 1
@@ -102,7 +131,7 @@ def _expected_token_blocks(rq: np.ndarray, rs: np.ndarray, M: int, K: int, m_til
     k_atoms = -(-K // 256)
     out = np.zeros((m_tiles, k_atoms, a_block), dtype=np.uint8)
     defined = np.zeros((m_tiles, k_atoms, a_block), dtype=bool)
-    nblk = K // 32
+    nblk = (K + 31) // 32
     for mt in range(m_tiles):
         for r in range(m_tile):
             row = mt * m_tile + r
@@ -120,21 +149,26 @@ def _expected_token_blocks(rq: np.ndarray, rs: np.ndarray, M: int, K: int, m_til
     return out.reshape(-1), defined.reshape(-1)
 
 
-@pytest.mark.parametrize("M,K,m_tile", [(40, 768, 0), (300, 512, 0), (33, 320, 0), (100, 1024, 64), (200, 7168, 0)])
+@pytest.mark.parametrize("M,K,m_tile", [(40, 768, 0), (300, 512, 0), (33, 320, 0), (100, 1024, 64), (200, 7168, 0),
+                                         (40, 776, 0), (33, 344, 0), (7, 8, 0), (200, 7176, 0)])
 def test_two_kernel_token_blocks_bit_exact(M, K, m_tile):
     # the standalone quantizer's output in the GEMM's token-block layout, read back from the
-    # workspace, byte for byte against the oracle's quantization of A (the last case has enough
-    # blocks for the one-lane-per-block kernel, the others use four lanes per block)
+    # workspace, byte for byte against the oracle's quantization of A (the (200, K) cases have
+    # enough blocks for the one-lane-per-block kernel, the others use four lanes per block; the
+    # K % 32 != 0 cases cut the last block, and A's row padding holds huge values that would
+    # change that block's scale if anything past K were read)
     import block_scaled_mxfp4_bf16_gb300 as mx
     N = 256
     a = workloads.random_bf16(M, K, seed=M * 7 + K)
+    a_store = torch.full((M, K + 24), 1.0e30, dtype=torch.bfloat16)
+    a_store[:, :K] = a
     plan = mx.mxfp4_gemm_plan(M, N, K, 2, 1, m_tile)
     assert plan["path"] == 2
     need = mx.mxfp4_gemm_workspace_size(M, N, K, 2, 1, m_tile)
     ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
     bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=5).cuda())
     packed = mx.mxfp4_prepack_b(bq, bs)
-    mx.mxfp4_gemm(a.cuda(), packed, N, workspace=ws, path=2, splits=1, m_tile=m_tile)
+    mx.mxfp4_gemm(a_store.cuda()[:, :K], packed, N, workspace=ws, path=2, splits=1, m_tile=m_tile)
     torch.cuda.synchronize()
     assert mx.mxfp4_device_status() == 0
     rq, rs = oracle.quantize(workloads.bf16_bits(a))

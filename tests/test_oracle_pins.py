@@ -93,6 +93,37 @@ def test_hand_worked_blocks(blk):
     assert got == codes
 
 
+TAIL_GOLD = os.path.join(os.path.dirname(__file__), "golden", "tail_blocks.json")
+
+
+def _load_tail_rows():
+    with open(TAIL_GOLD) as f:
+        return json.load(f)["rows"]
+
+
+def tail_row_input(row) -> np.ndarray:
+    """The fixture row as bf16 bit patterns [1, K] ("a-b" keys fill a range)."""
+    x = np.zeros(row["K"], np.uint16)
+    for key, h in row["x"].items():
+        lo, _, hi = key.partition("-")
+        x[int(lo):int(hi or lo) + 1] = int(h, 16)
+    return x.reshape(1, -1).copy()
+
+
+@pytest.mark.parametrize("row", _load_tail_rows(), ids=lambda r: r["name"])
+def test_hand_worked_tail_rows(row):
+    q, s = oracle.quantize(tail_row_input(row))
+    nblk = (row["K"] + 31) // 32
+    assert q.shape == (1, nblk * 16) and s.shape == (1, nblk)
+    assert [int(v) for v in s[0]] == row["scale_bytes"]
+    assert bytes(q[0]).hex() == row["packed_hex"]
+
+
+def test_k_not_multiple_of_8_is_refused():
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((1, 36), np.uint16))
+
+
 # ----------------------------------------------------------------------------- scale
 
 def _all_finite_positive_bf16():
@@ -224,19 +255,22 @@ def _exact_value(q, s, r, k) -> Fraction:
     return _decode_nibble(int(q[r, k // 2]), bool(k & 1)) * Fraction(2) ** (int(s[r, k // 32]) - 127)
 
 
-def test_gemm_closed_form_on_exact_mxfp4_operands():
-    # A, B already exact MXFP4 values (block max forced to +-6*2^s), so quantization is the
-    # identity and C = A . B^T exactly; M != N != K catches a transposed operand.
-    rng = np.random.default_rng(7)
-    M, N, K = 3, 5, 96
+@pytest.mark.parametrize("M,N,K", [(3, 5, 96), (2, 3, 40), (3, 4, 72), (1, 2, 8)])
+def test_gemm_closed_form_on_exact_mxfp4_operands(M, N, K):
+    # A, B already exact MXFP4 values (block max forced to +-6*2^s among the block's real
+    # elements), so quantization is the identity and C = A . B^T exactly over the K real
+    # elements, also when K cuts the last block (40, 72, 8); M != N != K catches a transposed
+    # operand.
+    rng = np.random.default_rng(7 + K)
     def make(rows):
         vals = np.zeros((rows, K))
         for r in range(rows):
-            for j in range(K // 32):
+            for j in range((K + 31) // 32):
+                n = min(32, K - 32 * j)
                 s = int(rng.integers(-4, 5))
-                codes = rng.integers(0, 16, 32)
-                codes[int(rng.integers(0, 32))] = 7 if rng.random() < 0.5 else 15
-                for i in range(32):
+                codes = rng.integers(0, 16, n)
+                codes[int(rng.integers(0, n))] = 7 if rng.random() < 0.5 else 15
+                for i in range(n):
                     vals[r, 32 * j + i] = math.ldexp(oracle.e2m1_decode(int(codes[i])), s)
         return vals
     a, b = make(M), make(N)
@@ -244,8 +278,9 @@ def test_gemm_closed_form_on_exact_mxfp4_operands():
     bb = np.vectorize(bf16_of_float, otypes=[np.uint16])(b)
     aq, as_ = oracle.quantize(ab)
     bq, bs = oracle.quantize(bb)
-    assert np.array_equal(oracle.dequantize(aq, as_), a)
-    assert np.array_equal(oracle.dequantize(bq, bs), b)
+    assert np.array_equal(oracle.dequantize(aq, as_)[:, :K], a)
+    assert np.array_equal(oracle.dequantize(bq, bs)[:, :K], b)
+    assert not oracle.dequantize(aq, as_)[:, K:].any()    # padding decodes to zero
     c = oracle.mxfp4_gemm_ref(aq, as_, bq, bs)
     for m in range(M):
         for n in range(N):

@@ -85,7 +85,7 @@ def test_cluster_residency_limits_the_split(mx):
 def test_errors(mx):
     import block_scaled_mxfp4_bf16_gb300 as m
     with pytest.raises(m.Mxfp4Error):
-        plan(mx, 8, 2112, 7200)          # K not a multiple of 64
+        plan(mx, 8, 2112, 7204)          # K not a multiple of 8
     with pytest.raises(m.Mxfp4Error):
         plan(mx, 0, 2112, 7168)
     with pytest.raises(m.Mxfp4Error):
