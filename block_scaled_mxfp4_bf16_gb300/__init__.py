@@ -169,6 +169,20 @@ def mxfp4_gemm_workspace_size(M: int, N: int, K: int, path: int = 0, splits: int
     return int(load_library().mxfp4_gemm_workspace_size_ex(M, N, K, _opts(path, splits, m_tile)))
 
 
+_WS_NEED: dict = {}
+
+
+def _ws_need(device: torch.device, M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> int:
+    """mxfp4_gemm_workspace_size, remembered per (device, shape, options): the plan depends only on
+    those, and the per-call query would otherwise cost a library round trip on every GEMM."""
+    key = (device.index, M, N, K, path, splits, m_tile)
+    need = _WS_NEED.get(key)
+    if need is None:
+        need = mxfp4_gemm_workspace_size(M, N, K, path, splits, m_tile) if M and N else 0
+        _WS_NEED[key] = need
+    return need
+
+
 def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
     _check(load_library().mxfp4_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
            "mxfp4_workspace_init")
@@ -201,13 +215,15 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
     st = _stream(stream)
-    need = mxfp4_gemm_workspace_size(M, N, K, path, splits, m_tile) if M and N else 0
     if workspace is None:
-        workspace = _workspace(a.device, need, stream)
+        dev = a.device
+        need = _ws_need(dev, M, N, K, path, splits, m_tile)
+        workspace = _workspace(dev, need, stream) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    opts = _opts(path, splits, m_tile) if (path or splits or m_tile) else None   # NULL: automatic plan
     _check(L.mxfp4_gemm_ex(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
-                           ws_ptr, ws_bytes, _opts(path, splits, m_tile), st), "mxfp4_gemm")
+                           ws_ptr, ws_bytes, opts, st), "mxfp4_gemm")
     return c
 
 
@@ -217,26 +233,30 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
     """mxfp4_gemm_host: A and C in (preferably pinned) host memory, device staging buffers a_dev
     [M, K] and c_dev [M, N] from the caller; asynchronous on `stream`. Returns c_host."""
     L = load_library()
-    if a_host.is_cuda or c_host.is_cuda:
-        raise ValueError("a_host and c_host must be host tensors")
-    for t, name in ((a_host, "a_host"), (c_host, "c_host"), (a_dev, "a_dev"), (c_dev, "c_dev")):
-        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
-            raise ValueError(f"{name} must be a 2-D bf16 tensor with unit column stride")
-    _dev(a_dev, "a_dev")
-    _dev(c_dev, "c_dev")
-    M, K = a_host.shape
-    if tuple(a_dev.shape) != (M, K) or a_dev.stride(0) != K or tuple(c_dev.shape) != (M, N) or c_dev.stride(0) != N:
-        raise ValueError("a_dev must be a packed [M, K] and c_dev a packed [M, N] tensor")
-    if tuple(c_host.shape) != (M, N):
+    # every tensor property is read once: this call sits on the per-step host path
+    bf16 = torch.bfloat16
+    if a_host.dtype != bf16 or c_host.dtype != bf16 or a_dev.dtype != bf16 or c_dev.dtype != bf16:
+        raise ValueError("a_host, c_host, a_dev and c_dev must be bf16 tensors")
+    if a_host.is_cuda or c_host.is_cuda or not a_dev.is_cuda or not c_dev.is_cuda:
+        raise ValueError("a_host and c_host must be host tensors, a_dev and c_dev CUDA tensors")
+    a_shape, c_shape = a_host.shape, c_host.shape
+    a_stride, c_stride = a_host.stride(), c_host.stride()
+    if len(a_shape) != 2 or len(c_shape) != 2 or a_stride[1] != 1 or c_stride[1] != 1:
+        raise ValueError("a_host and c_host must be 2-D with unit column stride")
+    M, K = a_shape
+    if tuple(c_shape) != (M, N):
         raise ValueError("c_host must be [M, N]")
+    if a_dev.shape != (M, K) or a_dev.stride() != (K, 1) or c_dev.shape != (M, N) or c_dev.stride() != (N, 1):
+        raise ValueError("a_dev must be a packed [M, K] and c_dev a packed [M, N] tensor")
     st = _stream(stream)
-    need = mxfp4_gemm_workspace_size(M, N, K) if M and N else 0
     if workspace is None:
-        workspace = _workspace(a_dev.device, need, stream)
+        dev = a_dev.device
+        need = _ws_need(dev, M, N, K)
+        workspace = _workspace(dev, need, stream) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(L.mxfp4_gemm_host(a_host.data_ptr(), M, K, a_host.stride(0), packed_b.data_ptr(), N, c_host.data_ptr(),
-                             c_host.stride(0), a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st),
+    _check(L.mxfp4_gemm_host(a_host.data_ptr(), M, K, a_stride[0], packed_b.data_ptr(), N, c_host.data_ptr(),
+                             c_stride[0], a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st),
            "mxfp4_gemm_host")
     return c_host
 

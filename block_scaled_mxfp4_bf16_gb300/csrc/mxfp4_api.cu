@@ -473,11 +473,23 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
         if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // one linear copy when the host rows are contiguous, a strided one otherwise
     const size_t a_row = static_cast<size_t>(K) * 2, c_row = static_cast<size_t>(N) * 2;
-    cudaError_t e = lda == K ? cudaMemcpyAsync(a_dev, a_host, a_row * M, cudaMemcpyHostToDevice, s)
-                             : cudaMemcpy2DAsync(a_dev, a_row, a_host, static_cast<size_t>(lda) * 2, a_row,
-                                                 static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+    // A: page-locked host memory mapped into the device's address space (16-byte aligned rows)
+    // is staged by a kernel that reads it in place, so the launch chain from the previous call's
+    // GEMM to this one is never broken by a copy-engine transfer; anything else is copied.
+    cudaPointerAttributes a_attr = {};
+    const void* a_mapped = nullptr;
+    if (cudaPointerGetAttributes(&a_attr, a_host) == cudaSuccess && a_attr.type == cudaMemoryTypeHost)
+        a_mapped = a_attr.devicePointer;
+    else
+        cudaGetLastError();   // clear the error an unregistered pointer leaves behind
+    cudaError_t e;
+    if (a_mapped && aligned(a_mapped, 16) && lda % 8 == 0)
+        e = launch_stage_rows(a_mapped, lda, a_dev, M, K, s);
+    else   // one linear copy when the host rows are contiguous, a strided one otherwise
+        e = lda == K ? cudaMemcpyAsync(a_dev, a_host, a_row * M, cudaMemcpyHostToDevice, s)
+                     : cudaMemcpy2DAsync(a_dev, a_row, a_host, static_cast<size_t>(lda) * 2, a_row,
+                                         static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
     // Page-locked host memory mapped into the device's address space takes C straight from the
     // epilogue's stores (no separate device -> host copy); anything else goes through c_dev.

@@ -168,6 +168,28 @@ prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, i
     }
 }
 
+// Host rows -> device rows for the host-buffer GEMM: one 16-byte piece per thread, read from
+// page-locked host memory mapped into the device's address space (zero-copy) BEFORE the wait on
+// the previous grid -- the host rows never depend on it, so the C2C round trip overlaps that
+// grid's tail -- and stored after it, since the previous grid may still read the destination.
+// Unlike a copy-engine transfer, a kernel keeps the programmatic-dependent-launch chain from the
+// previous GEMM through this copy to the next GEMM.
+__global__ void __launch_bounds__(256)
+stage_rows_kernel(const uint4* __restrict__ src, int64_t src_row16, uint4* __restrict__ dst, int64_t row16,
+                  int64_t pieces) {
+    pdl_launch_dependents();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    int64_t r = 0, c = 0;
+    if (i < pieces) {
+        r = i / row16;
+        c = i - r * row16;
+        v = src[r * src_row16 + c];
+    }
+    pdl_wait_prior_grid();
+    if (i < pieces) dst[r * row16 + c] = v;
+}
+
 constexpr int64_t kQuantFourLaneMaxBlocks = 16384;
 
 static int grid_for(int64_t items, int threads) {
@@ -195,6 +217,15 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
                           K, ld, blocks, m_tile, m_tiles, k_atoms, a_block);
     return launch_pdl(quantize_blocks_kernel, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K, ld,
                       blocks, m_tile, m_tiles, k_atoms, a_block);
+}
+
+cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, cudaStream_t s) {
+    const int threads = 256;
+    const int64_t row16 = K / 8, pieces = rows * row16;
+    const int64_t blocks = (pieces + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    return launch_pdl(stage_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                      static_cast<const uint4*>(src), lda / 8, static_cast<uint4*>(dst), row16, pieces);
 }
 
 cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out, cudaStream_t s) {

@@ -166,11 +166,14 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
                     int *path, int *splits, int *m_tile, int *ctas, int *stages);
 
 /*
- * mxfp4_gemm_host -- mxfp4_gemm for A and C in host memory: on `stream`, copy A (rows of K
+ * mxfp4_gemm_host -- mxfp4_gemm for A and C in host memory: on `stream`, move A (rows of K
  * elements, row stride lda) into the caller's device buffer a_dev, run mxfp4_gemm, and deliver C
  * into c_host (row stride ldc): page-locked host memory mapped into the device's address space
  * (cudaHostAlloc / cudaHostRegister) receives C straight from the GEMM's stores; any other host
- * memory receives it by a copy from the caller's device buffer c_dev. The call is
+ * memory receives it by a copy from the caller's device buffer c_dev. Likewise A: from mapped
+ * page-locked memory with 16-byte aligned rows (lda % 8 == 0) a small kernel reads it in place
+ * and writes a_dev (it chains with the GEMMs by programmatic dependent launch, so back-to-back
+ * calls overlap); from any other host memory it is copied. The call is
  * asynchronous like mxfp4_gemm: c_host is valid once `stream` has completed, and a_host /
  * c_host must stay valid until then (page-locked host memory lets the copies overlap other
  * work; pageable memory works but the copies then block the host).

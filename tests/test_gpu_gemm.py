@@ -199,28 +199,36 @@ def test_plan_invariants_over_a_shape_grid():
 
 
 def test_gemm_host_buffers_match_device_call():
-    # mxfp4_gemm_host: strided pinned host A in, strided pinned host C out, bit-identical to the
-    # device call; an undersized workspace is refused before anything is copied.
+    # mxfp4_gemm_host: strided host A in, strided host C out, bit-identical to the device call,
+    # for every way A and C can travel -- A from mapped page-locked memory by the staging kernel
+    # (16-byte rows) or by a copy (pageable memory, or a row stride that is not a multiple of 8),
+    # C written by the GEMM into mapped page-locked memory or copied back; an undersized
+    # workspace is refused before anything is copied.
     mx = _mx()
-    for M, N, K in ((8, 2112, 7168), (40, 300, 512)):
+    for M, N, K in ((8, 2112, 7168), (40, 300, 512), (5, 200, 72)):
         a = workloads.random_bf16(M, K, seed=M + 7)
         b = workloads.random_bf16(N, K, seed=N + 7)
         bq, bs = mx.mxfp4_quantize(b.cuda())
         packed = mx.mxfp4_prepack_b(bq, bs)
         want = mx.mxfp4_gemm(a.cuda(), packed, N)
-        a_store = torch.zeros(M, K + 64, dtype=torch.bfloat16).pin_memory()
-        a_store[:, :K] = a
-        for pinned in (True, False):   # mapped page-locked C (written by the GEMM) or a copy
-            c_store = torch.full((M, N + 3), 5.0, dtype=torch.bfloat16)
-            if pinned:
-                c_store = c_store.pin_memory()
-            a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-            c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-            mx.mxfp4_gemm_host(a_store[:, :K], packed, N, c_store[:, :N], a_dev, c_dev)
-            torch.cuda.synchronize()
-            assert mx.mxfp4_device_status() == 0
-            assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16)), pinned
-            assert torch.all(c_store[:, N:] == 5.0)
+        for a_kind, pad in (("pinned", 64), ("pageable", 64), ("pinned", 3)):
+            a_store = torch.full((M, K + pad), 1.0e30, dtype=torch.bfloat16)
+            if a_kind == "pinned":
+                a_store = a_store.pin_memory()
+            a_store[:, :K] = a
+            for c_pinned in (True, False):   # mapped page-locked C (written by the GEMM) or a copy
+                c_store = torch.full((M, N + 3), 5.0, dtype=torch.bfloat16)
+                if c_pinned:
+                    c_store = c_store.pin_memory()
+                a_dev = torch.full((M, K), 7.0, dtype=torch.bfloat16, device="cuda")
+                c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+                mx.mxfp4_gemm_host(a_store[:, :K], packed, N, c_store[:, :N], a_dev, c_dev)
+                torch.cuda.synchronize()
+                assert mx.mxfp4_device_status() == 0
+                what = (M, N, K, a_kind, pad, c_pinned)
+                assert torch.equal(a_dev.cpu().view(torch.int16), a.view(torch.int16)), what
+                assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16)), what
+                assert torch.all(c_store[:, N:] == 5.0)
     # M = 300 needs a workspace (two-kernel path): a one-byte one is refused, C untouched
     M, N, K = 300, 256, 256
     need = mx.mxfp4_gemm_workspace_size(M, N, K)
