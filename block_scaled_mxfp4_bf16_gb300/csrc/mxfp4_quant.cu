@@ -169,25 +169,23 @@ prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, i
 }
 
 // Host rows -> device rows for the host-buffer GEMM: one 16-byte piece per thread, read from
-// page-locked host memory mapped into the device's address space (zero-copy) BEFORE the wait on
-// the previous grid -- the host rows never depend on it, so the C2C round trip overlaps that
-// grid's tail -- and stored after it, since the previous grid may still read the destination.
-// Unlike a copy-engine transfer, a kernel keeps the programmatic-dependent-launch chain from the
-// previous GEMM through this copy to the next GEMM.
+// page-locked host memory mapped into the device's address space (zero-copy). Both the read and
+// the store come after the wait on the previous grid: that grid may still read the destination,
+// and it may also be writing the source (a chained call whose C, stored into mapped host memory,
+// is this call's A), so the stream order a copy would give is kept. Unlike a copy-engine
+// transfer, a kernel keeps the programmatic-dependent-launch chain from the previous GEMM
+// through this copy to the next GEMM, so their launches still overlap.
 __global__ void __launch_bounds__(256)
 stage_rows_kernel(const uint4* __restrict__ src, int64_t src_row16, uint4* __restrict__ dst, int64_t row16,
                   int64_t pieces) {
     pdl_launch_dependents();
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    int64_t r = 0, c = 0;
-    if (i < pieces) {
-        r = i / row16;
-        c = i - r * row16;
-        v = src[r * src_row16 + c];
-    }
     pdl_wait_prior_grid();
-    if (i < pieces) dst[r * row16 + c] = v;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < pieces) {
+        const int64_t r = i / row16;
+        const int64_t c = i - r * row16;
+        dst[r * row16 + c] = src[r * src_row16 + c];
+    }
 }
 
 constexpr int64_t kQuantFourLaneMaxBlocks = 16384;

@@ -132,6 +132,11 @@ int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  *              NULL when that size is 0. Calls sharing a workspace must be ordered (same
  *              stream, or synchronized); overlapping calls on one workspace race.
  *   K        : positive multiple of 8.  M == 0 or N == 0 is a no-op.
+ * Ordering: the call waits for the work before it on `stream` before it reads A or writes C.
+ * The weights in packed_b are requested before that wait (they are meant to be constant), so
+ * packed_b must not be written by a kernel that is still running when the call is enqueued and
+ * that lets dependent launches start early (programmatic dependent launch); ordinary kernels,
+ * copies and this library's own calls never do.
  * A is quantized exactly like mxfp4_quantize (bit-identical codes and scales). With split-K
  * the K slices of an output tile run as one thread-block cluster and their fp32 partial
  * sums are added in slice order through distributed shared memory, so results are
@@ -173,7 +178,8 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
  * memory receives it by a copy from the caller's device buffer c_dev. Likewise A: from mapped
  * page-locked memory with 16-byte aligned rows (lda % 8 == 0) a small kernel reads it in place
  * and writes a_dev (it chains with the GEMMs by programmatic dependent launch, so back-to-back
- * calls overlap); from any other host memory it is copied. The call is
+ * calls overlap; it still reads A only after the work before it on `stream` has finished, so A
+ * may be the C of a previous call); from any other host memory it is copied. The call is
  * asynchronous like mxfp4_gemm: c_host is valid once `stream` has completed, and a_host /
  * c_host must stay valid until then (page-locked host memory lets the copies overlap other
  * work; pageable memory works but the copies then block the host).

@@ -229,6 +229,25 @@ def test_gemm_host_buffers_match_device_call():
                 assert torch.equal(a_dev.cpu().view(torch.int16), a.view(torch.int16)), what
                 assert torch.equal(c_store[:, :N].view(torch.int16), want.cpu().view(torch.int16)), what
                 assert torch.all(c_store[:, N:] == 5.0)
+    # chained host-buffer calls: the first call's C (stored by its GEMM into mapped page-locked
+    # memory) is the second call's A, so the second call must see the first one's stores
+    M, N = 8, 512
+    a1 = workloads.random_bf16(M, 512, seed=21).pin_memory()
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, 512, seed=22).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c1 = torch.full((M, N), 3.0, dtype=torch.bfloat16).pin_memory()
+    c2 = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    a_dev = [torch.empty(M, 512, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    c_dev = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for _ in range(3):
+        c1.fill_(3.0)
+        mx.mxfp4_gemm_host(a1, packed, N, c1, a_dev[0], c_dev[0])
+        mx.mxfp4_gemm_host(c1, packed, N, c2, a_dev[1], c_dev[1])
+        torch.cuda.synchronize()
+        want1 = mx.mxfp4_gemm(a1.cuda(), packed, N)
+        want2 = mx.mxfp4_gemm(want1, packed, N)
+        assert torch.equal(c1.view(torch.int16), want1.cpu().view(torch.int16))
+        assert torch.equal(c2.view(torch.int16), want2.cpu().view(torch.int16))
     # M = 300 needs a workspace (two-kernel path): a one-byte one is refused, C untouched
     M, N, K = 300, 256, 256
     need = mx.mxfp4_gemm_workspace_size(M, N, K)
