@@ -130,6 +130,30 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
               GemmPlan* plan, const int* cluster_caps = nullptr);
 size_t packed_b_bytes(int64_t N, int64_t K);
 
+// Exact unsigned 32-bit division by a divisor fixed at launch: the round-up multiplier with one
+// correction step of Granlund and Montgomery, "Division by invariant integers using
+// multiplication" (1994): q = (t + ((n - t) >> s1)) >> s2 with t = umulhi(m, n), for every
+// n < 2^32 and 1 <= d < 2^31. A runtime integer division costs tens of dependent instructions
+// on the quantizers' critical path; this costs four.
+struct FastDiv {
+    uint32_t m, s1, s2;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;   // ceil(log2 d)
+    while ((uint64_t(1) << l) < d) ++l;
+    FastDiv f;
+    f.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+    f.s1 = l < 1 ? l : 1;
+    f.s2 = l > 1 ? l - 1 : 0;
+    return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+    const uint32_t t = __umulhi(f.m, n);
+    return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+#endif
+
 // Kernel launchers (return cudaError_t).
 // Natural layout: q [rows, nblk*16], scales [rows, nblk], nblk = ceil(K/32) (K % 8 == 0).
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q,

@@ -99,6 +99,9 @@ struct QuantSlice {
 __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, const GemmArgs& p,
                                                volatile uint32_t* abort_flag) {
     const int lane = qt & 31;
+    // idx / m_valid as a multiply-high (exact for idx < 2^16, m_valid <= 256), set up off the path
+    const uint32_t magic = 0xFFFFFFFFu / static_cast<uint32_t>(q.m_valid) + 1u;
+    const bool one_row = q.m_valid == 1;
     const bool got = mbar_wait(q.a_raw, 0, q.lim);
     if (qt == 96) MXFP4_PHASE(10);
     if (!got) fail(p, abort_flag);
@@ -112,7 +115,8 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
             // rows run fastest: eight consecutive items read eight rows (distinct banks) and
             // write eight rows of one chunk column (distinct swizzled chunks)
             const int idx = first + u * nq;
-            kk[u] = idx < total ? idx / q.m_valid : q.kblk;        // kblk: nothing to read
+            const int kq = one_row ? idx : static_cast<int>(__umulhi(static_cast<uint32_t>(idx), magic));
+            kk[u] = idx < total ? kq : q.kblk;        // kblk: nothing to read
             rr[u] = idx < total ? idx - kk[u] * q.m_valid : 0;
             if (kk[u] < q.kblk) {
                 const uint4* src = reinterpret_cast<const uint4*>(q.raw + rr[u] * q.raw_row + kk[u] * 64);
@@ -558,13 +562,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             const uint32_t bar_addr = smem_addr(red_bar);
             const uint32_t own_off = static_cast<uint32_t>((split * kTileN + nl) * stride) * 4u;
             for (int cb = half * 32; cb < m_valid; cb += 64) {
-                uint32_t r[32];
-                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                // destinations first: their division and address mapping overlap the loads below
                 int owner = cb / rows_per;
                 int lm = cb - owner * rows_per;
                 uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
                                 static_cast<uint32_t>(lm) * 4u;
                 uint32_t peer_bar = map_to_rank(bar_addr, static_cast<uint32_t>(owner));
+                uint32_t r[32];
+                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     if (cb + i < m_valid) {   // rows past M in this group of 4 carry padding, never stored
@@ -632,12 +637,13 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         const uint32_t recv_addr = smem_addr(sRecv);
         const uint32_t own_off = static_cast<uint32_t>(split * rows_per * kTileN + nl) * 4u;
         for (int cb = half * 32; cb < m_valid; cb += 64) {
-            uint32_t r[32];
-            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+            // destinations first: their division and address mapping overlap the loads below
             int owner = cb / rows_per;
             int lm = cb - owner * rows_per;
             uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
                             static_cast<uint32_t>(lm) * kTileN * 4u;
+            uint32_t r[32];
+            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 if (cb + i < m_valid) {

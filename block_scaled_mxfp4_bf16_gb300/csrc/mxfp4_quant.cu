@@ -33,20 +33,31 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t
     }
 }
 
+// Item index -> (quotient by a launch-fixed divisor): FastDiv when every item index fits 32 bits
+// (kNarrow), a 64-bit division otherwise.
+template <bool kNarrow>
+__device__ __forceinline__ int64_t div_items(int64_t n, int64_t d, const FastDiv& f) {
+    if constexpr (kNarrow) return fast_div(static_cast<uint32_t>(n), f);
+    else return n / d;
+}
+
 // Token blocks, one lane per 1x32 block (layout in internal.h): block (mt, j) at
 // (mt * k_atoms + j) * a_block. Items run
 // over every (row, block) of the padded [m_tiles*m_tile, k_atoms*256] matrix, so padding rows and
 // the K tail are written as zeros. Four consecutive lanes own the four blocks of one scale word.
+// fd_row divides by the items of a padded row (8 * k_atoms), fd_mtile by m_tile.
+template <bool kNarrow>
 __global__ void __launch_bounds__(256)
 quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
-                       uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
+                       uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block,
+                       FastDiv fd_row, FastDiv fd_mtile) {
     pdl_launch_dependents();
     const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * row_items;   // multiple of 8
     {   // warm L2 with this thread's first block while the previous grid finishes (see prefetch_l2)
         const int64_t it0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-        const int64_t r = it0 / row_items, kbp = it0 - (it0 / row_items) * row_items;
+        const int64_t r = div_items<kNarrow>(it0, row_items, fd_row), kbp = it0 - r * row_items;
         if (it0 < items && r < rows && kbp < nblk) prefetch_l2(x + r * ld + kbp * 32);
     }
     pdl_wait_prior_grid();
@@ -58,7 +69,7 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
          wbase += stride) {
         const int64_t it = wbase + lane;
         const bool in_range = it < items;
-        const int64_t r = in_range ? it / row_items : 0;
+        const int64_t r = in_range ? div_items<kNarrow>(it, row_items, fd_row) : 0;
         const int64_t kbp = in_range ? it - r * row_items : 0;     // block index within the padded row
         const bool live = in_range && r < rows && kbp < nblk;
         uint32_t w[16], out[4] = {0u, 0u, 0u, 0u}, byte = 0u;
@@ -70,7 +81,7 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
         if (in_range) {
-            const int mt = static_cast<int>(r / m_tile);
+            const int mt = static_cast<int>(div_items<kNarrow>(r, m_tile, fd_mtile));
             const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
             const uint32_t c = static_cast<uint32_t>(kbp & 7);
             uint8_t* blk = blocks + (static_cast<size_t>(mt) * k_atoms + static_cast<size_t>(kbp >> 3)) * a_block;
@@ -88,10 +99,12 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
 // block's amax is combined over the four lanes, and each lane writes its 4 bytes of codes. The
 // eight blocks of a warp are two scale words (four consecutive blocks of one row each),
 // assembled by shuffles. Shorter per-thread chains than one lane per block: the kernel sits
-// between two GEMMs on the critical path, so its latency is what counts.
+// between two GEMMs on the critical path, so its latency is what counts (launched for at most
+// kQuantFourLaneMaxBlocks items, so item indices fit 32 bits and divide by FastDiv).
 __global__ void __launch_bounds__(256)
 quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
-                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block) {
+                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block,
+                        FastDiv fd_row, FastDiv fd_mtile) {
     pdl_launch_dependents();
     const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
@@ -102,14 +115,14 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
     const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     {   // warm L2 with this lane's first 16 bytes while the previous grid finishes (see prefetch_l2)
         const int64_t it0 = warp_id * 8 + (lane >> 2);
-        const int64_t r = it0 / row_items, kbp = it0 - (it0 / row_items) * row_items;
+        const int64_t r = fast_div(static_cast<uint32_t>(it0), fd_row), kbp = it0 - r * row_items;
         if (it0 < items && r < rows && kbp * 32 + part * 8 < K) prefetch_l2(x + r * ld + kbp * 32 + part * 8);
     }
     pdl_wait_prior_grid();
     // the loop bound is uniform per warp, so the shuffles below always see all 32 lanes
     for (int64_t base = warp_id * 8; base < items; base += warps * 8) {
         const int64_t it = base + (lane >> 2);
-        const int64_t r = it / row_items;
+        const int64_t r = fast_div(static_cast<uint32_t>(it), fd_row);
         const int64_t kbp = it - r * row_items;          // block index within the padded row
         const bool live = r < rows && kbp < nblk;
         uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -130,7 +143,7 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
         uint32_t word = part == 0 ? byte << (8 * ((lane >> 2) & 3)) : 0u;
         word |= __shfl_xor_sync(0xffffffffu, word, 4);
         word |= __shfl_xor_sync(0xffffffffu, word, 8);
-        const int mt = static_cast<int>(r / m_tile);
+        const int mt = static_cast<int>(fast_div(static_cast<uint32_t>(r), fd_mtile));
         const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
         const uint32_t c = static_cast<uint32_t>(kbp & 7);
         uint8_t* blk = blocks + (static_cast<size_t>(mt) * k_atoms + static_cast<size_t>(kbp >> 3)) * a_block;
@@ -210,11 +223,18 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * 8 * k_atoms;
     // few blocks: four lanes each (shorter chains, the launch is latency-bound); many blocks: one
     // lane each (less total work; measured faster for 256x7168 and slower for 64x2048)
+    const FastDiv fd_row = make_fastdiv(8u * static_cast<uint32_t>(k_atoms));
+    const FastDiv fd_mtile = make_fastdiv(static_cast<uint32_t>(m_tile));
     if (items <= kQuantFourLaneMaxBlocks)
         return launch_pdl(quantize_blocks4_kernel, dim3(grid_for(items * 4, threads)), dim3(threads), 0, s, x, rows,
-                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block);
-    return launch_pdl(quantize_blocks_kernel, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K, ld,
-                      blocks, m_tile, m_tiles, k_atoms, a_block);
+                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+    // item indices (and the grid-stride overshoot, below one more grid) within 32 bits: FastDiv
+    const int64_t span = items + static_cast<int64_t>(grid_for(items, threads)) * threads;
+    if (span <= static_cast<int64_t>(UINT32_MAX))
+        return launch_pdl(quantize_blocks_kernel<true>, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows,
+                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+    return launch_pdl(quantize_blocks_kernel<false>, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K,
+                      ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
 }
 
 cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, cudaStream_t s) {
