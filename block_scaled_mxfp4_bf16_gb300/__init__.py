@@ -183,6 +183,20 @@ def _ws_need(device: torch.device, M: int, N: int, K: int, path: int = 0, splits
     return need
 
 
+_PACKED_NEED: dict = {}
+
+
+def _check_packed(packed_b: torch.Tensor, N: int, K: int) -> None:
+    """The packed weights must cover mxfp4_prepack_b_size(N, K) bytes on the GEMM's device: the
+    kernel streams that many bytes, so a smaller buffer would be read past its end."""
+    need = _PACKED_NEED.get((N, K))
+    if need is None:
+        need = mxfp4_prepack_b_size(N, K)
+        _PACKED_NEED[(N, K)] = need
+    if packed_b.nbytes < need or not packed_b.is_cuda:
+        raise ValueError(f"packed_b must be a CUDA buffer of at least mxfp4_prepack_b_size({N}, {K}) = {need} bytes")
+
+
 def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
     _check(load_library().mxfp4_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
            "mxfp4_workspace_init")
@@ -210,6 +224,8 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
         raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
     M, K = a.shape
+    if M and N:
+        _check_packed(packed_b, N, K)
     if c is None:
         c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
     if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
@@ -246,6 +262,8 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
     M, K = a_shape
     if tuple(c_shape) != (M, N):
         raise ValueError("c_host must be [M, N]")
+    if M and N:
+        _check_packed(packed_b, N, K)
     if a_dev.shape != (M, K) or a_dev.stride() != (K, 1) or c_dev.shape != (M, N) or c_dev.stride() != (N, 1):
         raise ValueError("a_dev must be a packed [M, K] and c_dev a packed [M, N] tensor")
     st = _stream(stream)

@@ -124,6 +124,11 @@ def test_gemm_empty_and_errors():
     if need:
         assert L.mxfp4_gemm(a.data_ptr(), 4, 128, 128, packed.data_ptr(), 64, c.data_ptr(), 64, None, 0, st) == 7
     assert L.mxfp4_prepack_b_size(64, 100) == 0
+    # the binding refuses packed weights smaller than the shape needs, before any launch
+    with pytest.raises(ValueError):
+        mx.mxfp4_gemm(a, packed[:1024], 64)
+    with pytest.raises(ValueError):
+        mx.mxfp4_gemm(a, packed, 64 + 128)        # N past the packed tiles
 
 
 def test_timeout_is_reported_not_hung():
