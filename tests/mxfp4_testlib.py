@@ -52,7 +52,7 @@ def check_tolerance(c: np.ndarray, c_ref: np.ndarray, what: str) -> float:
 
 
 def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: int = 0, lda_pad: int = 0,
-             ldc_pad: int = 0, canary: float = 777.0):
+             ldc_pad: int = 0, canary: float = 777.0, m_tile: int = 0):
     """Quantize B and prepack it on the GPU, run mxfp4_gemm, check the B bytes against the
     oracle and that nothing outside C[:M,:N] was written. Returns (C as fp64 [M,N], Bq, Bs)."""
     import block_scaled_mxfp4_bf16_gb300 as mx
@@ -67,7 +67,7 @@ def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: in
     a = a_store[:, :K]
     c_store = torch.full((M + 1, N + ldc_pad), canary, dtype=torch.bfloat16, device="cuda")
     c = c_store[:M, :N]
-    mx.mxfp4_gemm(a, packed, N, c=c, path=path, splits=splits)
+    mx.mxfp4_gemm(a, packed, N, c=c, path=path, splits=splits, m_tile=m_tile)
     torch.cuda.synchronize()
     st = mx.mxfp4_device_status()
     assert st == 0, f"device status {st}"
