@@ -286,10 +286,18 @@ def fp4_peak_tflops():
         return 13500.0, "nominal"
 
 
-def cpu_oracle_step_time(w, budget_s: float = 12.0):
+def cpu_oracle_step_time(w, budget_s: float = 12.0, threads: int = 0):
     """The oracle as it stands on the host cores: quantize A, dequantize, fp64 GEMM, bf16 cast.
-    Bounded sample: whole calls of workload w, repeated until budget_s has passed (min 1)."""
+    Bounded sample: whole calls of workload w, repeated until budget_s has passed (min 1).
+    threads > 0 runs it on that many threads (then restores the default)."""
     import oracle
+    if threads > 0:
+        default = oracle.num_threads()
+        oracle.set_num_threads(threads)
+        try:
+            return cpu_oracle_step_time(w, budget_s)
+        finally:
+            oracle.set_num_threads(default)
     a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
     bq, bs = oracle.quantize(workloads.bf16_bits(b_cpu))     # B pre-quantized: not timed
     a_bits = workloads.bf16_bits(a_cpu)
@@ -392,8 +400,11 @@ def main():
     cpu = None
     if not args.no_cpu:
         c = cpu_oracle_step_time(w)
+        c1 = cpu_oracle_step_time(w, budget_s=6.0, threads=1)
         cpu = {"value": c["us_per_call"], "unit": "us/call", "cores": c["cores"], "kind": "oracle",
-               "sample": c["sample"]}
+               "sample": c["sample"],
+               "single_core": {"value": c1["us_per_call"], "unit": "us/call", "cores": c1["cores"],
+                               "sample": c1["sample"]}}
     gbs = w.algorithmic_bytes / (main_res["us_per_call"] * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(t_us, 4), "unit": "us/call", "n_gpus": world, "steps": args.steps,

@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.POINTER(ctypes.c_uint32)]
             L.oracle_num_threads.restype = ctypes.c_int
             L.oracle_num_threads.argtypes = []
+            L.oracle_set_num_threads.restype = None
+            L.oracle_set_num_threads.argtypes = [ctypes.c_int]
             _LIB = L
     return _LIB
 
@@ -96,6 +98,11 @@ def _p(a: np.ndarray, t):
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (for timing it on one core)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
