@@ -40,9 +40,17 @@ def _deps() -> list[str]:
                                + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
+FLAGS_STAMP = os.path.join(BUILD_DIR, "lib.flags")   # the extra flags of the last link
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+    """The in-tree library exists, is newer than every source and was built without extra flags
+    (a phase-trace build, say, is never taken for the product build)."""
+    if not os.path.exists(LIB_PATH) or not os.path.exists(FLAGS_STAMP):
         return False
+    with open(FLAGS_STAMP) as fh:
+        if fh.read().strip():
+            return False
     t = os.path.getmtime(LIB_PATH)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
@@ -73,6 +81,8 @@ def build(force: bool = False, extra_flags: list[str] | None = None, verbose: bo
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(FLAGS_STAMP, "w") as fh:
+        fh.write(" ".join(extra_flags or []))
     return LIB_PATH
 
 
