@@ -18,8 +18,8 @@ from . import build as _build
 
 __all__ = [
     "Mxfp4Error", "load_library", "mxfp4_quantize", "mxfp4_prepack_b_size", "mxfp4_prepack_b",
-    "mxfp4_gemm_workspace_size", "mxfp4_workspace_init", "mxfp4_gemm", "mxfp4_gemm_plan",
-    "mxfp4_device_status", "mxfp4_selftest_timeout", "mxfp4_version",
+    "mxfp4_gemm_workspace_size", "mxfp4_workspace_init", "mxfp4_gemm", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
+    "mxfp4_gemm_plan", "mxfp4_gemm_plan_model", "mxfp4_device_status", "mxfp4_selftest_timeout", "mxfp4_version",
 ]
 
 _LOCK = threading.Lock()
@@ -82,6 +82,8 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_gemm_plan.restype = _int
             L.mxfp4_gemm_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
             L.mxfp4_gemm_host.restype = _int
+            L.mxfp4_gemm_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
+            L.mxfp4_gemm_noalloc.restype = _int
             L.mxfp4_gemm_plan_model.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_Options), _int,
                                                 ctypes.POINTER(_int), ctypes.POINTER(_PlanInfo)]
             L.mxfp4_gemm_plan_model.restype = _int
@@ -277,6 +279,26 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
                              c_stride[0], a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st),
            "mxfp4_gemm_host")
     return c_host
+
+
+def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """mxfp4_gemm without a workspace: the automatic plan with the library's own fixed scratch
+    (for callers that must not allocate device memory; calls on one device must be ordered)."""
+    L = load_library()
+    _dev(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    M, K = a.shape
+    if M and N:
+        _check_packed(packed_b, N, K)
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
+    _check(L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
+                                _stream(stream)), "mxfp4_gemm_noalloc")
+    return c
 
 
 _PLAN_FIELDS = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated",

@@ -56,6 +56,23 @@ def test_noalloc_matches_gemm_twice(M, N, K):
         assert ok, f"call {call}: worst ratio {worst:.3g}"
 
 
+def test_noalloc_python_binding_matches_c_call():
+    mx, L = _lib()
+    M, N, K = 40, 300, 520                  # two-kernel path (scratch in use), K cut inside a block
+    a = workloads.random_bf16(M, K, seed=9).cuda()
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=10).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c_py = mx.mxfp4_gemm_noalloc(a, packed, N)
+    c_c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, K, packed.data_ptr(), N, c_c.data_ptr(), N,
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(c_py.view(torch.int16), c_c.view(torch.int16))
+    # same automatic plan, deterministic kernels: bit-identical to the workspace call
+    assert torch.equal(c_py.view(torch.int16), mx.mxfp4_gemm(a, packed, N).view(torch.int16))
+
+
 def test_noalloc_rejects_scratch_beyond_its_limit():
     mx, L = _lib()
     # the two-kernel path keeps the quantized A (M*K/2 bytes) in the scratch: 8192 x 8192
