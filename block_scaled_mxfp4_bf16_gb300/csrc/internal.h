@@ -16,6 +16,7 @@ constexpr int kAtomK = 256;                // K elements per pipeline step (128-
 constexpr int kMaxMTile = 256;             // tokens per tile (the MMA's N)
 constexpr int kMaxSplits = 16;             // K slices per tile = cluster size (> 8 needs the non-portable opt-in)
 constexpr int kAutoMaxSplits = 8;          // the automatic plan stays within portable cluster sizes
+constexpr int kAutoMaxSplitsTwoKernel = 5;  // two-kernel path: 6 slices measured slower than 5
 constexpr uint32_t kBRowsBytes = kTileN * kAtomK / 2;    // 16 KB of e2m1 per weight tile per atom
 constexpr uint32_t kSfChunk = 512;         // 128 rows x 4 scale bytes
 constexpr size_t kSmemLimit = 227 * 1024;

@@ -28,6 +28,8 @@ def plan(mx, M, N, K, **kw):
     (32, 4096, 512, 2, 1, 32),       # standalone quantize + GEMM
     (64, 7168, 2048, 2, 1, 64),
     (256, 4096, 7168, 2, 2, 128),    # 128-token tiles, 2 slices (bulk split-K)
+    (16, 2112, 7168, 2, 5, 16),      # fused would be two blocks per thread: two-kernel, 5 slices
+    (4, 2880, 512, 1, 1, 16),        # fused, one 1x32 block per thread or less
 ])
 def test_workload_plans(mx, M, N, K, path, splits, m_tile):
     p = plan(mx, M, N, K)
