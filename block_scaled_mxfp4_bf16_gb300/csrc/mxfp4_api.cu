@@ -167,6 +167,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     // Token tile: all of M up to 128; 128 up to M = 512 (half the A traffic and reduction per
     // CTA of a 256 tile, measured faster on 256x4096x7168); 256 beyond.
     p.m_tile = M <= 128 ? static_cast<int>(cdiv(M, 16) * 16) : (M <= 512 ? 128 : kMaxMTile);
+    // 17..32 tokens with at most two 256-K steps: two 16-token tiles, twice the CTAs for a launch
+    // that is all latency (32x4096x512: 3.65 -> 3.51 us, 32x2880x512: 3.60 -> 3.53 us; 64 tokens
+    // at K = 2048 measured slower split)
+    if (M > 16 && M <= 32 && cdiv(K, kAtomK) <= 2) p.m_tile = 16;
     if (mtile_req > 0) p.m_tile = std::min(static_cast<int>(cdiv(M, 16) * 16), mtile_req);
     p.nmc = (p.m_tile + 127) / 128;
     p.m_tiles = static_cast<int>(cdiv(M, p.m_tile));
