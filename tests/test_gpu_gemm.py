@@ -72,6 +72,27 @@ def test_gemm_workloads_sampled_vs_oracle(w):
     check_tolerance(c[im, inn], ref, w.name)
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 7168), (8, 2112, 32768), (1, 128, 65536), (520, 7168, 1032)])
+def test_gemm_large_shapes_sampled_vs_oracle(M, N, K):
+    # sizes past the benchmark's: 256-token tiles over many token tiles, long K slices that refill
+    # every pipeline stage several times, one weight tile with the widest automatic split, a K
+    # cut inside a block at 520 tokens; automatic plans, sampled outputs against the oracle
+    a = workloads.random_bf16(M, K, seed=M + 3 * K)
+    b = workloads.random_bf16(N, K, seed=N + 5 * K, scale=0.5)
+    c, bq, bs = run_gemm(a, b)
+    rq, rs = oracle.quantize(workloads.bf16_bits(b))
+    assert_bytes_equal(bs, rs, "B scales")
+    assert_bytes_equal(bq, rq, "B e2m1")
+    aq, as_ = oracle.quantize(workloads.bf16_bits(a))
+    rng = np.random.default_rng(M + N + K)
+    rows = np.unique(np.concatenate([rng.choice(M, min(M, 96), replace=False), [0, M - 1]]))
+    cols = np.unique(np.concatenate([rng.choice(N, min(N, 96), replace=False), [0, N - 1]]))
+    im = np.repeat(rows, cols.size)
+    inn = np.tile(cols, rows.size)
+    ref = oracle.gemm_entries(aq, as_, bq, bs, im, inn)
+    check_tolerance(c[im, inn], ref, f"{M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("w", workloads.EXTRA_WORKLOADS, ids=lambda w: w.name)
 def test_gemm_leaderboard_shapes_full_oracle(w):
     a, b = workloads.make_inputs(w, seed=2)
