@@ -181,9 +181,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
     // Fused quantization puts A's load and quantization on the GEMM's critical path (behind the
-    // dependency wait), while the two-kernel path overlaps them with the weight prologue; the
-    // fused path only wins for the smallest token counts (measured on M = 8 and 16).
-    p.path = path_req ? path_req : (M <= 16 ? 1 : 2);
+    // dependency wait), while the two-kernel path overlaps them with the weight prologue but adds
+    // a kernel and a dependency hop; the fused path wins for small token counts (below).
+    p.path = path_req ? path_req : (M <= 32 ? 1 : 2);
     if (p.path != 1 && p.path != 2) return MXFP4_ERR_ARG;
     int dev = 0;
     if (!cluster_caps && cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -203,12 +203,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
         *P = p;
         return MXFP4_OK;
     }
-    // Automatic path: the fused plan only while its in-kernel quantization is at most one 1x32
-    // block per thread (16x2112x7168, two per thread: fused 5.40 us, two-kernel 5.09 us).
+    // Automatic path for up to 32 tokens: the fused plan in 16-token tiles, while its in-kernel
+    // quantization is at most one 1x32 block per thread and its CTAs fit in one wave. Measured:
+    // 16x2112x7168 (two blocks per thread) fused 5.40 us, two-kernel 5.09 us; 32x4096x512 fused in
+    // 16-token tiles 3.25 us, two-kernel 3.57 us; 32x2880x512 3.18 vs 3.46 us.
     if (path_req == 0 && p.path == 1) {
         GemmPlan f;
-        if (make_plan(M, N, K, 1, 0, mtile_req, sm_count, &f, cluster_caps) == MXFP4_OK &&
-            static_cast<int64_t>(p.raw_rows) * 8 * f.atoms_max <= kGemmThreads) {
+        if (make_plan(M, N, K, 1, 0, mtile_req ? mtile_req : 16, sm_count, &f, cluster_caps) == MXFP4_OK &&
+            static_cast<int64_t>(f.raw_rows) * 8 * f.atoms_max <= kGemmThreads && f.ctas <= sm_count) {
             *P = f;
             return MXFP4_OK;
         }

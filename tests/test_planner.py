@@ -25,12 +25,13 @@ def plan(mx, M, N, K, **kw):
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
     (16, 3072, 1536, 1, 3, 16),      # fused A quantization, 72 CTAs
     (8, 2112, 7168, 1, 6, 16),       # fused, 6-slice clusters, 102 CTAs
-    (32, 4096, 512, 2, 1, 16),       # standalone quantize + GEMM, two 16-token tiles (short K)
+    (32, 4096, 512, 1, 1, 16),       # fused in two 16-token tiles, one block per thread, 64 CTAs
     (64, 7168, 2048, 2, 1, 64),      # longer K keeps one token tile
     (256, 4096, 7168, 2, 2, 128),    # 128-token tiles, 2 slices (bulk split-K)
     (16, 2112, 7168, 2, 5, 16),      # fused would be two blocks per thread: two-kernel, 5 slices
     (4, 2880, 512, 1, 1, 16),        # fused, one 1x32 block per thread or less
-    (32, 2880, 512, 2, 1, 16),
+    (32, 2880, 512, 1, 1, 16),
+    (24, 2112, 7168, 2, 5, 32),      # fused would be two blocks per thread: two-kernel
 ])
 def test_workload_plans(mx, M, N, K, path, splits, m_tile):
     p = plan(mx, M, N, K)
