@@ -52,42 +52,46 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+def configure(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded oracle library (this one, or a test's variant)."""
+    L.oracle_round_amax_bits.restype = ctypes.c_uint32
+    L.oracle_round_amax_bits.argtypes = [ctypes.c_float]
+    L.oracle_scale_exponent.restype = ctypes.c_int
+    L.oracle_scale_exponent.argtypes = [ctypes.c_uint32]
+    L.oracle_e2m1_encode.restype = ctypes.c_uint8
+    L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    L.oracle_e2m1_encode_nearest.restype = ctypes.c_uint8
+    L.oracle_e2m1_encode_nearest.argtypes = [ctypes.c_float]
+    L.oracle_e2m1_decode.restype = ctypes.c_double
+    L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+    L.oracle_quantize.restype = None
+    L.oracle_quantize.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+    L.oracle_dequantize.restype = None
+    L.oracle_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
+    L.oracle_gemm_f64.restype = None
+    L.oracle_gemm_f64.argtypes = [_f64p, _f64p, _i64, _i64, _i64, _f64p]
+    L.oracle_gemm_entries.restype = None
+    L.oracle_gemm_entries.argtypes = [_u8p, _u8p, _u8p, _u8p, _i64, _i64p, _i64p, _i64, _f64p]
+    L.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+    L.oracle_f64_to_bf16_array.restype = None
+    L.oracle_f64_to_bf16_array.argtypes = [_f64p, _i64, _u16p]
+    L.oracle_encode_selfcheck.restype = ctypes.c_int64
+    L.oracle_encode_selfcheck.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                          ctypes.POINTER(ctypes.c_uint32)]
+    L.oracle_num_threads.restype = ctypes.c_int
+    L.oracle_num_threads.argtypes = []
+    L.oracle_set_num_threads.restype = None
+    L.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _LIB
     with _LOCK:
         if _LIB is None:
             build()
-            L = ctypes.CDLL(_SO)
-            L.oracle_round_amax_bits.restype = ctypes.c_uint32
-            L.oracle_round_amax_bits.argtypes = [ctypes.c_float]
-            L.oracle_scale_exponent.restype = ctypes.c_int
-            L.oracle_scale_exponent.argtypes = [ctypes.c_uint32]
-            L.oracle_e2m1_encode.restype = ctypes.c_uint8
-            L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
-            L.oracle_e2m1_encode_nearest.restype = ctypes.c_uint8
-            L.oracle_e2m1_encode_nearest.argtypes = [ctypes.c_float]
-            L.oracle_e2m1_decode.restype = ctypes.c_double
-            L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
-            L.oracle_quantize.restype = None
-            L.oracle_quantize.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
-            L.oracle_dequantize.restype = None
-            L.oracle_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
-            L.oracle_gemm_f64.restype = None
-            L.oracle_gemm_f64.argtypes = [_f64p, _f64p, _i64, _i64, _i64, _f64p]
-            L.oracle_gemm_entries.restype = None
-            L.oracle_gemm_entries.argtypes = [_u8p, _u8p, _u8p, _u8p, _i64, _i64p, _i64p, _i64, _f64p]
-            L.oracle_f64_to_bf16.restype = ctypes.c_uint16
-            L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
-            L.oracle_f64_to_bf16_array.restype = None
-            L.oracle_f64_to_bf16_array.argtypes = [_f64p, _i64, _u16p]
-            L.oracle_encode_selfcheck.restype = ctypes.c_int64
-            L.oracle_encode_selfcheck.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
-                                                  ctypes.POINTER(ctypes.c_uint32)]
-            L.oracle_num_threads.restype = ctypes.c_int
-            L.oracle_num_threads.argtypes = []
-            L.oracle_set_num_threads.restype = None
-            L.oracle_set_num_threads.argtypes = [ctypes.c_int]
-            _LIB = L
+            _LIB = configure(ctypes.CDLL(_SO))
     return _LIB
 
 
