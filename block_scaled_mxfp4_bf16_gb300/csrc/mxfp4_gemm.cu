@@ -153,8 +153,12 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
     if (lane == 0) mbar_arrive(q.a_full);   // one arrival per warp
 }
 
+// kTwoKernel: an instantiation that only runs the two-kernel path (no quantizer code in it);
+// the other takes the path from its arguments.
+template <bool kTwoKernel>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mxfp4_gemm_kernel(const GemmArgs p) {
+    const bool fused = kTwoKernel ? false : p.fused != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* sB = smem;                           // stages x kWBlock
@@ -241,7 +245,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
 
     const uint8_t* bsrc = p.bblk + (static_cast<size_t>(nt) * p.k_atoms + a0) * kWBlock;
     const uint8_t* asrc = p.ablk + (static_cast<size_t>(mt) * p.k_atoms + a0) * a_block;
-    const uint32_t tx_bytes = kWBlock + (p.fused ? 0u : a_block);
+    const uint32_t tx_bytes = kWBlock + (fused ? 0u : a_block);
     const int npro = na < stages ? na : stages;
     // ------------------------------------------------------------------------ set-up
     if (warp == 0) {
@@ -250,7 +254,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             // depend on the previous grid). In the fused path only two: the A slice is the first
             // thing the CTA needs once the wait returns, and copies leave in issue order.
             const uint64_t pol_b = policy_evict_first();
-            const int nfirst = p.fused ? min(npro, 2) : npro;
+            const int nfirst = fused ? min(npro, 2) : npro;
             for (int j = 0; j < nfirst; ++j) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
                 bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol_b);
@@ -258,7 +262,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             MXFP4_PHASE(1);
             pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
             MXFP4_PHASE(2);
-            if (p.fused) {
+            if (fused) {
                 // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip
                 const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
                 const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
@@ -289,7 +293,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         named_barrier_arrive(1, 32 + kEpiThreads);
     } else if (warp == 2) {
         named_barrier(3, 64);
-    } else if (p.fused) {
+    } else if (fused) {
         // Warm L2 with the CTA's A rows while the previous grid finishes (plain prefetches from
         // the idle epilogue warps: they do not queue in front of the bulk copies).
         const int lines = (kslice * 2 + 127) / 128;
@@ -316,7 +320,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     }
     __syncwarp();
     // Fused path: every warp quantizes (one call site, so the quantizer is inlined once).
-    if (p.fused) quantize_slice(qs, threadIdx.x, p, flags);
+    if (fused) quantize_slice(qs, threadIdx.x, p, flags);
 
     if (warp == 0) {
         // -------------------------------------------------------------------- producer
@@ -329,14 +333,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 if (!mbar_wait(&empty[s], ((j / stages) - 1) & 1, lim)) { fail(p, flags); break; }
                 mbar_arrive_expect_tx(&full[s], tx_bytes);
                 bulk_load(sB + s * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[s], pol_b);
-                if (!p.fused)
+                if (!fused)
                     bulk_load(sA + s * a_block, asrc + static_cast<size_t>(j) * a_block, a_block, &full[s], pol_a);
                 issued = j + 1;
             }
             // never leave copies in flight into shared memory that is about to be reused or freed
             for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
                 mbar_wait(&full[j % stages], (j / stages) & 1, lim);
-            if (p.fused) mbar_wait(a_raw, 0, lim);
+            if (fused) mbar_wait(a_raw, 0, lim);
         }
         __syncwarp();
         if (cluster_posts) cluster_wait();
@@ -364,7 +368,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             const uint32_t b_step = kWBlock >> 4, a_step = a_block >> 4, chunk_step = kSfChunk >> 4;
             const bool two_chunks = p.nmc == 2;
             bool mok = true;
-            if (p.fused) mok = mbar_wait(a_full, 0, lim);
+            if (fused) mok = mbar_wait(a_full, 0, lim);
             if (issuer == 0) MXFP4_PHASE(3);
             tc_fence_after_sync();
             int s = issuer;
@@ -376,7 +380,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 if (j == 0) MXFP4_PHASE(4);
                 if (j == na - 1) MXFP4_PHASE(5);
                 tc_fence_after_sync();
-                const uint32_t slot = static_cast<uint32_t>(p.fused ? j : s);
+                const uint32_t slot = static_cast<uint32_t>(fused ? j : s);
                 const uint64_t bd = b_desc0 + static_cast<uint32_t>(s) * b_step;
                 const uint64_t ad = a_desc0 + slot * a_step;
                 const uint64_t sfbd = sfb_desc0 + static_cast<uint32_t>(s) * b_step;
@@ -718,11 +722,12 @@ static cudaError_t set_kernel_attributes() {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(mxfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemLimit));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mxfp4_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
+        for (auto* kernel : {mxfp4_gemm_kernel<false>, mxfp4_gemm_kernel<true>}) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
         attr_set[dev] = true;
     }
     return cudaSuccess;
@@ -741,12 +746,13 @@ int max_active_clusters(int cluster_size, size_t smem_bytes) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_kernel, &cfg) != cudaSuccess) {
+    int n = 0, m = 0;   // the same resources either way; the smaller count if they ever differ
+    if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_kernel<true>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&m, mxfp4_gemm_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
-    return n;
+    return n < m ? n : m;
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t s) {
@@ -766,7 +772,8 @@ cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = plan.splits > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel, args);
+    return args.fused ? cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<false>, args)
+                      : cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true>, args);
 }
 
 cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {
