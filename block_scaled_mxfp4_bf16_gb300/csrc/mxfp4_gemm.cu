@@ -93,8 +93,8 @@ struct QuantSlice {
 };
 
 // Every thread of the CTA takes part (the copy and MMA warps have nothing else to do until the
-// token blocks exist): one 1x32 block per item, items dealt round-robin over the CTA, two per
-// thread per pass so their arithmetic interleaves; K past the end becomes zero codes and scales.
+// token blocks exist): one 1x32 block per item, items dealt round-robin over the CTA, one per
+// thread per pass; K past the end becomes zero codes and scales.
 // (In a last block cut by K the epilogue warps have zeroed the staged bytes past K.)
 // Rows past M are left as they are: a token row only feeds its own accumulator column, and
 // columns past M are never stored.
@@ -109,43 +109,33 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
     if (!got) fail(p, abort_flag);
     const int total = got ? q.m_valid * q.nblk : 0;
     constexpr int nq = kGemmThreads;
-    for (int first = qt; first < total; first += 2 * nq) {
-        uint32_t w[2][16], out[2][4], sbyte[2];
-        int rr[2], kk[2];
+    // one item per thread per pass: the automatic plan keeps the fused path at one 1x32 block
+    // per thread, and a single item keeps the code the CTA fetches small
+    for (int idx = qt; idx < total; idx += nq) {
+        uint32_t w[16], out[4];
+        // rows run fastest: eight consecutive items read eight rows (distinct banks) and
+        // write eight rows of one chunk column (distinct swizzled chunks)
+        const int kq = one_row ? idx : static_cast<int>(__umulhi(static_cast<uint32_t>(idx), magic));
+        const int rr = idx - kq * q.m_valid;
+        uint32_t sbyte = 0u;
+        out[0] = out[1] = out[2] = out[3] = 0u;
+        if (kq < q.kblk) {
+            const uint4* src = reinterpret_cast<const uint4*>(q.raw + rr * q.raw_row + kq * 64);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            // rows run fastest: eight consecutive items read eight rows (distinct banks) and
-            // write eight rows of one chunk column (distinct swizzled chunks)
-            const int idx = first + u * nq;
-            const int kq = one_row ? idx : static_cast<int>(__umulhi(static_cast<uint32_t>(idx), magic));
-            kk[u] = idx < total ? kq : q.kblk;        // kblk: nothing to read
-            rr[u] = idx < total ? idx - kk[u] * q.m_valid : 0;
-            if (kk[u] < q.kblk) {
-                const uint4* src = reinterpret_cast<const uint4*>(q.raw + rr[u] * q.raw_row + kk[u] * 64);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 v = src[i];
-                    w[u][4 * i + 0] = v.x;
-                    w[u][4 * i + 1] = v.y;
-                    w[u][4 * i + 2] = v.z;
-                    w[u][4 * i + 3] = v.w;
-                }
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = src[i];
+                w[4 * i + 0] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
             }
+            sbyte = quantize_block32(w, out);
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            out[u][0] = out[u][1] = out[u][2] = out[u][3] = 0u;
-            sbyte[u] = kk[u] < q.kblk ? quantize_block32(w[u], out[u]) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (first + u * nq >= total) continue;
-            const uint32_t c = static_cast<uint32_t>(kk[u] & 7);
-            uint8_t* blk = q.blocks + (kk[u] >> 3) * q.a_block;
-            *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(rr[u]), c)) =
-                make_uint4(out[u][0], out[u][1], out[u][2], out[u][3]);
-            blk[q.a_rows + block_sf_offset(static_cast<uint32_t>(rr[u]), c)] = static_cast<uint8_t>(sbyte[u]);
-        }
+        const uint32_t c = static_cast<uint32_t>(kq & 7);
+        uint8_t* blk = q.blocks + (kq >> 3) * q.a_block;
+        *reinterpret_cast<uint4*>(blk + swz_chunk_offset(static_cast<uint32_t>(rr), c)) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+        blk[q.a_rows + block_sf_offset(static_cast<uint32_t>(rr), c)] = static_cast<uint8_t>(sbyte);
     }
     if (qt == 96) MXFP4_PHASE(13);
     fence_proxy_async_smem();   // the MMAs read the token blocks through the async proxy
