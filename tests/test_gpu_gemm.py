@@ -152,6 +152,36 @@ def test_gemm_empty_and_errors():
         mx.mxfp4_gemm(a, packed, 64 + 128)        # N past the packed tiles
 
 
+def test_gemm_host_empty_and_errors():
+    # the host-buffer call checks everything before it copies anything: empty shapes are no-ops,
+    # bad strides, misaligned device buffers and missing host buffers are refused, and none of
+    # them touches the host or device buffers
+    mx = _mx()
+    L = mx.load_library()
+    st = torch.cuda.current_stream().cuda_stream
+    M, N, K = 4, 128, 64
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=1).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a_host = workloads.random_bf16(M, K, seed=2).pin_memory()
+    c_host = torch.full((M, N), 5.0, dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.full((M, K), 7.0, dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+
+    def call(a=a_host.data_ptr(), m=M, k=K, lda=K, n=N, c=c_host.data_ptr(), ldc=N, ad=a_dev.data_ptr(),
+             cd=c_dev.data_ptr()):
+        return L.mxfp4_gemm_host(a, m, k, lda, packed.data_ptr(), n, c, ldc, ad, cd, None, 0, st)
+
+    assert call(m=0) == 0 and call(n=0) == 0          # no-ops
+    assert call(lda=K - 8) == 2                         # host row stride shorter than K
+    assert call(ldc=N - 1) == 2                         # host C stride shorter than N
+    assert call(k=K + 4) == 2                           # K not a multiple of 8
+    assert call(ad=a_dev.data_ptr() + 2) == 3           # misaligned device A
+    assert call(a=None) == 1 and call(c=None) == 1      # missing host buffers
+    torch.cuda.synchronize()
+    assert torch.all(c_host == 5.0) and torch.all(a_dev == 7.0) and torch.all(c_dev == 9.0)
+    assert mx.mxfp4_device_status() == 0
+
+
 def test_timeout_is_reported_not_hung():
     mx = _mx()
     assert mx.mxfp4_device_status() == 0
