@@ -343,7 +343,7 @@ const char* mxfp4_status_string(int status) {
 
 int mxfp4_last_cuda_error(void) { return t_last_cuda_error; }
 
-int mxfp4_version(void) { return 200; }
+int mxfp4_version(void) { return 201; }
 
 int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, void* scales, void* stream) {
     if (rows < 0 || K < 0) return MXFP4_ERR_ARG;

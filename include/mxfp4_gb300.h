@@ -60,7 +60,7 @@ const char *mxfp4_status_string(int status);
  * on this host thread, 0 if none. */
 int mxfp4_last_cuda_error(void);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64). */
 int mxfp4_version(void);
 
 /*
