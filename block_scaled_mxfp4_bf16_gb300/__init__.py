@@ -204,14 +204,20 @@ def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
            "mxfp4_workspace_init")
 
 
-def _workspace(device: torch.device, nbytes: int, stream) -> torch.Tensor | None:
-    """A zero-initialised workspace of at least nbytes per device, grown on demand."""
+def _workspace(device: torch.device, nbytes: int, stream, st: int) -> torch.Tensor | None:
+    """A zero-initialised workspace of at least nbytes per (device, stream), grown on demand.
+    One per stream: calls sharing a workspace must be ordered, and calls on different streams
+    need not be. A workspace used on a stream other than the current one is recorded on it, so
+    that growing it never hands its memory to other work while that stream may still use it."""
     if nbytes == 0:
         return None
-    key = device.index if device.index is not None else torch.cuda.current_device()
+    dev_index = device.index if device.index is not None else torch.cuda.current_device()
+    key = (dev_index, st)
     ws = _WS.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        if st != torch.cuda.current_stream(dev_index).cuda_stream:
+            ws.record_stream(torch.cuda.ExternalStream(st, device=device))
         mxfp4_workspace_init(ws, stream)
         _WS[key] = ws
     return ws
@@ -236,7 +242,7 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     if workspace is None:
         dev = a.device
         need = _ws_need(dev, M, N, K, path, splits, m_tile)
-        workspace = _workspace(dev, need, stream) if need else None
+        workspace = _workspace(dev, need, stream, st) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = _opts(path, splits, m_tile) if (path or splits or m_tile) else None   # NULL: automatic plan
@@ -272,7 +278,7 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
     if workspace is None:
         dev = a_dev.device
         need = _ws_need(dev, M, N, K)
-        workspace = _workspace(dev, need, stream) if need else None
+        workspace = _workspace(dev, need, stream, st) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(L.mxfp4_gemm_host(a_host.data_ptr(), M, K, a_stride[0], packed_b.data_ptr(), N, c_host.data_ptr(),

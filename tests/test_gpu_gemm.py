@@ -152,6 +152,31 @@ def test_gemm_empty_and_errors():
         mx.mxfp4_gemm(a, packed, 64 + 128)        # N past the packed tiles
 
 
+def test_concurrent_streams_use_their_own_default_workspace():
+    # two-kernel GEMMs (the workspace holds the quantized A between the two kernels) on two streams
+    # at once through the binding's default workspaces: each stream must get its own, or the
+    # calls would overwrite each other's token blocks
+    mx = _mx()
+    M, N, K = 64, 512, 2048
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=31).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a = [workloads.random_bf16(M, K, seed=32 + i).cuda() for i in range(2)]
+    want = [mx.mxfp4_gemm(x, packed, N).clone() for x in a]
+    assert mx.mxfp4_gemm_plan(M, N, K)["path"] == 2
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for rep in range(20):
+        for i, s in enumerate(streams):
+            with torch.cuda.stream(s):
+                outs[i].append(mx.mxfp4_gemm(a[i], packed, N, stream=s))
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0
+    for i in range(2):
+        for c in outs[i]:
+            assert torch.equal(c.view(torch.int16), want[i].view(torch.int16))
+
+
 def test_gemm_host_empty_and_errors():
     # the host-buffer call checks everything before it copies anything: empty shapes are no-ops,
     # bad strides, misaligned device buffers and missing host buffers are refused, and none of
