@@ -86,6 +86,25 @@ def test_cluster_residency_limits_the_split(mx):
     assert mx.mxfp4_gemm_plan_model(1, 128, 65536, SM_COUNT, None)["splits"] <= 8
 
 
+def test_automatic_fused_plans_keep_one_block_per_thread_and_one_wave(mx):
+    # the automatic plan is fused only for M <= 32 in 16-token tiles, and only while the in-kernel
+    # quantization is at most one 1x32 block per thread (352 threads) and the CTAs fit one wave
+    fused = two_kernel = 0
+    for M in (1, 4, 8, 13, 16, 17, 24, 32, 33, 64):
+        for N in (128, 2112, 2880, 4096, 7168):
+            for K in (64, 512, 1536, 2048, 7168, 16384):
+                p = plan(mx, M, N, K)
+                if p["path"] == 1:
+                    fused += 1
+                    assert M <= 32 and p["m_tile"] == 16, (M, N, K, p)
+                    atoms_max = -(-(-(-K // 256)) // p["splits"])
+                    assert min(M, 16) * 8 * atoms_max <= 352, (M, N, K, p)
+                    assert p["ctas"] <= SM_COUNT, (M, N, K, p)
+                else:
+                    two_kernel += 1
+    assert fused and two_kernel
+
+
 def test_errors(mx):
     import block_scaled_mxfp4_bf16_gb300 as m
     with pytest.raises(m.Mxfp4Error):
