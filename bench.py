@@ -34,7 +34,7 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM launch from one ncu
 # capture (profiles/), valid only for the device code and the launch plan it was taken with (both
 # checked at run time; reported as null otherwise).
-MEASURED_TRAFFIC = {"M8_N2112_K7168": (8470272, "2a5a9267ba0daef0",
+MEASURED_TRAFFIC = {"M8_N2112_K7168": (8470784, "4597bb277acadcb2",
                                       "path=1,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=2,recv_dedicated=1")}
 HEADLINE = "M8_N2112_K7168"
 FALLBACK_HBM_GBS = 6800.0
