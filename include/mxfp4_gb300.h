@@ -110,8 +110,9 @@ int mxfp4_prepack_b(const void *bq, const void *bs, int64_t N, int64_t K,
 /*
  * mxfp4_gemm_workspace_size -- bytes of device workspace mxfp4_gemm needs for this shape
  * on the CURRENT device (the plan depends on its SM count). The workspace holds the
- * quantized A (as token blocks) of the two-kernel path used for M > 32; the fused path
- * needs none and returns 0. Split-K partial sums never leave the chip.
+ * quantized A (as token blocks) of the two-kernel path; plans that quantize A inside the
+ * GEMM (the automatic plan for small M, see mxfp4_gemm_plan_info) need none and return 0.
+ * Split-K partial sums never leave the chip.
  */
 size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -135,8 +136,9 @@ int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  * Ordering: the call waits for the work before it on `stream` before it reads A or writes C.
  * The weights in packed_b are requested before that wait (they are meant to be constant), so
  * packed_b must not be written by a kernel that is still running when the call is enqueued and
- * that lets dependent launches start early (programmatic dependent launch); ordinary kernels,
- * copies and this library's own calls never do.
+ * that lets dependent launches start early (programmatic dependent launch). Ordinary kernels and
+ * copies never let them; this library's kernels do, but none of them writes packed_b that way
+ * (mxfp4_prepack_b's kernel does not let dependents start early).
  * A is quantized exactly like mxfp4_quantize (bit-identical codes and scales). With split-K
  * the K slices of an output tile run as one thread-block cluster and their fp32 partial
  * sums are added in slice order through distributed shared memory, so results are
