@@ -251,9 +251,10 @@ int mxfp4_selftest_timeout(int limit_us, void *stream);
  * inference engine whose host owns the whole device-memory plan and forbids allocation once
  * it runs, or a latency-critical serving loop that must never call cudaMalloc/cudaFree
  * because those can synchronize the whole device. This entry point needs no workspace
- * argument: its scratch (the quantized A that the two-kernel path, M > 32, hands from its
- * quantize kernel to the GEMM kernel) lives in one statically sized array inside the
- * library, which every GPU that loads the library keeps for the life of the process.
+ * argument: its scratch (the quantized A that the two-kernel path -- M > 32, or a small M
+ * that the planner does not fuse -- hands from its quantize kernel to the GEMM kernel) lives
+ * in one statically sized array inside the library, which every GPU that loads the library
+ * keeps for the life of the process.
  *
  *   Arguments and results are those of mxfp4_gemm without `workspace` / `ws_bytes`; it runs
  *   the same plan, so the output is the same.
