@@ -16,10 +16,11 @@ Sources (the "amd-mxfp4-mm" leaderboard submissions):
 
 Pins (tests/test_oracle_pins.py): the e2m1 grid, an exhaustive fp32 cross-check against an
 independent nearest-value encoder, hand-worked blocks (tests/golden/hand_blocks.json) and rows
-whose K cuts the last block (tests/golden/tail_blocks.json), the scale formula as the method
-states it, evaluated literally for every bf16 amax, an error-bound invariant, exact closed-form
-GEMMs and brute-force tiny GEMMs. tests/test_oracle_mutants.py plants fourteen plausible mistakes
-in copies of mxfp4_oracle.c and checks that each fails a pin. No oracle function is "parity
+whose K cuts the last block (tests/golden/tail_blocks.json), the block maximum at every
+position of a block, the scale formula as the method states it, evaluated literally for every
+bf16 amax, an error-bound invariant, exact closed-form GEMMs and brute-force tiny GEMMs.
+tests/test_oracle_mutants.py plants fifteen plausible mistakes in copies of mxfp4_oracle.c and
+checks that each fails a pin. No oracle function is "parity
 unpinned".
 """
 from __future__ import annotations

@@ -19,6 +19,8 @@ MUTANTS = [
     ("overflow clamp", "if (amax_r_bits >= 0x7F800000u) return 127;", "if (amax_r_bits >= 0x7F800000u) return 126;"),
     ("scale applied inverted", "mul = ldexpf(1.0f, -s);", "mul = ldexpf(1.0f, s);"),
     ("amax without |x|", "amax = fmaxf(amax, fabsf(xs[i]));", "amax = fmaxf(amax, xs[i]);"),
+    ("amax misses the last element", "amax = fmaxf(amax, fabsf(xs[i]));",
+     "if (i < 31) amax = fmaxf(amax, fabsf(xs[i]));"),
     ("saturation threshold", "if (a >= 6.0f) {", "if (a >= 5.0f) {"),
     ("sub-one rounding step", "float t = a + 4194304.0f;", "float t = a + 8388608.0f;"),
     ("ties-to-even bit dropped", "uint32_t rounded = rebased + 0x1FFFFFu + keep;", "uint32_t rounded = rebased + 0x1FFFFFu;"),
@@ -41,6 +43,7 @@ def _pins():
         ("grid round trip", pins.test_encode_grid_points_round_trip),
         ("scale formula, every bf16 amax", pins.test_scale_formula_literal_log2_for_every_bf16_amax),
         ("unique octave", pins.test_scale_is_the_unique_octave_placing_amax_in_3p5_to_7),
+        ("block maximum at every position", pins.test_block_maximum_at_every_position),
         ("single product", pins.test_gemm_single_product_lands_in_place),
         ("brute-force GEMM", pins.test_gemm_brute_force_tiny_random),
         ("bf16 rounding", pins.test_bf16_rounding_matches_exact_rational_rounding),

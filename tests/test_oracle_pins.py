@@ -119,6 +119,26 @@ def test_hand_worked_tail_rows(row):
     assert bytes(q[0]).hex() == row["packed_hex"]
 
 
+def test_block_maximum_at_every_position():
+    # Rows of one 1x32 block: 1.0 everywhere except 4.0 at position p (row 2p) or -4.0 at p
+    # (row 2p+1). Worked by hand: the block maximum |x| = 4.0 is a power of two, so the
+    # rounding keeps it; floor(log2 4) - 2 = 0 gives scale byte 127 and a multiplier of 1;
+    # 1.0 encodes as code 2, 4.0 as code 6 and -4.0 as 0xE. A maximum that one position of
+    # the block does not reach would leave 1.0 as the maximum (byte 125) at that position.
+    x = np.full((64, 32), bf16_of_float(1.0), np.uint16)
+    for p in range(32):
+        x[2 * p, p] = bf16_of_float(4.0)
+        x[2 * p + 1, p] = bf16_of_float(-4.0)
+    q, s = oracle.quantize(x)
+    assert (s[:, 0] == 127).all(), np.nonzero(s[:, 0] != 127)[0]
+    for r in range(64):
+        p, neg = divmod(r, 2)
+        want = [2] * 32
+        want[p] = 0xE if neg else 6
+        got = [(int(q[r, i // 2]) >> (4 * (i & 1))) & 15 for i in range(32)]
+        assert got == want, r
+
+
 def test_k_not_multiple_of_8_is_refused():
     with pytest.raises(ValueError):
         oracle.quantize(np.zeros((1, 36), np.uint16))
