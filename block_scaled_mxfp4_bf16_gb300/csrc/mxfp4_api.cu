@@ -510,14 +510,15 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
                                          static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
     // Page-locked host memory mapped into the device's address space takes C straight from the
-    // epilogue's stores (no separate device -> host copy); anything else goes through c_dev.
+    // epilogue's stores (no separate device -> host copy) when it is aligned for bf16 stores;
+    // anything else goes through c_dev.
     cudaPointerAttributes attr = {};
     void* c_mapped = nullptr;
     if (cudaPointerGetAttributes(&attr, c_host) == cudaSuccess && attr.type == cudaMemoryTypeHost)
         c_mapped = attr.devicePointer;
     else
         cudaGetLastError();   // clear the error an unregistered pointer leaves behind
-    if (c_mapped)
+    if (c_mapped && aligned(c_mapped, 2))
         return run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_mapped, ldc, static_cast<uint8_t*>(workspace), s);
     st = run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_dev, N, static_cast<uint8_t*>(workspace), s);
     if (st != MXFP4_OK) return st;

@@ -176,8 +176,8 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
  * mxfp4_gemm_host -- mxfp4_gemm for A and C in host memory: on `stream`, move A (rows of K
  * elements, row stride lda) into the caller's device buffer a_dev, run mxfp4_gemm, and deliver C
  * into c_host (row stride ldc): page-locked host memory mapped into the device's address space
- * (cudaHostAlloc / cudaHostRegister) receives C straight from the GEMM's stores; any other host
- * memory receives it by a copy from the caller's device buffer c_dev. Likewise A: from mapped
+ * (cudaHostAlloc / cudaHostRegister), 2-byte aligned, receives C straight from the GEMM's stores;
+ * any other host memory receives it by a copy from the caller's device buffer c_dev. Likewise A: from mapped
  * page-locked memory with 16-byte aligned rows (lda % 8 == 0) a small kernel reads it in place
  * and writes a_dev (it chains with the GEMMs by programmatic dependent launch, so back-to-back
  * calls overlap; it still reads A only after the work before it on `stream` has finished, so A
@@ -186,7 +186,8 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
  * c_host must stay valid until then (page-locked host memory lets the copies overlap other
  * work; pageable memory works but the copies then block the host).
  *   a_host : bf16 [M, K], row stride lda (lda >= K); a_dev: device bf16 [M, K] packed
- *            (row stride K), 16-byte aligned; c_dev: device bf16 [M, N] packed (row stride N);
+ *            (row stride K), 16-byte aligned; c_dev: device bf16 [M, N] packed (row stride N),
+ *            2-byte aligned, required (and checked) even where C goes straight to c_host;
  *   packed_b, workspace: as for mxfp4_gemm.
  * Errors: as mxfp4_gemm, checked before any copy; MXFP4_ERR_CUDA if a copy fails to enqueue.
  */
