@@ -360,14 +360,20 @@ int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, 
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
 }
 
+// The largest weight matrix the GEMM takes (its own check below); prepacking a larger one
+// would only build a buffer that no GEMM call accepts.
+static bool weight_dims_fit(int64_t N, int64_t K) {
+    return N <= (int64_t(1) << 31) - 1 && K <= (int64_t(1) << 30);
+}
+
 size_t mxfp4_prepack_b_size(int64_t N, int64_t K) {
-    if (N <= 0 || K <= 0 || K % 8 != 0) return 0;
+    if (N <= 0 || K <= 0 || K % 8 != 0 || !weight_dims_fit(N, K)) return 0;
     return packed_b_bytes(N, K);
 }
 
 int mxfp4_prepack_b(const void* bq, const void* bs, int64_t N, int64_t K, void* packed, void* stream) {
     if (N <= 0 || K <= 0) return MXFP4_ERR_ARG;
-    if (K % 8 != 0) return MXFP4_ERR_SHAPE;
+    if (K % 8 != 0 || !weight_dims_fit(N, K)) return MXFP4_ERR_SHAPE;
     if (!bq || !bs || !packed) return MXFP4_ERR_ARG;
     if (!aligned(bq, 16) || !aligned(packed, 1024)) return MXFP4_ERR_ALIGN;
     DeviceInfo di;

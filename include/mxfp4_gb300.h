@@ -29,6 +29,8 @@
  *     the mask offs_k < K with 0 as the fill value: they do not change the block's scale and
  *     are stored as zero codes. The natural packed layout keeps whole blocks: codes
  *     [rows, nblk*16] bytes, scales [rows, nblk] bytes.
+ *   - Size limits of the GEMM and the weight prepack: M and N below 2^31, K at most 2^30
+ *     (MXFP4_ERR_SHAPE beyond; mxfp4_prepack_b_size returns 0).
  *   - The library targets compute capability 10.3 (GB300) only; other devices give
  *     MXFP4_ERR_ARCH.
  */
@@ -86,7 +88,7 @@ int mxfp4_quantize(const void *x, int64_t rows, int64_t K, int64_t ld,
  * tile and 256-element K step, each holding that piece's e2m1 rows (16 KB, swizzled the
  * way the tensor cores read shared memory) and its e8m0 scales (1 KB, in the tensor-memory
  * scale-factor layout). Rows past N and K past the last multiple of 256 are zero padding.
- * 0 for invalid sizes.
+ * 0 for invalid sizes (including N >= 2^31 or K > 2^30).
  */
 size_t mxfp4_prepack_b_size(int64_t N, int64_t K);
 

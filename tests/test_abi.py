@@ -52,6 +52,11 @@ def test_prepack_size_is_pure_host_arithmetic(lib):
     assert lib.mxfp4_prepack_b_size(100, 8) == 1 * 1 * 17408
     assert lib.mxfp4_prepack_b_size(100, 100) == 0    # K must be a multiple of 8
     assert lib.mxfp4_prepack_b_size(0, 64) == 0
+    # the GEMM's size limits: N below 2^31, K at most 2^30
+    assert lib.mxfp4_prepack_b_size(128, 1 << 30) == (1 << 30) // 256 * 17408
+    assert lib.mxfp4_prepack_b_size(128, (1 << 30) + 8) == 0
+    assert lib.mxfp4_prepack_b_size((1 << 31) - 1, 256) == (1 << 24) * 17408
+    assert lib.mxfp4_prepack_b_size(1 << 31, 256) == 0
 
 
 def test_no_cpu_fallback_when_cuda_missing(lib):
