@@ -111,8 +111,22 @@ def _stream(stream) -> int:
 
 
 def _dev(t: torch.Tensor, name: str) -> None:
+    """The library plans and launches on the current CUDA device: `t` must live there."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.get_device() != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current CUDA device")
+
+
+def _on(t: torch.Tensor, device: torch.device, name: str) -> None:
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, with the other operands")
+
+
+def _out_bytes(t: torch.Tensor, shape: tuple, device: torch.device, name: str) -> None:
+    """A caller-supplied uint8 output: the kernels write it as one dense [rows, cols] block."""
+    if t.device != device or t.dtype != torch.uint8 or tuple(t.shape) != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous uint8 tensor of shape {list(shape)} on {device}")
 
 
 def _opts(path: int, splits: int, m_tile: int = 0):
@@ -135,8 +149,12 @@ def mxfp4_quantize(x: torch.Tensor, q: torch.Tensor | None = None, scales: torch
     nblk = (K + 31) // 32
     if q is None:
         q = torch.empty(rows, nblk * 16, dtype=torch.uint8, device=x.device)
+    else:
+        _out_bytes(q, (rows, nblk * 16), x.device, "q")
     if scales is None:
         scales = torch.empty(rows, nblk, dtype=torch.uint8, device=x.device)
+    else:
+        _out_bytes(scales, (rows, nblk), x.device, "scales")
     _check(L.mxfp4_quantize(x.data_ptr(), rows, K, x.stride(0), q.data_ptr(), scales.data_ptr(), _stream(stream)),
            "mxfp4_quantize")
     return q, scales
@@ -152,9 +170,12 @@ def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | N
     packed uint8 buffer for mxfp4_gemm with any K in (32*(nblk-1), 32*nblk]."""
     L = load_library()
     _dev(bq, "bq")
+    _on(bs, bq.device, "bs")
     N, K = bq.shape[0], bq.shape[1] * 2
     if bs.shape != (N, K // 32) or not bq.is_contiguous() or not bs.is_contiguous():
         raise ValueError("bq [N, nblk*16] and bs [N, nblk] must be contiguous and consistent")
+    if bq.element_size() != 1 or bs.element_size() != 1:
+        raise ValueError("bq and bs must be byte tensors")
     size = mxfp4_prepack_b_size(N, K)
     if size == 0:
         raise Mxfp4Error(2, "mxfp4_prepack_b_size")
@@ -162,6 +183,8 @@ def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | N
         packed = torch.empty(size + 1024, dtype=torch.uint8, device=bq.device)
         off = (-packed.data_ptr()) % 1024
         packed = packed[off:off + size]
+    elif packed.device != bq.device or packed.nbytes < size or not packed.is_contiguous():
+        raise ValueError(f"packed must be a contiguous buffer of at least {size} bytes on {bq.device}")
     _check(L.mxfp4_prepack_b(bq.data_ptr(), bs.data_ptr(), N, K, packed.data_ptr(), _stream(stream)),
            "mxfp4_prepack_b")
     return packed
@@ -188,15 +211,17 @@ def _ws_need(device: torch.device, M: int, N: int, K: int, path: int = 0, splits
 _PACKED_NEED: dict = {}
 
 
-def _check_packed(packed_b: torch.Tensor, N: int, K: int) -> None:
+def _check_packed(packed_b: torch.Tensor, N: int, K: int, device: torch.device | None) -> None:
     """The packed weights must cover mxfp4_prepack_b_size(N, K) bytes on the GEMM's device: the
-    kernel streams that many bytes, so a smaller buffer would be read past its end."""
+    kernel streams that many bytes, so a smaller buffer would be read past its end. `device`
+    None checks only that the buffer is on a CUDA device (the per-step host call)."""
     need = _PACKED_NEED.get((N, K))
     if need is None:
         need = mxfp4_prepack_b_size(N, K)
         _PACKED_NEED[(N, K)] = need
-    if packed_b.nbytes < need or not packed_b.is_cuda:
-        raise ValueError(f"packed_b must be a CUDA buffer of at least mxfp4_prepack_b_size({N}, {K}) = {need} bytes")
+    if need == 0 or packed_b.nbytes < need or not packed_b.is_cuda or (device is not None and packed_b.device != device):
+        raise ValueError(f"packed_b must be a CUDA buffer of at least mxfp4_prepack_b_size({N}, {K}) = {need} bytes"
+                         " on the device of the other operands")
 
 
 def mxfp4_workspace_init(ws: torch.Tensor, stream=None) -> None:
@@ -233,13 +258,18 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
         raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
     M, K = a.shape
     if M and N:
-        _check_packed(packed_b, N, K)
+        _check_packed(packed_b, N, K, a.device)
     if c is None:
         c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _on(c, a.device, "c")
     if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
     st = _stream(stream)
-    if workspace is None:
+    if workspace is not None:
+        _on(workspace, a.device, "workspace")
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
+    else:
         dev = a.device
         need = _ws_need(dev, M, N, K, path, splits, m_tile)
         workspace = _workspace(dev, need, stream, st) if need else None
@@ -271,11 +301,14 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
     if tuple(c_shape) != (M, N):
         raise ValueError("c_host must be [M, N]")
     if M and N:
-        _check_packed(packed_b, N, K)
+        _check_packed(packed_b, N, K, None)
     if a_dev.shape != (M, K) or a_dev.stride() != (K, 1) or c_dev.shape != (M, N) or c_dev.stride() != (N, 1):
         raise ValueError("a_dev must be a packed [M, K] and c_dev a packed [M, N] tensor")
     st = _stream(stream)
-    if workspace is None:
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+    else:
         dev = a_dev.device
         need = _ws_need(dev, M, N, K)
         workspace = _workspace(dev, need, stream, st) if need else None
@@ -297,9 +330,10 @@ def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch
         raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
     M, K = a.shape
     if M and N:
-        _check_packed(packed_b, N, K)
+        _check_packed(packed_b, N, K, a.device)
     if c is None:
         c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _on(c, a.device, "c")
     if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
     _check(L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),

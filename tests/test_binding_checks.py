@@ -1,0 +1,178 @@
+"""The Python binding's argument checks, run on the CPU: every buffer it hands to the library
+must be on the operands' device and large enough, because the kernels would otherwise read or
+write past a buffer (or through a host pointer). Tensors here are CPU tensors that report
+is_cuda; the library's size queries are the real ones (host arithmetic), its compute entry
+points are recorded instead of called."""
+import pytest
+import torch
+
+import block_scaled_mxfp4_bf16_gb300 as mx
+
+
+class _OnDevice(torch.Tensor):
+    """A CPU tensor that reports is_cuda, standing for a tensor on the current CUDA device."""
+
+    @property
+    def is_cuda(self):
+        return True
+
+
+def dev(t: torch.Tensor) -> torch.Tensor:
+    return torch.Tensor._make_subclass(_OnDevice, t)
+
+
+class _Lib:
+    """The real library for size queries; compute calls are recorded and succeed."""
+
+    COMPUTE = ("mxfp4_quantize", "mxfp4_prepack_b", "mxfp4_gemm_ex", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
+               "mxfp4_workspace_init")
+
+    def __init__(self, real):
+        self.real = real
+        self.calls = []
+
+    def __getattr__(self, name):
+        if name in self.COMPUTE:
+            return lambda *args: self.calls.append((name, args)) or 0
+        if name == "mxfp4_gemm_workspace_size_ex":
+            return lambda *args: 0       # plans that need no workspace
+        return getattr(self.real, name)
+
+
+@pytest.fixture
+def lib(monkeypatch):
+    fake = _Lib(mx.load_library())
+    monkeypatch.setattr(mx, "load_library", lambda: fake)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: -1)   # a CPU tensor's get_device()
+    mx._WS_NEED.clear()
+    mx._PACKED_NEED.clear()
+    yield fake
+    mx._WS_NEED.clear()
+    mx._PACKED_NEED.clear()
+
+
+def _meta(*shape, dtype=torch.uint8):
+    return torch.empty(*shape, dtype=dtype, device="meta")   # another device
+
+
+def _gemm_operands(M=8, N=256, K=512):
+    a = dev(torch.zeros(M, K, dtype=torch.bfloat16))
+    packed = dev(torch.zeros(mx.mxfp4_prepack_b_size(N, K), dtype=torch.uint8))
+    return a, packed, N
+
+
+def test_gemm_passes_pointers_sizes_and_strides(lib):
+    a, packed, N = _gemm_operands()
+    c = dev(torch.zeros(8, N + 8, dtype=torch.bfloat16))[:, :N]
+    mx.mxfp4_gemm(a, packed, N, c=c, stream=0)
+    (name, args), = lib.calls
+    assert name == "mxfp4_gemm_ex"
+    assert args[:8] == (a.data_ptr(), 8, 512, 512, packed.data_ptr(), N, c.data_ptr(), N + 8)
+    assert args[8] is None and args[9] == 0 and args[10] is None   # no workspace, automatic plan
+
+
+def test_gemm_refuses_buffers_before_any_call(lib):
+    a, packed, N = _gemm_operands()
+    with pytest.raises(ValueError):   # packed weights too small
+        mx.mxfp4_gemm(a, packed[:1024], N, stream=0)
+    with pytest.raises(ValueError):   # N past the packed tiles
+        mx.mxfp4_gemm(a, packed, N + 128, stream=0)
+    with pytest.raises(ValueError, match="device of the other operands"):   # on another CUDA device
+        mx.mxfp4_gemm(a, dev(_meta(packed.numel())), N, stream=0)
+    with pytest.raises(ValueError):   # packed weights not on a CUDA device at all
+        mx.mxfp4_gemm(a, torch.zeros(packed.numel(), dtype=torch.uint8), N, stream=0)
+    with pytest.raises(ValueError):   # C on another device (the kernel would store through it)
+        mx.mxfp4_gemm(a, packed, N, c=_meta(8, N, dtype=torch.bfloat16), stream=0)
+    with pytest.raises(ValueError):   # C of the wrong shape
+        mx.mxfp4_gemm(a, packed, N, c=dev(torch.zeros(8, N - 1, dtype=torch.bfloat16)), stream=0)
+    with pytest.raises(ValueError):   # workspace on another device
+        mx.mxfp4_gemm(a, packed, N, workspace=_meta(1 << 20), stream=0)
+    with pytest.raises(ValueError):   # workspace not contiguous
+        mx.mxfp4_gemm(a, packed, N, workspace=dev(torch.zeros(64, 64, dtype=torch.uint8))[:, :32], stream=0)
+    with pytest.raises(ValueError):   # K not a multiple of 8: no packed size exists
+        mx.mxfp4_gemm(dev(torch.zeros(8, 100, dtype=torch.bfloat16)), packed, N, stream=0)
+    with pytest.raises(ValueError):   # A on the host
+        mx.mxfp4_gemm(torch.zeros(8, 512, dtype=torch.bfloat16), packed, N, stream=0)
+    assert lib.calls == []
+
+
+def test_gemm_refuses_a_tensor_off_the_current_device(lib, monkeypatch):
+    a, packed, N = _gemm_operands()
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    with pytest.raises(ValueError):
+        mx.mxfp4_gemm(a, packed, N, stream=0)
+    assert lib.calls == []
+
+
+def test_noalloc_checks_like_gemm(lib):
+    a, packed, N = _gemm_operands()
+    mx.mxfp4_gemm_noalloc(a, packed, N, stream=0)
+    assert [n for n, _ in lib.calls] == ["mxfp4_gemm_noalloc"]
+    with pytest.raises(ValueError):
+        mx.mxfp4_gemm_noalloc(a, packed, N, c=_meta(8, N, dtype=torch.bfloat16), stream=0)
+    with pytest.raises(ValueError):
+        mx.mxfp4_gemm_noalloc(a, packed[:17408], N, stream=0)
+    assert len(lib.calls) == 1
+
+
+def test_host_call_checks(lib):
+    M, N, K = 4, 256, 512
+    _, packed, _ = _gemm_operands(M, N, K)
+    a_host = torch.zeros(M, K, dtype=torch.bfloat16)
+    c_host = torch.zeros(M, N, dtype=torch.bfloat16)
+    a_dev = dev(torch.zeros(M, K, dtype=torch.bfloat16))
+    c_dev = dev(torch.zeros(M, N, dtype=torch.bfloat16))
+    mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0)
+    (name, args), = lib.calls
+    assert name == "mxfp4_gemm_host"
+    assert args[:10] == (a_host.data_ptr(), M, K, K, packed.data_ptr(), N, c_host.data_ptr(), N,
+                         a_dev.data_ptr(), c_dev.data_ptr())
+    with pytest.raises(ValueError):   # device staging buffers must be on the device
+        mx.mxfp4_gemm_host(a_host, packed, N, c_host, torch.zeros(M, K, dtype=torch.bfloat16), c_dev, stream=0)
+    with pytest.raises(ValueError):   # workspace on the host
+        mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, workspace=torch.zeros(64, dtype=torch.uint8),
+                           stream=0)
+    with pytest.raises(ValueError):   # packed weights too small
+        mx.mxfp4_gemm_host(a_host, packed[:1024], N, c_host, a_dev, c_dev, stream=0)
+    assert len(lib.calls) == 1
+
+
+def test_quantize_checks_supplied_outputs(lib):
+    rows, K = 3, 200                      # nblk = 7: the last block cut by K
+    x = dev(torch.zeros(rows, K, dtype=torch.bfloat16))
+    q, s = mx.mxfp4_quantize(x, stream=0)
+    assert tuple(q.shape) == (rows, 7 * 16) and tuple(s.shape) == (rows, 7)
+    q_ok = dev(torch.zeros(rows, 7 * 16, dtype=torch.uint8))
+    s_ok = dev(torch.zeros(rows, 7, dtype=torch.uint8))
+    mx.mxfp4_quantize(x, q_ok, s_ok, stream=0)
+    assert [a[4:6] for _, a in lib.calls] == [(q.data_ptr(), s.data_ptr()), (q_ok.data_ptr(), s_ok.data_ptr())]
+    for bad_q, bad_s in [
+        (dev(torch.zeros(rows, K // 2, dtype=torch.uint8)), s_ok),        # K/2 bytes: one block short
+        (q_ok, dev(torch.zeros(rows, K // 32, dtype=torch.uint8))),       # floor(K/32) scales: one short
+        (_meta(rows, 7 * 16), s_ok),                                       # another device
+        (q_ok, dev(torch.zeros(rows, 14, dtype=torch.uint8))[:, :7]),     # not contiguous
+        (dev(torch.zeros(rows, 7 * 16, dtype=torch.int32)), s_ok),        # not bytes
+    ]:
+        with pytest.raises(ValueError):
+            mx.mxfp4_quantize(x, bad_q, bad_s, stream=0)
+    assert len(lib.calls) == 2
+
+
+def test_prepack_checks(lib):
+    N, K = 130, 256
+    bq = dev(torch.zeros(N, K // 2, dtype=torch.uint8))
+    bs = dev(torch.zeros(N, K // 32, dtype=torch.uint8))
+    size = mx.mxfp4_prepack_b_size(N, K)
+    out = dev(torch.zeros(size, dtype=torch.uint8))
+    assert mx.mxfp4_prepack_b(bq, bs, out, stream=0) is out
+    assert lib.calls[-1][1][:4] == (bq.data_ptr(), bs.data_ptr(), N, K)
+    for args in [
+        (bq, _meta(N, K // 32)),                                   # scales on another device
+        (bq, dev(torch.zeros(N, K // 32 + 1, dtype=torch.uint8))),  # inconsistent scales
+        (bq, bs, out[:-1]),                                         # packed one byte short
+        (bq, bs, _meta(size)),                                      # packed on another device
+        (dev(torch.zeros(N, K // 2, dtype=torch.int16)), bs),       # codes not bytes
+    ]:
+        with pytest.raises(ValueError):
+            mx.mxfp4_prepack_b(*args, stream=0)
+    assert len(lib.calls) == 1
