@@ -51,6 +51,9 @@ class _Options(ctypes.Structure):
 def load_library() -> ctypes.CDLL:
     """Load (building first if needed) libmxfp4_gb300.so. Raises if that is impossible."""
     global _LIB
+    lib = _LIB
+    if lib is not None:   # loaded: no lock on the per-call path
+        return lib
     with _LOCK:
         if _LIB is None:
             path = _build.LIB_PATH
