@@ -10,7 +10,8 @@ streams its weights from DRAM rather than L2.
 Prints ONE JSON line. `value` is microseconds per call (lower is better); TFLOPS, GB/s and
 the roofline fraction ride along, with the same measurement for every workload in
 `per_shape`. `--impl reference` times the CPU oracle instead (the method has no runnable
-reference implementation here).
+reference implementation here): `--warmup` untimed and `--steps` timed whole calls on a sample
+of the output columns sized to about two minutes, time scaled to all of N.
 """
 from __future__ import annotations
 
@@ -318,6 +319,37 @@ def cpu_oracle_step_time(w, budget_s: float = 12.0, threads: int = 0):
             "sample": f"{n} oracle call(s) on {rows} of {w.M} rows of {w.name}, time scaled by {scale:g}"}
 
 
+def reference_arm(w, steps: int, warmup: int, budget_s: float = 120.0) -> dict:
+    """--impl reference: the oracle as it stands on the host cores, `warmup` untimed steps then
+    `steps` timed ones. A step is the whole call (quantize A, dequantize, fp64 GEMM, bf16 cast) on
+    the first `cols` weight rows, i.e. output columns; its cost grows in proportion to them, so
+    the time is scaled by N / cols. cols is all of N unless that would take the run past budget_s
+    (sized from an untimed probe on a few columns)."""
+    import oracle
+    a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
+    bq, bs = oracle.quantize(workloads.bf16_bits(b_cpu))     # B pre-quantized: not timed
+    a_bits = workloads.bf16_bits(a_cpu)
+
+    def call(cols):
+        aq, as_ = oracle.quantize(a_bits)
+        oracle.to_bf16(oracle.mxfp4_gemm_ref(aq, as_, bq[:cols], bs[:cols]))
+
+    probe = min(w.N, 128)
+    t0 = time.perf_counter()
+    call(probe)
+    per_col = (time.perf_counter() - t0) / probe
+    cols = max(1, min(w.N, int(budget_s / (max(1, steps + warmup) * per_col))))
+    for _ in range(warmup):
+        call(cols)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call(cols)
+    dt = (time.perf_counter() - t0) / max(1, steps)
+    return {"us_per_call": 1e6 * dt * w.N / cols, "cores": oracle.num_threads(),
+            "sample": f"{steps} timed steps after {warmup} untimed, each the whole call on {cols} of {w.N} "
+                      f"output columns of {w.name}, time scaled by {w.N / cols:g}"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -339,7 +371,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        r = cpu_oracle_step_time(w)
+        r = reference_arm(w, args.steps, args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": r["us_per_call"], "unit": "us/call",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": r["us_per_call"] / 1000.0, "higher_is_better": False, "scaling": "weak",

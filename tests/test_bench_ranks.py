@@ -49,3 +49,23 @@ def test_traffic_is_dropped_when_kernel_sources_or_plan_change(monkeypatch):
     assert bench.measured_traffic(name, dict(plan, splits=5)) is None          # another launch plan
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, "0000000000000000", sig))
     assert bench.measured_traffic(name, plan) is None                          # other device code
+
+
+def test_reference_arm_counts_steps_and_bounds_its_sample(monkeypatch):
+    # the reference arm runs `warmup` untimed and `steps` timed oracle calls on a column sample
+    # sized to its time budget, and scales the time by N / columns
+    import bench
+    import oracle
+    from block_scaled_mxfp4_bf16_gb300 import workloads
+    w = workloads.Workload("tiny", 4, 256, 128)
+    calls = []
+    real = oracle.mxfp4_gemm_ref
+    monkeypatch.setattr(oracle, "mxfp4_gemm_ref", lambda aq, as_, bq, bs: calls.append(bq.shape[0]) or
+                        real(aq, as_, bq, bs))
+    r = bench.reference_arm(w, steps=4, warmup=2)
+    assert calls == [128] + [256] * 6            # probe, then whole-N steps within the budget
+    assert r["us_per_call"] > 0 and "4 timed steps after 2 untimed" in r["sample"]
+    calls.clear()
+    r = bench.reference_arm(w, steps=4, warmup=2, budget_s=1e-9)
+    assert calls == [128] + [1] * 6              # a budget too small for anything: one column
+    assert "on 1 of 256 output columns" in r["sample"] and "scaled by 256" in r["sample"]
