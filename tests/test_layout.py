@@ -8,13 +8,19 @@ import re
 ROOT = pathlib.Path(__file__).resolve().parent.parent
 PKG = ROOT / "block_scaled_mxfp4_bf16_gb300"
 ORACLE = ROOT / "oracle"
-SKIP_DIRS = {"_work", "_build", "gpurun_out", "baseline", "__pycache__", ".git"}
+SOURCE_DIRS = (PKG, ORACLE, ROOT / "tests", ROOT / "include")   # plus the scripts at the root
 
 
 def _sources(base: pathlib.Path, suffixes):
     for p in base.rglob("*"):
-        if p.suffix in suffixes and p.is_file() and not SKIP_DIRS.intersection(p.relative_to(ROOT).parts):
+        if p.suffix in suffixes and p.is_file() and "__pycache__" not in p.parts:
             yield p
+
+
+def _all_sources(suffixes):
+    for d in SOURCE_DIRS:
+        yield from _sources(d, suffixes)
+    yield from (p for p in ROOT.glob("*") if p.suffix in suffixes and p.is_file())
 
 
 def _imported_modules(py: pathlib.Path):
@@ -47,7 +53,7 @@ def test_oracle_c_includes_only_system_headers():
 
 def test_no_source_reads_the_scratch_folder():
     pat = re.compile(r"""(["'/\\])_work(/|\\|["'])""")
-    this = pathlib.Path(__file__).resolve()   # names the folder only to skip it
-    for src in _sources(ROOT, {".py", ".cu", ".cuh", ".h", ".c", ".cpp", ".sh", ".toml", ".cfg", ".ini"}):
+    this = pathlib.Path(__file__).resolve()   # names the folder only to look for it
+    for src in _all_sources({".py", ".cu", ".cuh", ".h", ".c", ".cpp", ".sh", ".toml", ".cfg", ".ini"}):
         if src.resolve() != this:
             assert not pat.search(src.read_text()), src
