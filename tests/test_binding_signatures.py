@@ -88,3 +88,13 @@ def test_option_and_plan_structs_match_the_header(tmp_path):
     O, P = mx._Options, mx._PlanInfo
     assert opt == [ctypes.sizeof(O), O.path.offset, O.splits.offset, O.m_tile.offset]
     assert plan == [ctypes.sizeof(P), P.reduction.offset, P.tmem_cols.offset, P.reserved.offset]
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    # the no-allocation GEMM's tests size their shapes against the library's fixed scratch
+    m = re.search(r"#define\s+MXFP4_NOALLOC_SCRATCH_BYTES\s+\(([\du\s*]+)\)", open(HEADER).read())
+    value = 1
+    for factor in m.group(1).replace("u", "").split("*"):
+        value *= int(factor)
+    import test_zz_no_alloc
+    assert test_zz_no_alloc.NOALLOC_BYTES == value == 32 << 20
