@@ -169,8 +169,9 @@ int mxfp4_gemm_ex(const void *a, int64_t M, int64_t K, int64_t lda,
                   const mxfp4_gemm_options *opts, void *stream);
 size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts);
 
-/* The plan mxfp4_gemm_ex would run: path (1 fused / 2 two-kernel), splits, M tile, number
- * of CTAs, pipeline stages. Returns MXFP4_OK or an argument error. */
+/* The plan mxfp4_gemm_ex would run on the current device: path (1 fused / 2 two-kernel),
+ * splits, M tile, number of CTAs, pipeline stages (NULL outputs are skipped). Returns MXFP4_OK,
+ * an argument or shape error, or MXFP4_ERR_ARCH / MXFP4_ERR_CUDA from the device query. */
 int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts,
                     int *path, int *splits, int *m_tile, int *ctas, int *stages);
 
@@ -215,8 +216,9 @@ typedef struct mxfp4_plan_info {
     int reserved[6];
 } mxfp4_plan_info;
 
-/* The full plan mxfp4_gemm_ex would run (superset of mxfp4_gemm_plan). `info` must not be
- * NULL. Returns MXFP4_OK or an argument / shape error. */
+/* The full plan mxfp4_gemm_ex would run on the current device (superset of mxfp4_gemm_plan).
+ * `info` must not be NULL. Returns MXFP4_OK, an argument / shape error, or MXFP4_ERR_ARCH /
+ * MXFP4_ERR_CUDA from the device query. */
 int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts, mxfp4_plan_info *info);
 
 /*
