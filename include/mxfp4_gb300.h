@@ -236,7 +236,8 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
  * mxfp4_device_status -- synchronize `stream`, then read and clear the library's device
  * error word for the current device: MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel gave up a
  * bounded wait (the kernel then skipped its remaining work and released its resources;
- * its outputs are undefined). Returns MXFP4_ERR_CUDA if the synchronization failed.
+ * its outputs are undefined). Returns MXFP4_ERR_CUDA if the synchronization or the read
+ * failed, MXFP4_ERR_ARCH on a device other than compute capability 10.3.
  */
 int mxfp4_device_status(void *stream);
 
