@@ -69,3 +69,33 @@ def test_reference_arm_counts_steps_and_bounds_its_sample(monkeypatch):
     r = bench.reference_arm(w, steps=4, warmup=2, budget_s=1e-9)
     assert calls == [128] + [1] * 6              # a budget too small for anything: one column
     assert "on 1 of 256 output columns" in r["sample"] and "scaled by 256" in r["sample"]
+
+
+def _run_bench(args, env_extra):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **env_extra)
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], env=env, cwd=root,
+                         capture_output=True, text=True, timeout=600, check=True).stdout
+    return [json.loads(line) for line in out.splitlines() if line.startswith("{")]
+
+
+def test_reference_arm_json_line():
+    lines = _run_bench(["--impl", "reference", "--workload", "M4_N2880_K512", "--steps", "2", "--warmup", "3"],
+                       {"RANK": "0", "WORLD_SIZE": "1"})
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["unit"] == "us/call" and line["higher_is_better"] is False and line["value"] > 0
+    assert line["config"]["workload"] == "M4_N2880_K512"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1 and "2 timed steps after 3 untimed" in line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_bench(["--impl", "reference", "--workload", "M4_N2880_K512", "--steps", "2"],
+                      {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
