@@ -98,3 +98,14 @@ def test_noalloc_scratch_size_matches_the_header():
         value *= int(factor)
     import test_zz_no_alloc
     assert test_zz_no_alloc.NOALLOC_BYTES == value == 32 << 20
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None or shutil.which("g++") is None, reason="needs gcc and g++")
+@pytest.mark.parametrize("compiler,std", [("gcc", "c99"), ("gcc", "c11"), ("g++", "c++17")])
+def test_header_is_strict_c_and_cpp(tmp_path, compiler, std):
+    # the boundary is a plain C header: C callers include it as well as C++ ones
+    src = tmp_path / "use.c"
+    src.write_text('#include "mxfp4_gb300.h"\nint main(void) { return MXFP4_OK; }\n')
+    lang = ["-x", "c++"] if compiler == "g++" else []
+    subprocess.run([compiler, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), *lang, "-c", str(src), "-o", str(tmp_path / "use.o")], check=True)
