@@ -135,8 +135,9 @@ def _events():
 
 
 def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float = 0.0, e2e: bool = False,
-                   warm: bool = False):
-    """Time exactly `steps` back-to-back mxfp4_gemm calls of workload w.
+                   warm: bool = False, timings: int = 7):
+    """Time exactly `steps` back-to-back mxfp4_gemm calls of workload w (`timings` times; the
+    median counts).
 
     The calls are captured in CUDA graphs (programmatic-launch edges kept) and replayed, so
     the number is device time per call with host launch cost out of the way; each call uses
@@ -187,23 +188,29 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
         while time.time() < t_end:
             g_main.replay()
             torch.cuda.synchronize()
-    if torch.distributed.is_initialized():
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     e0, e1 = _events()
-    with torch.cuda.stream(side):
-        e0.record(side)
-        for _ in range(reps):
-            g_main.replay()
-        if g_tail is not None:
-            g_tail.replay()
-        e1.record(side)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    # The timed region -- exactly `steps` calls, a barrier and a synchronize on both sides -- is
+    # measured `timings` times; the median is reported, with every timing beside it.
+    elapsed = []
+    for _ in range(timings):
+        if torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            e0.record(side)
+            for _ in range(reps):
+                g_main.replay()
+            if g_tail is not None:
+                g_tail.replay()
+            e1.record(side)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        elapsed.append(e0.elapsed_time(e1))
+    ms = statistics.median(elapsed)
     status = mx.mxfp4_device_status()
     res = {"us_per_call": 1000.0 * ms / steps, "elapsed_ms": ms, "copies": copies, "plan": plan,
-           "kernels_per_call": 1 if plan["path"] == 1 else 2, "status": status}
+           "kernels_per_call": 1 if plan["path"] == 1 else 2, "status": status,
+           "timings_us_per_call": [round(1000.0 * t / steps, 3) for t in elapsed]}
     # the same calls launched one by one from the host (no graph), for comparison
     n_direct = min(steps, 2000)
     with torch.cuda.stream(side):
@@ -453,8 +460,10 @@ def main():
         "e2e": {"value": round(main_res["e2e_us_per_call"], 3), "unit": "us/call",
                 "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},
         "gpu_launches": args.steps * main_res["kernels_per_call"],
-        "timing": "CUDA-graph replay of back-to-back calls; direct host launches: "
+        "timing": f"CUDA-graph replay of back-to-back calls, the {args.steps}-call region timed "
+                  f"{len(main_res['timings_us_per_call'])} times, median reported; direct host launches: "
                   f"{main_res['direct_us_per_call']:.3f} us/call",
+        "timings_us_per_call": main_res["timings_us_per_call"],
         "clocks": clocks,
         "cpu_baseline": cpu,
         "per_shape": per_shape,

@@ -33,6 +33,9 @@
 // status word and unwinds (outputs undefined, no hang, tensor memory released).
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_device.cuh"
@@ -504,12 +507,16 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                                   map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(o)));
             }
         }
+        // An owner whose rows did not all arrive in time skips its sum and stores (the status
+        // word reports it). The bytes it still lacks belong to a peer that failed before posting:
+        // a peer that posted has its copy land well within the limit.
         const bool owner = warp >= 3 && r1 > r0;
-        if (owner && !mbar_wait_cluster(red_bar, 0, lim)) fail(p, flags);
+        const bool got = !owner || mbar_wait_cluster(red_bar, 0, lim);
+        if (!got) fail(p, flags);
         __syncwarp();
         cluster_arrive();
         if (threadIdx.x == 96) MXFP4_PHASE(9);
-        if (owner) {
+        if (owner && got) {
             const int et = threadIdx.x - 96;
             const int nrows = r1 - r0;
             const int nl4 = (et & 31) * 4;
@@ -598,7 +605,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             tmem_dealloc(tmem_base, p.tmem_cols);
         }
         if (warp >= 3 && r1 > r0) {
-            if (!mbar_wait_cluster(red_bar, 0, lim)) fail(p, flags);
+            if (!mbar_wait_cluster(red_bar, 0, lim)) {   // rows missing: no sum, no stores
+                fail(p, flags);
+                return;
+            }
             if (threadIdx.x == 96) MXFP4_PHASE(9);
             // owner: a thread sums 4 consecutive rows of one column over the sources in rank order
             const int et = threadIdx.x - 96;
@@ -710,19 +720,22 @@ __global__ void timeout_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
 }
 
 static cudaError_t set_kernel_attributes() {
-    static bool attr_set[64] = {};
+    static std::mutex mu;
+    static std::atomic<bool> attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
         for (auto* kernel : {mxfp4_gemm_kernel<false>, mxfp4_gemm_kernel<true>}) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     return cudaSuccess;
 }

@@ -84,7 +84,10 @@ int mxfp4_quantize(const void *x, int64_t rows, int64_t K, int64_t ld,
 
 /*
  * mxfp4_prepack_b_size -- bytes of the packed-B buffer mxfp4_prepack_b writes for an
- * [N, K] weight matrix: ceil(N/128) x ceil(K/256) blocks of 17408 bytes, one per 128-row
+ * [N, K] weight matrix. Its counterpart in the pages is the shuffled weight buffer their
+ * harness builds once before timing (submission 608632, `_new_generate_input`: B quantized,
+ * then `shuffle_weight` and `e8m0_shuffle` for the MFMA layout). Here the buffer is
+ * ceil(N/128) x ceil(K/256) blocks of 17408 bytes, one per 128-row
  * tile and 256-element K step, each holding that piece's e2m1 rows (16 KB, swizzled the
  * way the tensor cores read shared memory) and its e8m0 scales (1 KB, in the tensor-memory
  * scale-factor layout). Rows past N and K past the last multiple of 256 are zero padding.
@@ -111,7 +114,9 @@ int mxfp4_prepack_b(const void *bq, const void *bs, int64_t N, int64_t K,
 
 /*
  * mxfp4_gemm_workspace_size -- bytes of device workspace mxfp4_gemm needs for this shape
- * on the CURRENT device (the plan depends on its SM count). The workspace holds the
+ * on the CURRENT device (the plan depends on its SM count). Its counterpart in the pages is
+ * the per-shape buffer cache of submission 711914 (`_quant_buffers`: the quantized A and its
+ * scales, kept between calls of one shape), here owned by the caller. The workspace holds the
  * quantized A (as token blocks) of the two-kernel path; plans that quantize A inside the
  * GEMM (the automatic plan for small M, see mxfp4_gemm_plan_info) need none and return 0.
  * Split-K partial sums never leave the chip.
@@ -126,6 +131,11 @@ int mxfp4_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * mxfp4_gemm -- C = MXFP4(A) . MXFP4(B)^T in bf16, A quantized inside the call.
+ * Defined by the pages' GEMM kernels, for example submission 711914's
+ * `mxfp4_gemm_fused_k512_kernel`: A quantized per 1x32 block (`_mxfp4_quant_tile`), then
+ * `tl.dot_scaled(a_fp4, a_scales, "e2m1", b, b_scales, "e2m1")` accumulated in fp32 over K and cast
+ * to bf16; the entry point there is `custom_kernel`, which takes A, the pre-quantized B and
+ * its scales and returns C.
  * The products of e2m1 values and e8m0 scales are accumulated in fp32 on the tensor cores
  * (tcgen05.mma kind::mxf4, block size 32) and rounded once to bf16 (round to nearest even).
  *   a        : bf16 [M, K], row stride lda elements (lda >= K, lda % 8 == 0), 16-byte aligned.
@@ -238,6 +248,11 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
  * bounded wait (the kernel then skipped its remaining work and released its resources;
  * its outputs are undefined). Returns MXFP4_ERR_CUDA if the synchronization or the read
  * failed, MXFP4_ERR_ARCH on a device other than compute capability 10.3.
+ * There is one error word per device, shared by every stream. Only `stream` is synchronized:
+ * a kernel still running on another stream may set the word after it is read, and a timeout
+ * it set before is reported (and cleared) here. To attribute a timeout to one stream's work,
+ * synchronize the device (or every stream using the library) first, or pass NULL with the
+ * legacy default stream ordering every other blocking stream.
  */
 int mxfp4_device_status(void *stream);
 
@@ -269,7 +284,10 @@ int mxfp4_selftest_timeout(int limit_us, void *stream);
  *   MXFP4_ERR_WORKSPACE before anything is enqueued.
  *   No allocation: the call never calls cudaMalloc, cudaFree or any allocating routine.
  *   First call per device: it looks up the array's device address (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   with that device current; make that first call before any stream capture. The address
+ *   is kept for the life of the process: after cudaDeviceReset on a device the library must
+ *   not be called on that device again in the same process (the same holds for every entry
+ *   point, which keep the device's error-word address the same way).
  *   Sharing: all calls on a device share the one array and it keeps the previous call's
  *   contents; nothing in it has to start at zero (each call rewrites every byte it reads).
  *   Calls that can overlap on the GPU (different streams without ordering, or several host

@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE ONLY. The product package never imports this module; it is loaded by
 the tests, by ``__graft_entry__.smoke()`` and by the CPU-baseline leg of ``bench.py``.
 
-The arithmetic lives in ``mxfp4_oracle.c`` (plain C, fp32 quantizer exactly as the pages
-spell it out, fp64 GEMM); this module only compiles it with gcc and marshals numpy arrays.
+The arithmetic lives in ``mxfp4_oracle.c`` (plain C: the fp32 block scale as the pages
+spell it out, the element encode from the e2m1 definition, fp64 GEMM); this module only
+compiles it with gcc and marshals numpy arrays.
 It shares no code with the CUDA path.
 
 Sources (the "amd-mxfp4-mm" leaderboard submissions):
@@ -14,8 +15,9 @@ Sources (the "amd-mxfp4-mm" leaderboard submissions):
   * GEMM: ``dot_scaled`` of the two e2m1 operands with their e8m0 scales, fp32 accumulate
     in the pages; fp64 here, rounded once to bf16 (round to nearest even).
 
-Pins (tests/test_oracle_pins.py): the e2m1 grid, an exhaustive fp32 cross-check against an
-independent nearest-value encoder, hand-worked blocks (tests/golden/hand_blocks.json) and rows
+Pins (tests/test_oracle_pins.py): the e2m1 grid, an exhaustive fp32 cross-check of the
+nearest-value encoder against an independently built midpoint-counting encoder, hand-worked
+blocks (tests/golden/hand_blocks.json) and rows
 whose K cuts the last block (tests/golden/tail_blocks.json), the block maximum at every
 position of a block, the scale formula as the method states it, evaluated literally for every
 bf16 amax, an error-bound invariant, exact closed-form GEMMs and brute-force tiny GEMMs.
@@ -64,8 +66,8 @@ def configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_scale_exponent.argtypes = [ctypes.c_uint32]
     L.oracle_e2m1_encode.restype = ctypes.c_uint8
     L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
-    L.oracle_e2m1_encode_nearest.restype = ctypes.c_uint8
-    L.oracle_e2m1_encode_nearest.argtypes = [ctypes.c_float]
+    L.oracle_e2m1_encode_count.restype = ctypes.c_uint8
+    L.oracle_e2m1_encode_count.argtypes = [ctypes.c_float]
     L.oracle_e2m1_decode.restype = ctypes.c_double
     L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
     L.oracle_quantize.restype = None
@@ -199,8 +201,9 @@ def e2m1_encode(qx: float) -> int:
     return int(lib().oracle_e2m1_encode(float(qx)))
 
 
-def e2m1_encode_nearest(v: float) -> int:
-    return int(lib().oracle_e2m1_encode_nearest(float(v)))
+def e2m1_encode_count(v: float) -> int:
+    """The self-check's second encoder (midpoints counted), for the pins."""
+    return int(lib().oracle_e2m1_encode_count(float(v)))
 
 
 def e2m1_decode(code: int) -> float:

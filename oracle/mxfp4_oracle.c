@@ -11,8 +11,9 @@
  *     +0x200000 / &0xFF800000 rounding, floor(log2)-2 clamped to [-127,127], +127 bias);
  *     cross-checked against submission 608632, `_hw_mxfp4_quant_op` step 1 (direct
  *     exponent form).
- *   - element encode: submission 711914, `_mxfp4_quant_tile` (three-way saturate /
- *     sub-one / normal branch, round to nearest even, sign in bit 3).
+ *   - element encode: what submission 711914's `_mxfp4_quant_tile` computes for each
+ *     scaled element, written from the e2m1 definition: the nearest grid value, ties to
+ *     even, saturating at 6, sign in bit 3.
  *   - packing: even element in the low nibble, odd element in the high nibble
  *     (submission 608632, `_hw_mxfp4_quant_op` step 3).
  *   - GEMM: C = dequant(A) . dequant(B)^T accumulated in fp64, rounded once to bf16.
@@ -70,68 +71,54 @@ int oracle_scale_exponent(uint32_t amax_r_bits)
 uint8_t oracle_scale_byte(int s) { return (uint8_t)(s + 127); }
 
 /* ---------------------------------------------------------------------------------------
- * Element encode (submission 711914, `_mxfp4_quant_tile`, the sat / den / nor branch)
+ * Element encode: round an already-scaled fp32 value onto the e2m1 grid
  * ------------------------------------------------------------------------------------- */
-
-/* Encode one already-scaled fp32 value qx as an e2m1 code (bit 3 sign, bits 2..1
- * exponent with bias 1, bit 0 mantissa), round to nearest even, saturating at 6. */
-uint8_t oracle_e2m1_encode(float qx)
-{
-    uint32_t u = bits_of(qx);
-    uint32_t sign = u & 0x80000000u;
-    uint32_t mag = u ^ sign;             /* |qx| as bits */
-    float a = f32_of(mag);
-    uint8_t code;
-
-    if (a >= 6.0f) {
-        code = 7;                        /* saturate to 6.0 */
-    } else if (a < 1.0f) {
-        /* Sub-one range: the e2m1 grid is 0, 0.5 (and 1.0 by rounding up). Adding 2^22
-         * puts the fp32 ulp at 0.5, so the fp32 add itself rounds a to the nearest
-         * multiple of 0.5 with ties to even; the mantissa field then holds 2*round(a). */
-        float t = a + 4194304.0f;
-        code = (uint8_t)(bits_of(t) - (149u << 23));
-    } else {
-        /* [1, 6): move the exponent bias from 127 to 1 (subtract 126 from the exponent
-         * field), then round the 23-bit mantissa to its top bit, ties to even; a carry
-         * out of the mantissa bumps the exponent, which is the correct next code. */
-        uint32_t rebased = mag - (126u << 23);
-        uint32_t keep = (rebased >> 22) & 1u;      /* lsb that survives */
-        uint32_t rounded = rebased + 0x1FFFFFu + keep;
-        code = (uint8_t)(rounded >> 22);
-    }
-    return (uint8_t)(code | (sign >> 28));   /* sign into bit 3, also for values that round to 0 */
-}
 
 /* e2m1 decode from the bit fields of the format: exponent bias 1, one mantissa bit,
  * exponent 0 is the subnormal binade with step 0.5. */
 double oracle_e2m1_decode(uint8_t code)
 {
     int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
-    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    double v = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * (double)(1 << (e - 1));
     return s ? -v : v;
 }
 
-/* Independent encoder for cross-checking oracle_e2m1_encode: search the eight decoded
- * magnitudes for the nearest one, ties to the even code; finite values past 6 saturate by
- * being nearest to 6. Sign copied from the input's sign bit. Distances are compared
- * exactly: a is nearer to g2 than to g1 < g2 iff a is above their midpoint, and the
- * midpoint of two grid values is exact in double. */
-uint8_t oracle_e2m1_encode_nearest(float v)
+/* The e2m1 code of qx, from the definition of the element step in submission 711914's
+ * `_mxfp4_quant_tile` (its saturate / sub-one / normal branches): the grid magnitude
+ * nearest to |qx|, a tie going to the code whose mantissa bit is 0 (round to nearest even),
+ * finite magnitudes past 6 saturating to 6 (6 is the nearest grid value to them), and the
+ * sign of qx in bit 3 even when the magnitude rounds to 0 (reading Q6).
+ * The eight codes are scanned keeping the nearest so far. Distances are compared through
+ * midpoints, which is exact: two grid values are short dyadic fractions, so their midpoint
+ * is exact in double, and a float converts to double exactly. */
+uint8_t oracle_e2m1_encode(float qx)
 {
-    double grid[8];
-    double a = fabs((double)v);
+    double a = fabs((double)qx);
     int best = 0, c;
-    for (c = 0; c < 8; ++c) grid[c] = oracle_e2m1_decode((uint8_t)c);
     for (c = 1; c < 8; ++c) {
-        double lo = grid[best] < grid[c] ? grid[best] : grid[c];
-        double hi = grid[best] < grid[c] ? grid[c] : grid[best];
-        double mid = 0.5 * (lo + hi);
-        int c_nearer = (grid[c] == hi) ? (a > mid) : (a < mid);
-        int tie = (a == mid);
-        if (c_nearer || (tie && (c & 1) == 0 && (best & 1) == 1)) best = c;
+        double g_best = oracle_e2m1_decode((uint8_t)best), g_c = oracle_e2m1_decode((uint8_t)c);
+        double mid = 0.5 * (g_best + g_c);
+        int c_nearer = (g_c > g_best) ? (a > mid) : (a < mid);
+        int tie_to_even = (a == mid) && (c & 1) == 0 && (best & 1) == 1;
+        if (c_nearer || tie_to_even) best = c;
     }
-    return (uint8_t)(best | (signbit(v) ? 8 : 0));
+    return (uint8_t)(best | (signbit(qx) ? 8 : 0));
+}
+
+/* A second, independently built encoder for the exhaustive self-check below: the grid
+ * ascends with the code, so the code of |v| is the number of the seven midpoints between
+ * neighbouring grid values that |v| lies above, plus one when |v| sits exactly on a
+ * midpoint whose upper neighbour has the even code. Sign from v's sign bit. */
+uint8_t oracle_e2m1_encode_count(float v)
+{
+    double a = fabs((double)v);
+    int code = 0, c;
+    for (c = 0; c < 7; ++c) {
+        double mid = 0.5 * (oracle_e2m1_decode((uint8_t)c) + oracle_e2m1_decode((uint8_t)(c + 1)));
+        if (a > mid) code += 1;
+        else if (a == mid && ((c + 1) & 1) == 0) code += 1;
+    }
+    return (uint8_t)(code | (signbit(v) ? 8 : 0));
 }
 
 /* ---------------------------------------------------------------------------------------
@@ -248,8 +235,8 @@ void oracle_f64_to_bf16_array(const double *in, int64_t n, uint16_t *out)
 }
 
 /* ---------------------------------------------------------------------------------------
- * Exhaustive self-check: compare oracle_e2m1_encode with oracle_e2m1_encode_nearest over
- * every fp32 bit pattern in [lo, hi) (both signs). Returns the mismatch count and the
+ * Exhaustive self-check: compare oracle_e2m1_encode with oracle_e2m1_encode_count over
+ * every step-th fp32 bit pattern in [lo, hi) (both signs). Returns the mismatch count and the
  * first mismatching pattern through *first (0xFFFFFFFF if none).
  * ------------------------------------------------------------------------------------- */
 int64_t oracle_encode_selfcheck(uint32_t lo, uint32_t hi, uint32_t step, uint32_t *first)
@@ -263,7 +250,7 @@ int64_t oracle_encode_selfcheck(uint32_t lo, uint32_t hi, uint32_t step, uint32_
         int sgn;
         for (sgn = 0; sgn < 2; ++sgn) {
             float v = f32_of(u | (sgn ? 0x80000000u : 0u));
-            if (oracle_e2m1_encode(v) != oracle_e2m1_encode_nearest(v)) {
+            if (oracle_e2m1_encode(v) != oracle_e2m1_encode_count(v)) {
                 ++bad;
 #pragma omp critical
                 if (u < first_bad) first_bad = u;

@@ -21,11 +21,13 @@ MUTANTS = [
     ("amax without |x|", "amax = fmaxf(amax, fabsf(xs[i]));", "amax = fmaxf(amax, xs[i]);"),
     ("amax misses the last element", "amax = fmaxf(amax, fabsf(xs[i]));",
      "if (i < 31) amax = fmaxf(amax, fabsf(xs[i]));"),
-    ("saturation threshold", "if (a >= 6.0f) {", "if (a >= 5.0f) {"),
-    ("sub-one rounding step", "float t = a + 4194304.0f;", "float t = a + 8388608.0f;"),
-    ("ties-to-even bit dropped", "uint32_t rounded = rebased + 0x1FFFFFu + keep;", "uint32_t rounded = rebased + 0x1FFFFFu;"),
-    ("sign dropped", "return (uint8_t)(code | (sign >> 28));", "return (uint8_t)(code);"),
-    ("decode exponent bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("saturation: the search stops below 6", "for (c = 1; c < 8; ++c) {", "for (c = 1; c < 7; ++c) {"),
+    ("ties go to the odd code", "int tie_to_even = (a == mid) && (c & 1) == 0 && (best & 1) == 1;",
+     "int tie_to_even = (a == mid) && (c & 1) == 1 && (best & 1) == 0;"),
+    ("ties always round up", "int c_nearer = (g_c > g_best) ? (a > mid) : (a < mid);",
+     "int c_nearer = (g_c > g_best) ? (a >= mid) : (a < mid);"),
+    ("sign dropped", "return (uint8_t)(best | (signbit(qx) ? 8 : 0));", "return (uint8_t)(best);"),
+    ("decode exponent bias", "(1.0 + 0.5 * m) * (double)(1 << (e - 1))", "(1.0 + 0.5 * m) * (double)(1 << e)"),
     ("dequantize scale bias", "ldexp(1.0, (int)srow[k / 32] - 127)", "ldexp(1.0, (int)srow[k / 32] - 126)"),
     ("B transposed in the GEMM", "acc += a[m * K + k] * b[n * K + k];", "acc += a[m * K + k] * b[k * N + n];"),
     ("bf16 output rounds half up", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
@@ -47,7 +49,7 @@ def _pins():
         ("single product", pins.test_gemm_single_product_lands_in_place),
         ("brute-force GEMM", pins.test_gemm_brute_force_tiny_random),
         ("bf16 rounding", pins.test_bf16_rounding_matches_exact_rational_rounding),
-        ("encoder vs nearest search, |x| < 8 (every 97th pattern)",
+        ("encoder vs midpoint count, |x| < 8 (every 97th pattern)",
          lambda: _assert_selfcheck(0, 0x41000000, 97)),
     ]
     return out

@@ -47,7 +47,7 @@ def test_encode_grid_points_round_trip():
     for c in range(16):
         v = oracle.e2m1_decode(c)
         assert oracle.e2m1_encode(v) == c
-        assert oracle.e2m1_encode_nearest(v) == c
+        assert oracle.e2m1_encode_count(v) == c
 
 
 @pytest.mark.parametrize("qx,code", [
@@ -60,9 +60,9 @@ def test_encode_ties_and_saturation(qx, code):
     assert oracle.e2m1_encode(qx) == code
 
 
-def test_encode_exhaustive_below_8_matches_nearest_search():
-    # every fp32 bit pattern with |x| < 8, both signs: the pages' bit-trick encoder vs an
-    # independent nearest-grid search
+def test_encode_exhaustive_below_8_matches_midpoint_count():
+    # every fp32 bit pattern with |x| < 8, both signs: the nearest-grid search vs an
+    # independently built encoder that counts the grid midpoints below |x|
     bad, first = oracle.encode_selfcheck(0, 0x41000000, 1)
     assert bad == 0, hex(first)
 

@@ -4,8 +4,10 @@ cudaFree because they can synchronize the device). Its scratch is a fixed array 
 library instead of a caller workspace.
 
 Checked through the C ABI against the regular mxfp4_gemm, within the same tolerance the
-parity tests use, on two calls in a row (the array keeps the previous call's contents, so
-the second call shows the counters are cleared and nothing stale leaks through). This file
+parity tests use, on two calls in a row. The array keeps the previous call's contents and
+nothing in it is cleared between calls, so the second call of each shape shows that a call
+reads only bytes it has written itself; a larger call followed by a smaller one with a
+different tile shape shows the same when the stale bytes differ from the new ones. This file
 is collected last on purpose; it passes alone in a fresh process as well as after the rest.
 """
 import ctypes
@@ -88,3 +90,31 @@ def test_noalloc_rejects_scratch_beyond_its_limit():
     assert st == 7, L.mxfp4_status_string(st)          # MXFP4_ERR_WORKSPACE, nothing enqueued
     torch.cuda.synchronize()
     assert bool((c == 777.0).all())
+
+
+def test_noalloc_stale_larger_call_does_not_leak():
+    """A large two-kernel call with large-magnitude A leaves its quantized A in the array; a
+    smaller two-kernel call with another token tile and K-step count then reuses the same
+    bytes. The second result must be bit-identical to mxfp4_gemm with its own workspace."""
+    mx, L = _lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    big = (256, 512, 4096)
+    small = (40, 300, 520)
+    plans = [mx.mxfp4_gemm_plan(*s) for s in (big, small)]
+    assert all(p["path"] == 2 for p in plans)                     # both use the scratch
+    assert plans[0]["m_tile"] != plans[1]["m_tile"]
+    assert mx.mxfp4_gemm_workspace_size(*big) > mx.mxfp4_gemm_workspace_size(*small)
+    outs = []
+    for (M, N, K), scale in ((big, 1e3), (small, 1.0)):
+        a = workloads.random_bf16(M, K, seed=M + 3, scale=scale).cuda()
+        bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=N + 4).cuda())
+        packed = mx.mxfp4_prepack_b(bq, bs)
+        c = torch.full((M, N), 777.0, dtype=torch.bfloat16, device="cuda")
+        st = L.mxfp4_gemm_noalloc(a.data_ptr(), M, K, K, packed.data_ptr(), N, c.data_ptr(), N, stream)
+        assert st == 0, L.mxfp4_status_string(st)
+        torch.cuda.synchronize()
+        assert mx.mxfp4_device_status() == 0
+        outs.append((c, mx.mxfp4_gemm(a, packed, N)))
+    c_small, want_small = outs[1]
+    torch.cuda.synchronize()
+    assert torch.equal(c_small.view(torch.int16), want_small.view(torch.int16))
