@@ -209,7 +209,7 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
     ms = statistics.median(elapsed)
     status = mx.mxfp4_device_status()
     res = {"us_per_call": 1000.0 * ms / steps, "elapsed_ms": ms, "copies": copies, "plan": plan,
-           "kernels_per_call": 1 if plan["path"] == 1 else 2, "status": status,
+           "kernels_per_call": 2 if plan["path"] == 2 else 1, "status": status,
            "timings_us_per_call": [round(1000.0 * t / steps, 3) for t in elapsed]}
     # the same calls launched one by one from the host (no graph), for comparison
     n_direct = min(steps, 2000)

@@ -67,9 +67,25 @@ __host__ __device__ inline uint32_t block_sf_offset(uint32_t r, uint32_t kb_in_a
            (kb_in_atom & 3u);
 }
 
+// Weight-resident kernel (path 3, small token counts): each CTA requests its whole K slice of
+// weights (at most kResMaxAtoms 256-K steps) the moment it starts, loads its bf16 A blocks
+// straight into registers once the previous grid is done, quantizes them into token blocks in
+// shared memory, runs every MMA of the slice from one thread and reduces the K slices of a tile
+// by weight-row owners through distributed shared memory.
+constexpr int kResThreads = 384;           // 12 warps: warps 1-2 run tensor memory and the MMAs,
+constexpr int kResQuantThreads = kResThreads - 64;   // the other 10 quantize A
+constexpr int kResMaxAtoms = 8;
+constexpr int kResMaxMTile = 32;
+constexpr int kResMaxItemsPerThread = 2;   // 1x32 blocks of A per quantizing thread
+// Rows of the 128-row weight tile each cluster rank owns in the split-K reduction, and the
+// fp32 words one owned row takes per source in the receive buffer (tokens rounded up to 4).
+__host__ __device__ inline int res_rows_per_owner(int splits) { return (kTileN + splits - 1) / splits; }
+__host__ __device__ inline int res_row_words(int m_valid) { return (m_valid + 3) / 4 * 4; }
+
 // Tiling of one mxfp4_gemm call.
 struct GemmPlan {
-    int path;          // 1: A quantized by the GEMM's own warps; 2: standalone quantize first
+    int path;          // 1: A quantized by the GEMM's own warps; 2: standalone quantize first;
+                       // 3: the weight-resident kernel (A quantized inside it)
     int splits;        // K slices per output tile (= thread-block cluster size)
     int m_tile;        // tokens per tile = MMA N (multiple of 16, <= 256)
     int nmc;           // 128-row scale chunks per token tile
@@ -112,6 +128,21 @@ struct GemmArgs {
     uint32_t tmem_cols;
     int fused;
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)
+    uint64_t wait_limit_ns;
+};
+
+struct ResidentArgs {
+    const uint16_t* a;     // bf16 A [M, lda]
+    int64_t lda;
+    const uint8_t* bblk;   // weight blocks (packed B)
+    uint16_t* c;
+    int64_t ldc;
+    uint32_t* status;      // device error word
+    int M, N, K;
+    int m_tile, m_tiles, n_tiles, splits, k_atoms;
+    uint32_t a_block;      // bytes of one token block
+    uint32_t off_a, off_recv, off_bar;   // shared-memory offsets from the 1 KB-aligned base
+    uint32_t tmem_cols;
     uint64_t wait_limit_ns;
 };
 
@@ -169,6 +200,9 @@ cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t r
 cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out,
                            cudaStream_t s);
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t s);
+cudaError_t launch_gemm_resident(const GemmPlan& plan, const ResidentArgs& args, cudaStream_t s);
+// Clusters of `cluster_size` weight-resident CTAs with this much shared memory resident at once.
+int max_active_clusters_resident(int cluster_size, size_t smem_bytes);
 cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 // Clusters of `cluster_size` GEMM CTAs with this much shared memory resident at once (0 if unknown).
 int max_active_clusters(int cluster_size, size_t smem_bytes);

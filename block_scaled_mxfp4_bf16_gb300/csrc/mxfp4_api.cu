@@ -159,11 +159,111 @@ static int active_clusters(int device, int size, size_t smem) {
     return n;
 }
 
+static int active_clusters_resident(int device, int size, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(device, size, smem);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int n = max_active_clusters_resident(size, smem);
+    cache[key] = n;
+    return n;
+}
+
+// Shared memory, tensor memory and limits of a weight-resident plan whose token tile and split
+// count are set. one_per_sm pads shared memory so that no second CTA fits on an SM; otherwise a
+// CTA of the next call can start beside one of this call (and request its weights early).
+// MXFP4_ERR_SHAPE if the slice does not fit the kernel.
+static int plan_resident_layout(GemmPlan& p, bool one_per_sm) {
+    p.atoms_max = static_cast<int>(cdiv(p.k_atoms, p.splits));
+    if (p.atoms_max > kResMaxAtoms) return MXFP4_ERR_SHAPE;
+    if (static_cast<int64_t>(p.raw_rows) * p.atoms_max * 8 > static_cast<int64_t>(kResQuantThreads) * kResMaxItemsPerThread)
+        return MXFP4_ERR_SHAPE;                   // at most two 1x32 blocks of A per thread
+    p.nmc = 1;
+    p.a_block = static_cast<uint32_t>(p.m_tile) * 128u + 2u * kSfChunk;
+    p.stages = p.atoms_max;
+    p.issuers = 2;
+    p.off_a = static_cast<uint32_t>(p.atoms_max) * kWBlock;
+    p.off_araw = 0;
+    p.off_recv = p.off_a + static_cast<uint32_t>(p.atoms_max) * p.a_block;
+    const size_t recv_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * res_rows_per_owner(p.splits) *
+                                                 res_row_words(p.m_tile) * sizeof(float)
+                                           : 0;
+    p.off_bar = static_cast<uint32_t>(align_up(p.off_recv + recv_bytes, 16));
+    size_t end = p.off_bar + static_cast<size_t>(kResMaxAtoms + 3) * 8 + 8;
+    // one CTA per SM: pad so that a second one cannot fit next to it
+    const size_t sm_smem = 233472, one_only = sm_smem / 2 + 1;
+    if (one_per_sm && end + 2048 < one_only) end = one_only - 2048;
+    p.smem_bytes = align_up(end, 16) + 1024;      // + the 1 KB alignment of the base
+    if (p.smem_bytes > kSmemLimit) return MXFP4_ERR_SHAPE;
+    const uint32_t cols = 2u * static_cast<uint32_t>(p.m_tile) + 16u * static_cast<uint32_t>(p.atoms_max);
+    p.tmem_cols = 32;
+    while (p.tmem_cols < cols) p.tmem_cols <<= 1;
+    p.recv_dedicated = p.splits > 1 ? 1 : 0;
+    p.red_bulk = 0;
+    p.off_stage = 0;
+    p.ctas = p.m_tiles * p.n_tiles * p.splits;
+    p.ws_total = 0;
+    return MXFP4_OK;
+}
+
+// The weight-resident plan (rules from same-box measurements of the small-M workloads):
+//   * token tile 16 for M <= 16; for 17..32 tokens two 16-token tiles when K is at most two
+//     256-K steps (twice the CTAs for a launch that is all latency), one 32-token tile otherwise;
+//   * the most K slices, up to the portable cluster size, that keep at least two 256-K steps per
+//     slice, one wave of CTAs and every cluster resident with one CTA per SM (a one-step slice
+//     costs more in the reduction than it saves: 32x4096x512 2.38 us unsplit, 3.34 us in two);
+//   * with split-K, shared memory is not padded, so the next call's CTAs start beside this
+//     call's and request their weights early (8x2112x7168: 4.00 -> 3.70 us); without it one CTA
+//     per SM measured faster (32x4096x512: 2.50 -> 2.38 us, 4x2880x512: 2.04 -> 1.91 us).
+static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, int mtile_req, int sm_count,
+                              GemmPlan* P, const int* cluster_caps) {
+    GemmPlan p = {};
+    p.path = 3;
+    if (mtile_req != 0 && mtile_req != 16 && mtile_req != 32) return MXFP4_ERR_ARG;
+    p.k_atoms = static_cast<int>(cdiv(K, kAtomK));
+    p.m_tile = M <= 16 || p.k_atoms <= 2 ? 16 : kResMaxMTile;
+    if (mtile_req) p.m_tile = mtile_req;
+    p.m_tiles = static_cast<int>(cdiv(M, p.m_tile));
+    p.n_tiles = static_cast<int>(cdiv(N, kTileN));
+    p.raw_rows = static_cast<int>(std::min<int64_t>(M, p.m_tile));
+    const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
+    if (splits_req > 0) {
+        p.splits = std::max(1, std::min({splits_req, p.k_atoms, kMaxSplits}));
+        const int st = plan_resident_layout(p, p.splits == 1);
+        if (st != MXFP4_OK) return st;
+        *P = p;
+        return MXFP4_OK;
+    }
+    int dev = 0;
+    if (!cluster_caps && cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const int s_max = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(kAutoMaxSplits),
+                                                          std::max(1, p.k_atoms / 2),
+                                                          std::max<int64_t>(1, sm_count / std::max<int64_t>(1, units))}));
+    int last = MXFP4_ERR_SHAPE;
+    for (int s = s_max; s >= 1; --s) {
+        GemmPlan q = p;
+        q.splits = s;
+        last = plan_resident_layout(q, true);     // residency judged with one CTA per SM
+        if (last != MXFP4_OK) break;              // fewer slices only make each one larger
+        const int resident = cluster_caps ? cluster_caps[s] : active_clusters_resident(dev, s, q.smem_bytes);
+        if (s == 1 || units <= resident) {
+            if (s > 1 && (last = plan_resident_layout(q, false)) != MXFP4_OK) break;
+            *P = q;
+            return MXFP4_OK;
+        }
+    }
+    return last;
+}
+
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
               GemmPlan* P, const int* cluster_caps) {
     GemmPlan p = {};
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_SHAPE;
     if (mtile_req < 0 || mtile_req > kMaxMTile || mtile_req % 16 != 0) return MXFP4_ERR_ARG;
+    if (path_req == 3) return make_resident_plan(M, N, K, splits_req, mtile_req, sm_count, P, cluster_caps);
     // Token tile: all of M up to 128; 128 up to M = 512 (half the A traffic and reduction per
     // CTA of a 256 tile, measured faster on 256x4096x7168); 256 beyond.
     p.m_tile = M <= 128 ? static_cast<int>(cdiv(M, 16) * 16) : (M <= 512 ? 128 : kMaxMTile);
@@ -180,6 +280,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     p.raw_rows = static_cast<int>(std::min<int64_t>(M, p.m_tile));
     const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
+    // Up to 32 tokens the weight-resident kernel is the automatic choice wherever its K slices
+    // fit (it measured faster than both other paths on every such workload).
+    if (path_req == 0 && M <= 32 && mtile_req == 0 &&
+        make_resident_plan(M, N, K, splits_req, 0, sm_count, P, cluster_caps) == MXFP4_OK)
+        return MXFP4_OK;
     // Fused quantization puts A's load and quantization on the GEMM's critical path (behind the
     // dependency wait), while the two-kernel path overlaps them with the weight prologue but adds
     // a kernel and a dependency hop; the fused path wins for small token counts (below).
@@ -258,6 +363,31 @@ static int check_gemm_args(const void* a, int64_t M, int64_t K, int64_t lda, con
 // Enqueue one planned GEMM: the quantize kernel into `ws` for the two-kernel path, then the GEMM.
 static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, int64_t M, int64_t K, int64_t lda,
                     const void* packed_b, int64_t N, void* c, int64_t ldc, uint8_t* ws, cudaStream_t s) {
+    if (plan.path == 3) {
+        ResidentArgs r = {};
+        r.a = static_cast<const uint16_t*>(a);
+        r.lda = lda;
+        r.bblk = static_cast<const uint8_t*>(packed_b);
+        r.c = static_cast<uint16_t*>(c);
+        r.ldc = ldc;
+        r.status = di.status;
+        r.M = static_cast<int>(M);
+        r.N = static_cast<int>(N);
+        r.K = static_cast<int>(K);
+        r.m_tile = plan.m_tile;
+        r.m_tiles = plan.m_tiles;
+        r.n_tiles = plan.n_tiles;
+        r.splits = plan.splits;
+        r.k_atoms = plan.k_atoms;
+        r.a_block = plan.a_block;
+        r.off_a = plan.off_a;
+        r.off_recv = plan.off_recv;
+        r.off_bar = plan.off_bar;
+        r.tmem_cols = plan.tmem_cols;
+        r.wait_limit_ns = g_wait_limit_ns;
+        cudaError_t e = launch_gemm_resident(plan, r, s);
+        return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+    }
     if (plan.path == 2) {
         cudaError_t e = launch_quantize_blocks(static_cast<const uint16_t*>(a), M, K, lda, ws, plan.m_tile,
                                                plan.m_tiles, plan.k_atoms, plan.a_block, s);
@@ -317,6 +447,7 @@ static void fill_plan_info(const mxfp4::GemmPlan& plan, mxfp4_plan_info* info) {
     out.issuers = plan.issuers;
     // the form every CTA of a full token tile uses (a ragged last tile may post short runs)
     out.reduction = plan.splits == 1 ? 0
+                    : plan.path == 3 ? 4
                     : plan.red_bulk ? 3
                     : (red_rows_per(plan.m_tile, plan.splits) <= kRedVecMaxRows ? 2 : 1);
     out.recv_dedicated = plan.splits > 1 ? plan.recv_dedicated : 0;
@@ -408,7 +539,7 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
                     int* m_tile, int* ctas, int* stages) {
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
@@ -427,7 +558,7 @@ int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_optio
     if (!info) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
@@ -443,7 +574,7 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
     if (!info || sm_count < 1) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     int caps[kMaxSplits + 1];
     for (int s = 0; s <= kMaxSplits; ++s) caps[s] = cluster_caps ? cluster_caps[s] : (1 << 30);
     GemmPlan plan;
@@ -456,7 +587,7 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
 
 int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
                   int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts, void* stream) {
-    if (opts && (opts->path < 0 || opts->path > 2 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
     int st = check_gemm_args(a, M, K, lda, packed_b, N, c, ldc);
     if (st != MXFP4_OK || M == 0 || N == 0) return st;
     DeviceInfo di;

@@ -37,28 +37,11 @@
 #include <mutex>
 
 #include "internal.h"
+#include "mma_desc.cuh"
 #include "ptx.cuh"
 #include "quant_device.cuh"
 
 namespace mxfp4 {
-
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
-__device__ __forceinline__ uint64_t desc_sf(uint32_t addr) { return smem_desc(addr, 0, 128, 0); }
-
-// Instruction descriptor, kind::mxf4: e2m1 x e2m1, both K-major, UE8M0 scales, M = 128.
-__device__ __forceinline__ uint32_t idesc_mxf4(uint32_t n_mma) {
-    return (1u << 7)                        // A format: e2m1
-         | (1u << 10)                       // B format: e2m1
-         | ((n_mma >> 3) << 17)             // N / 8
-         | (1u << 23)                       // scale factor type UE8M0
-         | ((uint32_t(kTileN) >> 4) << 24); // M / 16
-}
-
-// Two fp32 -> two bf16 (round to nearest even) in one word, `lo` in the low half.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 __device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp == 3 && lane == 0; }
 

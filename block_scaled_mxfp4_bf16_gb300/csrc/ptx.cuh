@@ -20,6 +20,13 @@ namespace mxfp4 {
 
 #ifdef MXFP4_TRACE
 static __device__ unsigned long long trace_buffer[4096][16];
+static __device__ unsigned int trace_counter;   // next trace row (a timing build's CTAs take one each)
+
+__device__ __forceinline__ uint64_t grid_id() {
+    uint64_t v;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(v));
+    return v;
+}
 #endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -62,6 +69,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Non-blocking probe of the same (test_wait never suspends the thread, so a loop can poll
+// several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(smem_addr(bar)), "r"(parity)

@@ -23,15 +23,16 @@ def plan(mx, M, N, K, **kw):
 
 
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
-    (16, 3072, 1536, 1, 3, 16),      # fused A quantization, 72 CTAs
-    (8, 2112, 7168, 1, 6, 16),       # fused, 6-slice clusters, 102 CTAs
-    (32, 4096, 512, 1, 1, 16),       # fused in two 16-token tiles, one block per thread, 64 CTAs
+    (16, 3072, 1536, 3, 3, 16),      # weight-resident, two 256-K steps per slice, 72 CTAs
+    (8, 2112, 7168, 3, 6, 16),       # weight-resident, 6-slice clusters, 102 CTAs
+    (32, 4096, 512, 3, 1, 16),       # weight-resident in two 16-token tiles, unsplit, 64 CTAs
     (64, 7168, 2048, 2, 1, 64),      # longer K keeps one token tile
     (256, 4096, 7168, 2, 2, 128),    # 128-token tiles, 2 slices (bulk split-K)
-    (16, 2112, 7168, 2, 5, 16),      # fused would be two blocks per thread: two-kernel, 5 slices
-    (4, 2880, 512, 1, 1, 16),        # fused, one 1x32 block per thread or less
-    (32, 2880, 512, 1, 1, 16),
-    (24, 2112, 7168, 2, 5, 32),      # fused would be two blocks per thread: two-kernel
+    (16, 2112, 7168, 3, 6, 16),      # weight-resident: two 1x32 blocks of A per thread
+    (4, 2880, 512, 3, 1, 16),
+    (32, 2880, 512, 3, 1, 16),
+    (24, 2112, 7168, 2, 5, 32),      # too many A blocks per thread for the resident kernel
+    (1, 128, 65536, 1, 8, 16),       # slices too long for the resident kernel: fused path
 ])
 def test_workload_plans(mx, M, N, K, path, splits, m_tile):
     p = plan(mx, M, N, K)
@@ -45,7 +46,7 @@ def test_invariants_over_a_grid(mx):
     for M in (1, 5, 8, 16, 17, 33, 64, 100, 128, 200, 256, 300, 512, 1000, 4096):
         for N in (128, 2112, 7168):
             for K in (8, 40, 64, 256, 1280, 1288, 4096, 7168, 16384, 65536):   # with K tails
-                for path in (0, 1, 2):
+                for path in (0, 1, 2, 3):
                     for splits in (0, 1, 2, 3, 5, 8, 16):
                         try:
                             p = plan(mx, M, N, K, path=path, splits=splits)
@@ -54,6 +55,10 @@ def test_invariants_over_a_grid(mx):
                         checked += 1
                         steps = -(-(-(-K // 256)) // p["splits"])     # 256-K steps of the longest slice
                         assert 1 <= p["issuers"] <= 2 and 1 <= p["stages"] <= 8, p
+                        if p["path"] == 3:    # the whole slice resident, two A blocks per thread at most
+                            assert p["stages"] == steps and p["m_tile"] in (16, 32), p
+                            assert min(M, p["m_tile"]) * steps * 8 <= 640, (M, N, K, p)
+                            assert p["smem_bytes"] <= 227 * 1024, p
                         if steps > p["stages"]:   # refilled stages: one MMA thread per stage
                             assert p["stages"] % p["issuers"] == 0, (M, N, K, path, splits, p)
                         t = p["tmem_cols"]
@@ -86,23 +91,31 @@ def test_cluster_residency_limits_the_split(mx):
     assert mx.mxfp4_gemm_plan_model(1, 128, 65536, SM_COUNT, None)["splits"] <= 8
 
 
-def test_automatic_fused_plans_keep_one_block_per_thread_and_one_wave(mx):
-    # the automatic plan is fused only for M <= 32 in 16-token tiles, and only while the in-kernel
-    # quantization is at most one 1x32 block per thread (352 threads) and the CTAs fit one wave
-    fused = two_kernel = 0
+def test_automatic_small_m_plans_keep_their_limits_and_one_wave(mx):
+    # up to 32 tokens the automatic plan is the weight-resident kernel wherever its slices fit
+    # (at most two 1x32 blocks of A per quantizing thread, eight 256-K steps per slice); where
+    # they do not, the fused plan only while its quantization is at most one block per thread
+    # (352 threads); the CTAs fit one wave either way
+    resident = fused = two_kernel = 0
     for M in (1, 4, 8, 13, 16, 17, 24, 32, 33, 64):
         for N in (128, 2112, 2880, 4096, 7168):
             for K in (64, 512, 1536, 2048, 7168, 16384):
                 p = plan(mx, M, N, K)
-                if p["path"] == 1:
+                atoms_max = -(-(-(-K // 256)) // p["splits"])
+                if p["path"] == 3:
+                    resident += 1
+                    assert M <= 32 and p["m_tile"] in (16, 32), (M, N, K, p)
+                    assert min(M, p["m_tile"]) * 8 * atoms_max <= 640 and atoms_max <= 8, (M, N, K, p)
+                    assert p["splits"] == 1 or atoms_max >= 2, (M, N, K, p)
+                    assert p["ctas"] <= SM_COUNT, (M, N, K, p)
+                elif p["path"] == 1:
                     fused += 1
                     assert M <= 32 and p["m_tile"] == 16, (M, N, K, p)
-                    atoms_max = -(-(-(-K // 256)) // p["splits"])
                     assert min(M, 16) * 8 * atoms_max <= 352, (M, N, K, p)
                     assert p["ctas"] <= SM_COUNT, (M, N, K, p)
                 else:
                     two_kernel += 1
-    assert fused and two_kernel
+    assert resident and two_kernel
 
 
 def test_errors(mx):
