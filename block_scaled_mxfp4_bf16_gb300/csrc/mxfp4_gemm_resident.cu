@@ -35,9 +35,10 @@
 
 // Phase stamps of a timing build (-DMXFP4_TRACE): each CTA takes its own row of the trace buffer
 // (in start order, so consecutive launches stay apart) and records its grid id, block index and
-// SM; a product build compiles them to nothing.
+// SM, the global timer and the SM clock at its start and end (slots 0/10 and 13/11), and the SM
+// clock at each phase; a product build compiles them to nothing.
 #ifdef MXFP4_TRACE
-#define RES_PHASE(slot) (::mxfp4::trace_buffer[trace_row][(slot)] = ::mxfp4::global_timer_ns())
+#define RES_PHASE(slot) (::mxfp4::trace_buffer[trace_row][(slot)] = ::mxfp4::sm_clock())
 #else
 #define RES_PHASE(slot) ((void)0)
 #endif
@@ -45,6 +46,11 @@
 namespace mxfp4 {
 
 namespace {
+
+__device__ __forceinline__ void res_fail(const ResidentArgs& p, volatile uint32_t* abort_flag) {
+    atomicOr(p.status, 1u);
+    *abort_flag = 1u;
+}
 
 // 32 bf16 of A from `src` with `avail` elements left in the row (a multiple of 8, > 0): the
 // 16-byte pieces at or past the row's end are not read and count as zeros. Loads bypass L1
@@ -59,11 +65,6 @@ __device__ __forceinline__ void load_a_block(const uint16_t* src, int avail, uin
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
-}
-
-__device__ __forceinline__ void res_fail(const ResidentArgs& p, volatile uint32_t* abort_flag) {
-    atomicOr(p.status, 1u);
-    *abort_flag = 1u;
 }
 
 // One 1x32 block of A owned by a quantizing thread.
@@ -144,6 +145,7 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
     if (threadIdx.x == 0) {
         const unsigned int row = atomicAdd(&trace_counter, 1u) & 4095u;
         trace_row_s = row;
+        trace_buffer[row][10] = sm_clock();
         trace_buffer[row][0] = global_timer_ns();
         trace_buffer[row][12] = sm_id();
         trace_buffer[row][14] = grid_id();
@@ -174,7 +176,6 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             mbar_arrive_expect_tx(&full[j], kWBlock);
             bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol);
         }
-        RES_PHASE(1);
     }
 
     if (warp == 1 || warp == 2) {
@@ -197,7 +198,6 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         }
         tc_fence_after_sync();
         const uint32_t tmem_base = *tmem_slot;
-        if (threadIdx.x == 32) RES_PHASE(7);
         if (lane == 0) {
             // columns: accumulators [0, 2*m_tile), weight scales 8 per step, token scales 8 per step
             const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
@@ -230,7 +230,7 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
                     }
                 }
             }
-            if (threadIdx.x == 32) RES_PHASE(3);
+            if (threadIdx.x == 32) RES_PHASE(5);
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll 1
@@ -253,12 +253,11 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
                     mma_mxf4(t_acc, wd + 2, td + 2, idesc1, sfw, sft, 1);
                     mma_mxf4(t_acc, wd + 4, td + 4, idesc0, sfw + 4u, sft + 4u, 1);
                     mma_mxf4(t_acc, wd + 6, td + 6, idesc1, sfw + 4u, sft + 4u, 1);
-                    if (j == 0 && threadIdx.x == 32) RES_PHASE(5);
                 }
             }
             if (!ok) res_fail(p, abort_flag);
             tc_commit(acc_full);                      // one arrival per issuer
-            if (threadIdx.x == 32) RES_PHASE(4);
+            if (threadIdx.x == 32) RES_PHASE(6);
             // never leave copies in flight into shared memory that is about to be freed
             for (int j = issuer; j < na; j += 2) mbar_wait(&full[j], 0, lim);
         }
@@ -289,11 +288,12 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         if (it0.valid && it0.avail > 0) load_a_block(it0.src, it0.avail, w0);
         if (it1.valid && it1.avail > 0) load_a_block(it1.src, it1.avail, w1);
         quantize_item(it0, w0, sA);
+        if (threadIdx.x == 0) RES_PHASE(3);
         quantize_item(it1, w1, sA);
         fence_proxy_async_smem();                     // the MMAs read the token blocks (async proxy)
         __syncwarp();
         if (lane == 0) mbar_arrive(a_ready);
-        if (threadIdx.x == 0) RES_PHASE(13);
+        if (threadIdx.x == 0) RES_PHASE(4);
     }
     if (warp < 4 || warp >= 8) {
         if (S > 1) cluster_wait();
@@ -304,14 +304,29 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
     named_barrier(1, 32 + 128);                       // the column base, published by warp 1
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // every peer's barriers exist (long since): settled here, while the MMAs run, with the
+    // destinations of this thread's split-K posts
+    const int q = warp & 3;                           // lane quadrant this warp may read
+    const int nl = q * 32 + lane;                     // weight row of the tile
+    const int G = words / 4;                          // groups of 4 tokens
+    uint32_t dst = 0u, bar = 0u;
+    int owner = 0;
+    if (S > 1) {
+        cluster_wait();
+        owner = nl / R;
+        const int rl = nl - owner * R;
+        // receive buffer [source][token group][owned row][4 floats]: the owner's summing
+        // threads read consecutive rows, 16 bytes apart
+        const uint32_t off = static_cast<uint32_t>(split * G * R + rl) * 16u;
+        dst = map_to_rank(smem_addr(sRecv) + off, static_cast<uint32_t>(owner));
+        bar = map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(owner));
+    }
     const bool waited = mbar_wait(acc_full, 0, lim);
     tc_fence_after_sync();
     if (!waited) res_fail(p, abort_flag);
-    if (threadIdx.x == 128) RES_PHASE(6);
+    if (threadIdx.x == 128) RES_PHASE(7);
     // one decision per warp (tcgen05.ld is warp-collective)
     const bool ok = !__any_sync(0xffffffffu, !waited || abort_flag[0] != 0u);
-    const int q = warp & 3;                           // lane quadrant this warp may read
-    const int nl = q * 32 + lane;                     // weight row of the tile
     uint32_t v[32];
     if (ok) {
         // the two issuers' accumulators, added (the second holds data from two steps on)
@@ -330,6 +345,7 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             tmem_load_wait();
         }
     }
+    if (threadIdx.x == 128) RES_PHASE(1);
     tc_fence_before_sync();
     named_barrier_arrive(2, 32 + 128);                // warp 1 may free tensor memory now
 
@@ -343,26 +359,22 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
                 cp += p.ldc;
             }
         }
-        if (threadIdx.x == 128) RES_PHASE(11);
+#ifdef MXFP4_TRACE
+        if (threadIdx.x == 128) {
+            trace_buffer[trace_row][11] = sm_clock();
+            trace_buffer[trace_row][13] = global_timer_ns();
+        }
+#endif
         return;
     }
 
     // K slices > 1: every weight row goes to its owner's receive buffer, slot = this rank
-    cluster_wait();                                   // every peer's barriers exist (long since)
-    const int G = words / 4;                          // groups of 4 tokens
     if (ok) {
-        const int o = nl / R;                         // owner rank of this row
-        const int rl = nl - o * R;
-        // receive buffer [source][token group][owned row][4 floats]: the owner's summing
-        // threads read consecutive rows, 16 bytes apart
-        const uint32_t off = static_cast<uint32_t>(split * G * R + rl) * 16u;
         const uint32_t gstep = static_cast<uint32_t>(R) * 16u;
-        const uint32_t dst = map_to_rank(smem_addr(sRecv) + off, static_cast<uint32_t>(o));
-        const uint32_t bar = map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(o));
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             if (g < G) {
-                if (o == split)
+                if (owner == split)
                     st_cluster_v4(dst + gstep * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
                 else
                     st_async_v4(dst + gstep * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], bar);
@@ -403,7 +415,12 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             }
         }
     }
-    if (threadIdx.x == 128) RES_PHASE(11);
+#ifdef MXFP4_TRACE
+    if (threadIdx.x == 128) {
+        trace_buffer[trace_row][11] = sm_clock();
+        trace_buffer[trace_row][13] = global_timer_ns();
+    }
+#endif
 }
 
 static cudaError_t set_resident_attributes() {

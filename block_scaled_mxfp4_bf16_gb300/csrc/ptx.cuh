@@ -39,6 +39,12 @@ __device__ __forceinline__ uint32_t sm_id() {
     return v;
 }
 
+__device__ __forceinline__ uint64_t sm_clock() {
+    uint64_t v;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(v));
+    return v;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
