@@ -43,6 +43,26 @@
 
 namespace mxfp4 {
 
+// A timing build (-DMXFP4_TRACE) gives each CTA its own row of the trace buffer (in start order,
+// so consecutive launches stay apart): grid id, block index, SM, the global timer and the SM
+// clock at its start (slots 0/10) and where it stores C (slots 13/11), and the SM clock at each
+// other phase.
+#ifdef MXFP4_TRACE
+static __shared__ unsigned int g_trace_row;
+__device__ __forceinline__ void trace_phase(int slot) {
+    const unsigned int row = g_trace_row;
+    if (slot == 0 || slot == 10 || slot == 13 || slot == 12) return;
+    if (slot == 11) {
+        trace_buffer[row][11] = sm_clock();
+        trace_buffer[row][13] = global_timer_ns();
+        return;
+    }
+    trace_buffer[row][slot] = sm_clock();
+}
+#undef MXFP4_PHASE
+#define MXFP4_PHASE(slot) ::mxfp4::trace_phase(slot)
+#endif
+
 __device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp == 3 && lane == 0; }
 
 // 32 accumulator columns of this thread's lane (the second 16 only if `upper`), plus the
@@ -192,8 +212,18 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     qs.a_full = a_full;
     qs.lim = lim;
 
-    if (threadIdx.x == 0) MXFP4_PHASE(0);
-    if (threadIdx.x == 0) MXFP4_TRACE_SM(12);
+#ifdef MXFP4_TRACE
+    if (threadIdx.x == 0) {
+        const unsigned int row = atomicAdd(&trace_counter, 1u) & 4095u;
+        g_trace_row = row;
+        trace_buffer[row][10] = sm_clock();
+        trace_buffer[row][0] = global_timer_ns();
+        trace_buffer[row][12] = sm_id();
+        trace_buffer[row][14] = grid_id();
+        trace_buffer[row][15] = blockIdx.x;
+    }
+    __syncthreads();
+#endif
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -713,7 +743,11 @@ static cudaError_t set_kernel_attributes() {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
         for (auto* kernel : {mxfp4_gemm_kernel<false>, mxfp4_gemm_kernel<true>}) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
+            cudaFuncAttributes fa = {};
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemLimit - fa.sharedSizeBytes));
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;

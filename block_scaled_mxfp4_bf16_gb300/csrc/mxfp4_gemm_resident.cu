@@ -389,22 +389,31 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         if (!got) res_fail(p, abort_flag);
         if (threadIdx.x == 128) RES_PHASE(9);
         if (got && ok) {
-            // thread t sums owned row t (consecutive threads: consecutive rows, contiguous in C)
-            // over the sources in rank order, four tokens at a time
-            const int r = static_cast<int>(threadIdx.x) - 128;
-            const int n = n0 + own0 + r;
-            if (r < own_rows && n < p.N) {
-                const float4* rv = reinterpret_cast<const float4*>(sRecv);
-                uint16_t* cp = p.c + static_cast<int64_t>(m0) * p.ldc + n;
-                for (int g = 0; g < G; ++g) {
-                    float4 acc = rv[g * R + r];
-                    for (int src = 1; src < S; ++src) {
-                        const float4 x = rv[(src * G + g) * R + r];
-                        acc.x += x.x;
-                        acc.y += x.y;
-                        acc.z += x.z;
-                        acc.w += x.w;
+            // thread t sums owned row t % own_rows, tokens 4g..4g+3 with g = t / own_rows, over
+            // the sources in rank order (consecutive threads: consecutive rows, contiguous in C)
+            const float4* rv = reinterpret_cast<const float4*>(sRecv);
+            for (int t = static_cast<int>(threadIdx.x) - 128; t < own_rows * G; t += 128) {
+                const int g = t / own_rows;
+                const int r = t - g * own_rows;
+                const int n = n0 + own0 + r;
+                float4 acc = rv[g * R + r];
+                for (int s0 = 1; s0 < S; s0 += 8) {
+                    float4 x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (s0 + i < S) x[i] = rv[((s0 + i) * G + g) * R + r];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (s0 + i < S) {
+                            acc.x += x[i].x;
+                            acc.y += x[i].y;
+                            acc.z += x[i].z;
+                            acc.w += x[i].w;
+                        }
                     }
+                }
+                if (n < p.N) {
+                    uint16_t* cp = p.c + static_cast<int64_t>(m0 + 4 * g) * p.ldc + n;
                     const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {

@@ -284,6 +284,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                  : "memory");
 }
 
+// Arrive on an mbarrier of (another) CTA of the cluster (a map_to_rank address), releasing this
+// thread's prior memory operations at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t rank) {
     uint32_t r;
