@@ -35,8 +35,22 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM launch from one ncu
 # capture (profiles/), valid only for the device code and the launch plan it was taken with (both
 # checked at run time; reported as null otherwise).
-MEASURED_TRAFFIC = {"M8_N2112_K7168": (8470784, "4597bb277acadcb2",
-                                      "path=1,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=2,recv_dedicated=1")}
+# Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
+# hash, plan signature); from the per-configuration ncu capture in profiles/.
+MEASURED_TRAFFIC = {
+    "M16_N3072_K1536": (2590460, None, "c8386da68f09d170",
+                        "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
+    "M8_N2112_K7168": (8435712, None, "c8386da68f09d170",
+                       "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=4,recv_dedicated=1"),
+    "M32_N4096_K512": (1180930, None, "c8386da68f09d170",
+                       "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
+    "M64_N7168_K2048": (7934210, 270848, "c8386da68f09d170",
+                        "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=2,reduction=0,recv_dedicated=0"),
+    "M256_N4096_K7168": (16633900, 3679740, "c8386da68f09d170",
+                         "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
+}
+NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against
+STEADY_STEPS = 1000                  # calls in a steady-state region
 HEADLINE = "M8_N2112_K7168"
 SUBMIT_COVER_CYCLES = 200_000        # ~0.1 ms of device time ahead of each timed region
 FALLBACK_HBM_GBS = 6800.0
@@ -70,10 +84,12 @@ def plan_signature(plan: dict) -> str:
 
 
 def measured_traffic(name: str, plan: dict):
+    """(GEMM bytes, quantizer bytes or None) of one launch, or None when the kernels' source or
+    the plan differ from the ones captured."""
     entry = MEASURED_TRAFFIC.get(name)
-    if entry is None or entry[1] != kernel_source_hash() or entry[2] != plan_signature(plan):
+    if entry is None or entry[2] != kernel_source_hash() or entry[3] != plan_signature(plan):
         return None
-    return entry[0]
+    return entry[0], entry[1]
 
 
 def max_over_ranks(value: float) -> float:
@@ -418,20 +434,32 @@ def main():
     if not args.no_shapes:
         fp4_peak, _ = fp4_peak_tflops()
         for ws_ in workloads.WORKLOADS + workloads.EXTRA_WORKLOADS:
-            r = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2)
-            rw = bench_workload(mx, ws_, max(200, args.steps // 4), args.warmup, l2, warm=True)
+            # the same --steps region as the headline (so the two agree for the same workload; a
+            # short region carries the first call, which no earlier call overlaps), a long
+            # region for the steady state, and a long region with one copy resident in L2
+            r = bench_workload(mx, ws_, args.steps, args.warmup, l2)
+            rs = bench_workload(mx, ws_, STEADY_STEPS, args.warmup, l2)
+            rw = bench_workload(mx, ws_, STEADY_STEPS, args.warmup, l2, warm=True)
             gbs = ws_.algorithmic_bytes / (r["us_per_call"] * 1e-6) / 1e9
+            gbs_s = ws_.algorithmic_bytes / (rs["us_per_call"] * 1e-6) / 1e9
             tf = ws_.flops / (r["us_per_call"] * 1e-6) / 1e12
             tf_warm = ws_.flops / (rw["us_per_call"] * 1e-6) / 1e12
+            traffic = measured_traffic(ws_.name, r["plan"])
             per_shape[ws_.name] = {"us_per_call": round(r["us_per_call"], 3),
-                                   "direct_us_per_call": round(r["direct_us_per_call"], 3),
+                                   "steady_us_per_call": round(rs["us_per_call"], 3),
+                                   "steady_hbm_frac": round(gbs_s / peak, 4),
+                                   "direct_us_per_call": round(rs["direct_us_per_call"], 3),
                                    "tflops": round(tf, 2),
                                    "algorithmic_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+                                   "hbm_frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                                    "fp4_frac": round(tf / fp4_peak, 4),
                                    "warm_l2_us_per_call": round(rw["us_per_call"], 3),
                                    "warm_l2_fp4_frac": round(tf_warm / fp4_peak, 4),
+                                   "gemm_dram_bytes": traffic[0] if traffic else None,
+                                   "quantizer_dram_bytes": traffic[1] if traffic else None,
                                    "path": r["plan"]["path"], "splits": r["plan"]["splits"],
-                                   "ctas": r["plan"]["ctas"], "status": max(r["status"], rw["status"])}
+                                   "ctas": r["plan"]["ctas"],
+                                   "status": max(r["status"], rs["status"], rw["status"])}
 
     quantizer = None
     if not args.no_shapes:
@@ -461,7 +489,9 @@ def main():
                    "ctas": main_res["plan"]["ctas"]},
         "tflops": round(w.flops / (t_us * 1e-6) / 1e12, 3),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "traffic": measured_traffic(w.name, main_res["plan"]), "peak_kind": peak_kind,
+                     "frac": round(gbs / peak, 4),
+                     "traffic": (measured_traffic(w.name, main_res["plan"]) or (None,))[0],
+                     "peak_kind": peak_kind, "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": w.algorithmic_bytes},
         "e2e": {"value": round(main_res["e2e_us_per_call"], 3), "unit": "us/call",
                 "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},

@@ -55,16 +55,33 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, extra_flags: list[str] | None = None, verbose: bool = False) -> str:
+def variant_path(variant: str) -> str:
+    """Path of a separately built variant of the library (for example the test-hook build)."""
+    return os.path.join(HERE, f"libmxfp4_gb300_{variant}.so")
+
+
+def build_variant(variant: str, extra_flags: list[str]) -> str:
+    """Build a variant of the library with extra flags into its own file and object directory,
+    leaving the product library alone; rebuilt only when a source is newer. Returns its path."""
+    path = variant_path(variant)
+    if os.path.exists(path) and all(os.path.getmtime(d) <= os.path.getmtime(path) for d in _deps()):
+        return path
+    return build(force=True, extra_flags=extra_flags, lib_path=path, obj_dir=os.path.join(BUILD_DIR, variant))
+
+
+def build(force: bool = False, extra_flags: list[str] | None = None, verbose: bool = False,
+          lib_path: str | None = None, obj_dir: str | None = None) -> str:
     """Compile and link the library if any source is newer than it. Returns its path."""
-    if not force and not extra_flags and up_to_date():
+    if lib_path is None and not force and not extra_flags and up_to_date():
         return LIB_PATH
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    out_path = lib_path or LIB_PATH
+    objs_dir = obj_dir or BUILD_DIR
+    os.makedirs(objs_dir, exist_ok=True)
     flags = NVCC_FLAGS + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objs_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -75,15 +92,16 @@ def build(force: bool = False, extra_flags: list[str] | None = None, verbose: bo
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    with open(FLAGS_STAMP, "w") as fh:
-        fh.write(" ".join(extra_flags or []))
-    return LIB_PATH
+    os.replace(tmp, out_path)
+    if lib_path is None:
+        with open(FLAGS_STAMP, "w") as fh:
+            fh.write(" ".join(extra_flags or []))
+    return out_path
 
 
 if __name__ == "__main__":

@@ -129,6 +129,9 @@ struct GemmArgs {
     int fused;
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)
     uint64_t wait_limit_ns;
+#ifdef MXFP4_TEST_HOOKS
+    uint8_t* token_dump;   // test build only: the fused CTAs of weight tile 0 copy their token blocks here
+#endif
 };
 
 struct ResidentArgs {
@@ -144,6 +147,9 @@ struct ResidentArgs {
     uint32_t off_a, off_recv, off_bar;   // shared-memory offsets from the 1 KB-aligned base
     uint32_t tmem_cols;
     uint64_t wait_limit_ns;
+#ifdef MXFP4_TEST_HOOKS
+    uint8_t* token_dump;   // test build only: the CTAs of weight tile 0 copy their token blocks here
+#endif
 };
 
 // Device properties the planner needs (cached per device).

@@ -347,6 +347,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
 
 static uint64_t g_wait_limit_ns = 1000000000ull;   // 1 s per bounded wait
 
+#ifdef MXFP4_TEST_HOOKS
+static void* g_token_dump = nullptr;   // test build only: see mxfp4_test_token_dump
+#endif
+
 // Argument checks shared by the GEMM entry points.
 static int check_gemm_args(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
                            const void* c, int64_t ldc) {
@@ -385,6 +389,9 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
         r.off_bar = plan.off_bar;
         r.tmem_cols = plan.tmem_cols;
         r.wait_limit_ns = g_wait_limit_ns;
+#ifdef MXFP4_TEST_HOOKS
+        r.token_dump = static_cast<uint8_t*>(g_token_dump);
+#endif
         cudaError_t e = launch_gemm_resident(plan, r, s);
         return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
     }
@@ -425,6 +432,9 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     g.fused = plan.path == 1 ? 1 : 0;
     g.c_vec4 = (ldc % 4 == 0 && aligned(c, 8)) ? 1 : 0;
     g.wait_limit_ns = g_wait_limit_ns;
+#ifdef MXFP4_TEST_HOOKS
+    g.token_dump = static_cast<uint8_t*>(g_token_dump);
+#endif
     cudaError_t e = launch_gemm(plan, g, s);
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
 }
@@ -686,6 +696,14 @@ int mxfp4_selftest_timeout(int limit_us, void* stream) {
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
 }
+
+#ifdef MXFP4_TEST_HOOKS
+// Test build only (-DMXFP4_TEST_HOOKS, never the product library): the CTAs of weight tile 0 of
+// a plan that quantizes A inside the GEMM (fused or weight-resident) copy the token blocks they
+// quantized to `dump` ([m_tiles][k_atoms][token block bytes], device memory, large enough), so a
+// test can compare the GEMM's own quantization of A byte for byte. NULL turns it off.
+void mxfp4_test_token_dump(void* dump) { g_token_dump = dump; }
+#endif
 
 }  // extern "C"
 

@@ -96,6 +96,9 @@ struct QuantSlice {
     uint64_t* a_raw;       // the staged rows have landed
     uint64_t* a_full;      // the token blocks are written (one arrival per warp)
     uint64_t lim;
+#ifdef MXFP4_TEST_HOOKS
+    uint8_t* dump;         // test build only: where this CTA's token blocks go (null: nowhere)
+#endif
 };
 
 // Every thread of the CTA takes part (the copy and MMA warps have nothing else to do until the
@@ -144,6 +147,16 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
         blk[q.a_rows + block_sf_offset(static_cast<uint32_t>(rr), c)] = static_cast<uint8_t>(sbyte);
     }
     if (qt == 96) MXFP4_PHASE(13);
+#ifdef MXFP4_TEST_HOOKS
+    // test build: the token blocks of weight tile 0's CTAs, as quantized, to the dump buffer
+    // [m_tiles][k_atoms][a_block] (every thread of the CTA runs this function)
+    __syncthreads();
+    if (q.dump) {
+        const int words = q.nblk / 8 * static_cast<int>(q.a_block) / 16;
+        for (int i = qt; i < words; i += kGemmThreads)
+            reinterpret_cast<uint4*>(q.dump)[i] = reinterpret_cast<const uint4*>(q.blocks)[i];
+    }
+#endif
     fence_proxy_async_smem();   // the MMAs read the token blocks through the async proxy
     __syncwarp();
     if (lane == 0) mbar_arrive(q.a_full);   // one arrival per warp
@@ -211,6 +224,9 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     qs.a_raw = a_raw;
     qs.a_full = a_full;
     qs.lim = lim;
+#ifdef MXFP4_TEST_HOOKS
+    qs.dump = (nt == 0 && p.token_dump) ? p.token_dump + (static_cast<size_t>(mt) * p.k_atoms + a0) * a_block : nullptr;
+#endif
 
 #ifdef MXFP4_TRACE
     if (threadIdx.x == 0) {

@@ -290,6 +290,17 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         quantize_item(it0, w0, sA);
         if (threadIdx.x == 0) RES_PHASE(3);
         quantize_item(it1, w1, sA);
+#ifdef MXFP4_TEST_HOOKS
+        // test build: the token blocks of weight tile 0's CTAs, as quantized, to the dump buffer
+        // [m_tiles][k_atoms][a_block]
+        named_barrier(5, kResQuantThreads);
+        if (nt == 0 && p.token_dump) {
+            uint8_t* dump = p.token_dump + (static_cast<size_t>(mt) * p.k_atoms + a0) * p.a_block;
+            const int words = na * static_cast<int>(p.a_block) / 16;
+            for (int i = qt; i < words; i += kResQuantThreads)
+                reinterpret_cast<uint4*>(dump)[i] = reinterpret_cast<const uint4*>(sA)[i];
+        }
+#endif
         fence_proxy_async_smem();                     // the MMAs read the token blocks (async proxy)
         __syncwarp();
         if (lane == 0) mbar_arrive(a_ready);
