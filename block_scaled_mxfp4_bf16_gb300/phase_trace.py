@@ -107,8 +107,9 @@ def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0
         rows = np.array(grids[gid])
         ghz = float(np.median((rows[:, 11] - rows[:, 10]) / np.maximum(1, rows[:, 13] - rows[:, 0])))
         for slot, name in names.items():
-            ok = rows[:, slot] > 0
-            agg[name].append(float(np.median((rows[ok, slot] - rows[ok, 2]) / ghz)))
+            ok = rows[:, slot] >= rows[:, 10]        # stamped by this launch (not left from another)
+            if ok.any():
+                agg[name].append(float(np.median((rows[ok, slot] - rows[ok, 2]) / ghz)))
         agg["cta_start"].append(float(np.median((rows[:, 10] - rows[:, 2]) / ghz)))
         agg["cta_end"].append(float(np.median((rows[:, 11] - rows[:, 2]) / ghz)))
         agg["sm_ghz"].append(ghz)
