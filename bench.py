@@ -38,15 +38,15 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2590460, None, "c8386da68f09d170",
+    "M16_N3072_K1536": (2590460, None, "08a99b7e175208b7",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8435712, None, "c8386da68f09d170",
+    "M8_N2112_K7168": (8435712, None, "08a99b7e175208b7",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1180930, None, "c8386da68f09d170",
+    "M32_N4096_K512": (1180930, None, "08a99b7e175208b7",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7934210, 270848, "c8386da68f09d170",
+    "M64_N7168_K2048": (7937280, 271104, "dcc610032c44da12",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=2,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16633900, 3679740, "c8386da68f09d170",
+    "M256_N4096_K7168": (16649728, 3679232, "dcc610032c44da12",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against
@@ -57,19 +57,24 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES_DEFAULT = 126 * 1024 * 1024
 
 
-# The GEMM kernels' translation units and everything they include (the quantize kernels live in
-# mxfp4_quant.cu and do not change a GEMM launch's traffic).
-DEVICE_SOURCES = ("mxfp4_gemm.cu", "mxfp4_gemm_resident.cu", "mma_desc.cuh", "ptx.cuh", "quant_device.cuh",
-                  "internal.h")
+# Per plan path, the translation units of the kernels one call launches and everything they
+# include: a capture stays valid while these are unchanged (the two-kernel path also launches the
+# token-block quantizer of mxfp4_quant.cu).
+KERNEL_SOURCES = {
+    1: ("mxfp4_gemm.cu", "mma_desc.cuh", "ptx.cuh", "quant_device.cuh", "internal.h"),
+    2: ("mxfp4_gemm.cu", "mxfp4_quant.cu", "mma_desc.cuh", "ptx.cuh", "quant_device.cuh", "internal.h"),
+    3: ("mxfp4_gemm_resident.cu", "mma_desc.cuh", "ptx.cuh", "quant_device.cuh", "internal.h"),
+}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the GEMM kernel's device code (its source file and the headers it includes), with
-    comments and blank lines left out so that editing a comment keeps the measured traffic."""
+def kernel_source_hash(path: int) -> str:
+    """Hash of the device code a call on plan path `path` launches (the kernels' source files and
+    the headers they include), with comments and blank lines left out so that editing a comment
+    keeps the measured traffic."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for name in DEVICE_SOURCES:
+    for name in KERNEL_SOURCES[path]:
         h.update(name.encode())
         with open(os.path.join(ROOT, "block_scaled_mxfp4_bf16_gb300", "csrc", name)) as fh:
             text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
@@ -87,7 +92,7 @@ def measured_traffic(name: str, plan: dict):
     """(GEMM bytes, quantizer bytes or None) of one launch, or None when the kernels' source or
     the plan differ from the ones captured."""
     entry = MEASURED_TRAFFIC.get(name)
-    if entry is None or entry[2] != kernel_source_hash() or entry[3] != plan_signature(plan):
+    if entry is None or entry[2] != kernel_source_hash(plan["path"]) or entry[3] != plan_signature(plan):
         return None
     return entry[0], entry[1]
 
@@ -232,24 +237,30 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
     res = {"us_per_call": 1000.0 * ms / steps, "elapsed_ms": ms, "copies": copies, "plan": plan,
            "kernels_per_call": 2 if plan["path"] == 2 else 1, "status": status,
            "timings_us_per_call": [round(1000.0 * t / steps, 3) for t in elapsed]}
-    # the same calls launched one by one from the host (no graph), for comparison
+    # the same calls launched one by one from the host (no graph, each copy's call prepared
+    # once), for comparison
     n_direct = min(steps, 2000)
+    dev_calls = [mx.prepare_gemm(As[j], packs[j], w.N, Cs[j], workspace=ws, stream=side) for j in range(copies)]
     with torch.cuda.stream(side):
         e0.record(side)
         for i in range(n_direct):
-            step(i, side)
+            dev_calls[i % copies]()
         e1.record(side)
     e1.synchronize()
     res["direct_us_per_call"] = 1000.0 * e0.elapsed_time(e1) / n_direct
     if e2e:
         # end to end through the C-ABI host-buffer call (mxfp4_gemm_host): pinned host A ->
-        # device, GEMM, C -> pinned host, all enqueued by the library
+        # device, GEMM, C -> pinned host, all enqueued by the library. A serving loop keeps its
+        # buffers, so each rotating copy's call is prepared (its tensors checked) once, outside
+        # the timed region, and each step is one call into the library.
         a_host = a_cpu.pin_memory()
         c_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
         n_e2e = max(20, min(steps, 2000))
+        host_calls = [mx.prepare_gemm_host(a_host, packs[j], w.N, c_host, As[j], Cs[j], workspace=ws, stream=side)
+                      for j in range(copies)]
 
         def step_host(j):
-            mx.mxfp4_gemm_host(a_host, packs[j], w.N, c_host, As[j], Cs[j], workspace=ws, stream=side)
+            host_calls[j]()
 
         with torch.cuda.stream(side):
             for i in range(3):
@@ -263,7 +274,8 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
         res["e2e_us_per_call"] = 1000.0 * e0.elapsed_time(e1) / n_e2e
         res["h2d_bytes"] = w.M * w.K * 2
         res["d2h_bytes"] = w.M * w.N * 2
-    del packs, As, Cs, ws, g_main, g_tail
+    del packs, As, Cs, ws, g_main, g_tail, dev_calls
+    host_calls = None
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
@@ -304,6 +316,63 @@ def bench_quantizer(mx, rows: int, K: int, steps: int, warmup: int, l2_bytes: in
     torch.cuda.empty_cache()
     return {"rows": rows, "K": K, "us_per_call": round(us, 3), "algorithmic_bytes": per_copy,
             "gbs": round(per_copy / (us * 1e-6) / 1e9, 1), "status": status}
+
+
+def bench_two_kernel_parts(mx, w, plan: dict, steps: int, warmup: int, l2_bytes: int) -> dict:
+    """The two kernels of a two-kernel plan timed apart, through the public token-block entry
+    points: `steps` back-to-back mxfp4_quantize_tokens calls of A [M, K], then `steps`
+    mxfp4_gemm_tokens calls on the blocks, each chain in a CUDA graph over enough rotating copies
+    (> 3x L2) that every call reads from HBM. The quantizer's algorithmic bytes: A's bf16 read,
+    the codes' and scales' writes."""
+    dev = torch.device("cuda")
+    a_cpu, b_cpu = workloads.make_inputs(w, seed=0)
+    bq, bs = mx.mxfp4_quantize(b_cpu.to(dev))
+    packed0 = mx.mxfp4_prepack_b(bq, bs)
+    a0 = a_cpu.to(dev)
+    mt, splits = plan["m_tile"], plan["splits"]
+    tok_bytes = mx.mxfp4_token_blocks_size(w.M, w.K, mt)
+    per_copy = packed0.numel() + a0.numel() * 2 + tok_bytes + w.M * w.N * 2
+    copies = max(2, min(512, -(-3 * l2_bytes // per_copy)))
+    As = [a0] + [a0.clone() for _ in range(copies - 1)]
+    packs = [packed0] + [packed0.clone() for _ in range(copies - 1)]
+    toks = [mx.mxfp4_quantize_tokens(As[j], mt) for j in range(copies)]
+    Cs = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    side = torch.cuda.Stream()
+
+    def quant(i):
+        j = i % copies
+        mx.mxfp4_quantize_tokens(As[j], mt, out=toks[j].data, stream=side)
+
+    def gemm(i):
+        j = i % copies
+        mx.mxfp4_gemm_tokens(toks[j], packs[j], w.N, c=Cs[j], splits=splits, stream=side)
+
+    out = {}
+    for name, fn in (("token_quantizer", quant), ("gemm_tokens", gemm)):
+        with torch.cuda.stream(side):
+            for i in range(max(warmup, copies)):
+                fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(steps):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = _events()
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(SUBMIT_COVER_CYCLES)
+            e0.record(side)
+            g.replay()
+            e1.record(side)
+        e1.synchronize()
+        out[name] = 1000.0 * e0.elapsed_time(e1) / steps
+        del g
+    out["quant_algorithmic_bytes"] = w.M * w.K * 2 + w.M * w.K // 2 + w.M * ((w.K + 31) // 32)
+    out["status"] = mx.mxfp4_device_status()
+    del As, packs, toks, Cs
+    torch.cuda.empty_cache()
+    return out
 
 
 def fp4_peak_tflops():
@@ -460,6 +529,17 @@ def main():
                                    "path": r["plan"]["path"], "splits": r["plan"]["splits"],
                                    "ctas": r["plan"]["ctas"],
                                    "status": max(r["status"], rs["status"], rw["status"])}
+            if r["plan"]["path"] == 2:
+                # the two kernels of the call apart (each chain alone, back to back)
+                parts = bench_two_kernel_parts(mx, ws_, r["plan"], STEADY_STEPS, args.warmup, l2)
+                q_gbs = parts["quant_algorithmic_bytes"] / (parts["token_quantizer"] * 1e-6) / 1e9
+                per_shape[ws_.name].update({
+                    "token_quantizer_us_per_call": round(parts["token_quantizer"], 3),
+                    "token_quantizer_algorithmic_gbs": round(q_gbs, 1),
+                    "token_quantizer_hbm_frac": round(q_gbs / peak, 4),
+                    "gemm_tokens_us_per_call": round(parts["gemm_tokens"], 3),
+                    "gemm_tokens_fp4_frac": round(ws_.flops / (parts["gemm_tokens"] * 1e-6) / 1e12 / fp4_peak, 4)})
+                per_shape[ws_.name]["status"] = max(per_shape[ws_.name]["status"], parts["status"])
 
     quantizer = None
     if not args.no_shapes:

@@ -20,6 +20,8 @@ __all__ = [
     "Mxfp4Error", "load_library", "mxfp4_quantize", "mxfp4_prepack_b_size", "mxfp4_prepack_b",
     "mxfp4_gemm_workspace_size", "mxfp4_workspace_init", "mxfp4_gemm", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
     "mxfp4_gemm_plan", "mxfp4_gemm_plan_model", "mxfp4_device_status", "mxfp4_selftest_timeout", "mxfp4_version",
+    "PreparedCall", "prepare_gemm", "prepare_gemm_host", "TokenBlocks", "mxfp4_token_tile", "mxfp4_token_blocks_size",
+    "mxfp4_quantize_tokens", "mxfp4_gemm_tokens",
 ]
 
 _LOCK = threading.Lock()
@@ -96,6 +98,14 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_device_status.restype = _int
             L.mxfp4_selftest_timeout.argtypes = [_int, _vp]
             L.mxfp4_selftest_timeout.restype = _int
+            L.mxfp4_token_tile.argtypes = [_i64, _i64, _int]
+            L.mxfp4_token_tile.restype = _int
+            L.mxfp4_token_blocks_size.argtypes = [_i64, _i64, _int]
+            L.mxfp4_token_blocks_size.restype = _sz
+            L.mxfp4_quantize_tokens.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]
+            L.mxfp4_quantize_tokens.restype = _int
+            L.mxfp4_gemm_tokens.argtypes = [_vp, _sz, _i64, _i64, _int, _vp, _i64, _vp, _i64, _int, _vp]
+            L.mxfp4_gemm_tokens.restype = _int
             _LIB = L
     return _LIB
 
@@ -193,6 +203,74 @@ def mxfp4_prepack_b(bq: torch.Tensor, bs: torch.Tensor, packed: torch.Tensor | N
     return packed
 
 
+class TokenBlocks:
+    """A quantized into the GEMM's token-block layout (mxfp4_quantize_tokens): `data` is the
+    uint8 buffer (256-byte aligned), M, K and m_tile the layout's parameters, m_tile already
+    cut to M (mxfp4_token_tile)."""
+
+    __slots__ = ("data", "M", "K", "m_tile")
+
+    def __init__(self, data: torch.Tensor, M: int, K: int, m_tile: int):
+        self.data, self.M, self.K, self.m_tile = data, M, K, m_tile
+
+
+def mxfp4_token_tile(M: int, K: int, m_tile: int = 0) -> int:
+    return int(load_library().mxfp4_token_tile(M, K, m_tile))
+
+
+def mxfp4_token_blocks_size(M: int, K: int, m_tile: int = 0) -> int:
+    return int(load_library().mxfp4_token_blocks_size(M, K, m_tile))
+
+
+def _aligned_bytes(nbytes: int, align: int, device: torch.device) -> torch.Tensor:
+    buf = torch.empty(nbytes + align, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % align
+    return buf[off:off + nbytes]
+
+
+def mxfp4_quantize_tokens(a: torch.Tensor, m_tile: int = 0, out: torch.Tensor | None = None,
+                          stream=None) -> TokenBlocks:
+    """bf16 A [M, K] (row stride may exceed K, K % 8 == 0) -> TokenBlocks for mxfp4_gemm_tokens.
+    `out`, if given, is a contiguous uint8 buffer of at least mxfp4_token_blocks_size bytes,
+    256-byte aligned, on A's device."""
+    L = load_library()
+    _dev(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    M, K = a.shape
+    mt = mxfp4_token_tile(M, K, m_tile)
+    size = mxfp4_token_blocks_size(M, K, m_tile)
+    if mt == 0 or size == 0:
+        raise ValueError(f"no token-block layout for M={M}, K={K}, m_tile={m_tile}")
+    if out is None:
+        out = _aligned_bytes(size, 256, a.device)
+    elif (out.device != a.device or out.dtype != torch.uint8 or out.nbytes < size or not out.is_contiguous()
+          or out.data_ptr() % 256):
+        raise ValueError(f"out must be a contiguous 256-byte aligned uint8 buffer of at least {size} bytes on "
+                         f"{a.device}")
+    _check(L.mxfp4_quantize_tokens(a.data_ptr(), M, K, a.stride(0), mt, out.data_ptr(), out.nbytes, _stream(stream)),
+           "mxfp4_quantize_tokens")
+    return TokenBlocks(out, M, K, mt)
+
+
+def mxfp4_gemm_tokens(tokens: TokenBlocks, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
+                      splits: int = 0, stream=None) -> torch.Tensor:
+    """C [M, N] bf16 = A . MXFP4(B)^T for A already quantized by mxfp4_quantize_tokens."""
+    L = load_library()
+    data, M, K = tokens.data, tokens.M, tokens.K
+    _dev(data, "tokens")
+    if M and N:
+        _check_packed(packed_b, N, K, data.device)
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=data.device)
+    _on(c, data.device, "c")
+    if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
+    _check(L.mxfp4_gemm_tokens(data.data_ptr(), data.nbytes, M, K, tokens.m_tile, packed_b.data_ptr(), N,
+                               c.data_ptr(), c.stride(0), splits, _stream(stream)), "mxfp4_gemm_tokens")
+    return c
+
+
 def mxfp4_gemm_workspace_size(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> int:
     return int(load_library().mxfp4_gemm_workspace_size_ex(M, N, K, _opts(path, splits, m_tile)))
 
@@ -251,10 +329,8 @@ def _workspace(device: torch.device, nbytes: int, stream, st: int) -> torch.Tens
     return ws
 
 
-def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
-               workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
-               stream=None, m_tile: int = 0) -> torch.Tensor:
-    """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b."""
+def _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile) -> tuple:
+    """(C, the checked arguments of one mxfp4_gemm_ex call in C order)."""
     L = load_library()
     _dev(a, "a")
     if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
@@ -279,16 +355,30 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = _opts(path, splits, m_tile) if (path or splits or m_tile) else None   # NULL: automatic plan
-    _check(L.mxfp4_gemm_ex(a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0),
-                           ws_ptr, ws_bytes, opts, st), "mxfp4_gemm")
+    return c, (a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0), ws_ptr, ws_bytes,
+               opts, st), workspace
+
+
+def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
+               stream=None, m_tile: int = 0) -> torch.Tensor:
+    """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b."""
+    c, args, _ = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
+    _check(load_library().mxfp4_gemm_ex(*args), "mxfp4_gemm")
     return c
 
 
-def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host: torch.Tensor,
-                    a_dev: torch.Tensor, c_dev: torch.Tensor, workspace: torch.Tensor | None = None,
-                    stream=None) -> torch.Tensor:
-    """mxfp4_gemm_host: A and C in (preferably pinned) host memory, device staging buffers a_dev
-    [M, K] and c_dev [M, N] from the caller; asynchronous on `stream`. Returns c_host."""
+def prepare_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor,
+                 workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
+                 stream=None, m_tile: int = 0) -> PreparedCall:
+    """mxfp4_gemm prepared for repeated calls on the same buffers (see PreparedCall); `c` is
+    required, the other arguments are those of mxfp4_gemm."""
+    c, args, ws = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
+    return PreparedCall(load_library().mxfp4_gemm_ex, args, "mxfp4_gemm", (a, packed_b, c, ws))
+
+
+def _host_call_args(a_host, packed_b, N, c_host, a_dev, c_dev, workspace, stream) -> tuple:
+    """The checked arguments of one mxfp4_gemm_host call, in C order."""
     L = load_library()
     # every tensor property is read once: this call sits on the per-step host path
     bf16 = torch.bfloat16
@@ -317,10 +407,47 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
         workspace = _workspace(dev, need, stream, st) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(L.mxfp4_gemm_host(a_host.data_ptr(), M, K, a_stride[0], packed_b.data_ptr(), N, c_host.data_ptr(),
-                             c_stride[0], a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st),
-           "mxfp4_gemm_host")
+    return (a_host.data_ptr(), M, K, a_stride[0], packed_b.data_ptr(), N, c_host.data_ptr(), c_stride[0],
+            a_dev.data_ptr(), c_dev.data_ptr(), ws_ptr, ws_bytes, st)
+
+
+def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host: torch.Tensor,
+                    a_dev: torch.Tensor, c_dev: torch.Tensor, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """mxfp4_gemm_host: A and C in (preferably pinned) host memory, device staging buffers a_dev
+    [M, K] and c_dev [M, N] from the caller; asynchronous on `stream`. Returns c_host."""
+    args = _host_call_args(a_host, packed_b, N, c_host, a_dev, c_dev, workspace, stream)
+    _check(load_library().mxfp4_gemm_host(*args), "mxfp4_gemm_host")
     return c_host
+
+
+class PreparedCall:
+    """A GEMM call whose buffers stay the same from one call to the next (a serving loop with
+    fixed input and output buffers): the tensors are checked once, when the call is prepared,
+    and each call passes the saved pointers and sizes straight to the C entry point. The
+    tensors are kept alive by this object; the caller must not resize or replace their storage
+    while it is in use. Calling it enqueues one call on the stream given when it was prepared
+    and raises Mxfp4Error if the library refuses it."""
+
+    __slots__ = ("_fn", "_args", "_where", "_keep")
+
+    def __init__(self, fn, args: tuple, where: str, keep: tuple):
+        self._fn, self._args, self._where, self._keep = fn, args, where, keep
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != 0:
+            raise Mxfp4Error(st, self._where)
+
+
+def prepare_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host: torch.Tensor,
+                      a_dev: torch.Tensor, c_dev: torch.Tensor, workspace: torch.Tensor | None = None,
+                      stream=None) -> PreparedCall:
+    """mxfp4_gemm_host prepared for repeated calls on the same buffers (see PreparedCall); the
+    arguments are those of mxfp4_gemm_host."""
+    args = _host_call_args(a_host, packed_b, N, c_host, a_dev, c_dev, workspace, stream)
+    keep = (a_host, packed_b, c_host, a_dev, c_dev, workspace)
+    return PreparedCall(load_library().mxfp4_gemm_host, args, "mxfp4_gemm_host", keep)
 
 
 def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,

@@ -258,20 +258,27 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
     return last;
 }
 
+// Token tile of the streaming kernel's plans (and of the public token-block layout) for M tokens
+// of depth K: the request (a multiple of 16, at most kMaxMTile) cut to M rounded up to 16, or
+// the planner's own choice when mtile_req is 0.
+static int token_tile(int64_t M, int64_t K, int mtile_req) {
+    if (mtile_req > 0) return static_cast<int>(std::min<int64_t>(cdiv(M, 16) * 16, mtile_req));
+    // 17..32 tokens with at most two 256-K steps: two 16-token tiles, twice the CTAs for a launch
+    // that is all latency (32x4096x512: 3.65 -> 3.51 us, 32x2880x512: 3.60 -> 3.53 us; 64 tokens
+    // at K = 2048 measured slower split)
+    if (M > 16 && M <= 32 && cdiv(K, kAtomK) <= 2) return 16;
+    // all of M up to 128; 128 up to M = 512 (half the A traffic and reduction per CTA of a 256
+    // tile, measured faster on 256x4096x7168); 256 beyond
+    return M <= 128 ? static_cast<int>(cdiv(M, 16) * 16) : (M <= 512 ? 128 : kMaxMTile);
+}
+
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
               GemmPlan* P, const int* cluster_caps) {
     GemmPlan p = {};
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_SHAPE;
     if (mtile_req < 0 || mtile_req > kMaxMTile || mtile_req % 16 != 0) return MXFP4_ERR_ARG;
     if (path_req == 3) return make_resident_plan(M, N, K, splits_req, mtile_req, sm_count, P, cluster_caps);
-    // Token tile: all of M up to 128; 128 up to M = 512 (half the A traffic and reduction per
-    // CTA of a 256 tile, measured faster on 256x4096x7168); 256 beyond.
-    p.m_tile = M <= 128 ? static_cast<int>(cdiv(M, 16) * 16) : (M <= 512 ? 128 : kMaxMTile);
-    // 17..32 tokens with at most two 256-K steps: two 16-token tiles, twice the CTAs for a launch
-    // that is all latency (32x4096x512: 3.65 -> 3.51 us, 32x2880x512: 3.60 -> 3.53 us; 64 tokens
-    // at K = 2048 measured slower split)
-    if (M > 16 && M <= 32 && cdiv(K, kAtomK) <= 2) p.m_tile = 16;
-    if (mtile_req > 0) p.m_tile = std::min(static_cast<int>(cdiv(M, 16) * 16), mtile_req);
+    p.m_tile = token_tile(M, K, mtile_req);
     p.nmc = (p.m_tile + 127) / 128;
     p.m_tiles = static_cast<int>(cdiv(M, p.m_tile));
     p.n_tiles = static_cast<int>(cdiv(N, kTileN));
@@ -345,6 +352,37 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     return MXFP4_ERR_SHAPE;
 }
 
+// The plan of (device, M, N, K, options) never changes within a process (it depends on the
+// device's SM count and cluster residency, both fixed), so the entry points keep the last few in
+// a small per-thread table instead of running the planner on every call (about 0.5 us of host
+// time a call on the benchmark's workloads).
+static int cached_plan(const DeviceInfo& di, int64_t M, int64_t N, int64_t K, int path_req, int splits_req,
+                       int mtile_req, GemmPlan* P) {
+    struct Entry {
+        int device, path, splits, mtile;
+        int64_t M, N, K;
+        GemmPlan plan;
+        bool used;
+    };
+    constexpr int kEntries = 16;
+    static thread_local Entry table[kEntries] = {};
+    static thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const Entry& e = table[i];
+        if (e.used && e.M == M && e.N == N && e.K == K && e.device == di.device && e.path == path_req &&
+            e.splits == splits_req && e.mtile == mtile_req) {
+            *P = e.plan;
+            return MXFP4_OK;
+        }
+    }
+    const int st = make_plan(M, N, K, path_req, splits_req, mtile_req, di.sm_count, P);
+    if (st != MXFP4_OK) return st;
+    Entry& e = table[next];
+    next = (next + 1) % kEntries;
+    e = Entry{di.device, path_req, splits_req, mtile_req, M, N, K, *P, true};
+    return MXFP4_OK;
+}
+
 static uint64_t g_wait_limit_ns = 1000000000ull;   // 1 s per bounded wait
 
 #ifdef MXFP4_TEST_HOOKS
@@ -365,8 +403,10 @@ static int check_gemm_args(const void* a, int64_t M, int64_t K, int64_t lda, con
 }
 
 // Enqueue one planned GEMM: the quantize kernel into `ws` for the two-kernel path, then the GEMM.
+// quantize_a = false: the two-kernel plan's token blocks are already in `ws` (the GEMM alone).
 static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, int64_t M, int64_t K, int64_t lda,
-                    const void* packed_b, int64_t N, void* c, int64_t ldc, uint8_t* ws, cudaStream_t s) {
+                    const void* packed_b, int64_t N, void* c, int64_t ldc, uint8_t* ws, cudaStream_t s,
+                    bool quantize_a = true) {
     if (plan.path == 3) {
         ResidentArgs r = {};
         r.a = static_cast<const uint16_t*>(a);
@@ -395,7 +435,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
         cudaError_t e = launch_gemm_resident(plan, r, s);
         return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
     }
-    if (plan.path == 2) {
+    if (plan.path == 2 && quantize_a) {
         cudaError_t e = launch_quantize_blocks(static_cast<const uint16_t*>(a), M, K, lda, ws, plan.m_tile,
                                                plan.m_tiles, plan.k_atoms, plan.a_block, s);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -484,7 +524,7 @@ const char* mxfp4_status_string(int status) {
 
 int mxfp4_last_cuda_error(void) { return t_last_cuda_error; }
 
-int mxfp4_version(void) { return 201; }
+int mxfp4_version(void) { return 202; }
 
 int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, void* scales, void* stream) {
     if (rows < 0 || K < 0) return MXFP4_ERR_ARG;
@@ -530,7 +570,8 @@ size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4
     DeviceInfo di;
     if (device_info(&di) != MXFP4_OK) return 0;
     GemmPlan plan;
-    if (make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan) != MXFP4_OK) return 0;
+    if (cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan) != MXFP4_OK)
+        return 0;
     return plan.ws_total;
 }
 
@@ -554,7 +595,7 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
+    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
     if (st != MXFP4_OK) return st;
     if (path) *path = plan.path;
     if (splits) *splits = plan.splits;
@@ -573,7 +614,7 @@ int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_optio
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
+    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
     if (st != MXFP4_OK) return st;
     fill_plan_info(plan, info);
     return MXFP4_OK;
@@ -604,7 +645,7 @@ int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* 
     st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, di.sm_count, &plan);
+    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
     if (st != MXFP4_OK) return st;
     if (plan.ws_total > 0) {
         if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
@@ -631,7 +672,7 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
     st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = make_plan(M, N, K, 0, 0, 0, di.sm_count, &plan);
+    st = cached_plan(di, M, N, K, 0, 0, 0, &plan);
     if (st != MXFP4_OK) return st;
     if (plan.ws_total > 0) {
         if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
@@ -673,6 +714,76 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
                  : cudaMemcpy2DAsync(c_host, static_cast<size_t>(ldc) * 2, c_dev, c_row, c_row,
                                      static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+}
+
+// Token-block layout of M tokens of depth K in tiles of m_tile tokens: (tiles, bytes).
+static bool token_blocks_layout(int64_t M, int64_t K, int m_tile, int* m_tile_out, size_t* bytes) {
+    if (M <= 0 || M > (int64_t(1) << 31) - 1 || K <= 0 || K % 8 != 0 || K > (int64_t(1) << 30)) return false;
+    if (m_tile < 0 || m_tile > kMaxMTile || m_tile % 16 != 0) return false;
+    const int mt = token_tile(M, K, m_tile);
+    const int64_t nmc = (mt + 127) / 128;
+    const size_t a_block = static_cast<size_t>(mt) * 128u + static_cast<size_t>(nmc) * 2u * kSfChunk;
+    *m_tile_out = mt;
+    *bytes = static_cast<size_t>(cdiv(M, mt)) * static_cast<size_t>(cdiv(K, kAtomK)) * a_block;
+    return true;
+}
+
+int mxfp4_token_tile(int64_t M, int64_t K, int m_tile) {
+    int mt = 0;
+    size_t bytes = 0;
+    return token_blocks_layout(M, K, m_tile, &mt, &bytes) ? mt : 0;
+}
+
+size_t mxfp4_token_blocks_size(int64_t M, int64_t K, int m_tile) {
+    int mt = 0;
+    size_t bytes = 0;
+    return token_blocks_layout(M, K, m_tile, &mt, &bytes) ? bytes : 0;
+}
+
+int mxfp4_quantize_tokens(const void* a, int64_t M, int64_t K, int64_t lda, int m_tile, void* blocks,
+                          size_t blocks_bytes, void* stream) {
+    if (M < 0 || K < 0 || m_tile < 0) return MXFP4_ERR_ARG;
+    if (K == 0 || K % 8 != 0) return MXFP4_ERR_SHAPE;
+    if (M == 0) return MXFP4_OK;
+    int mt = 0;
+    size_t need = 0;
+    if (m_tile > kMaxMTile || m_tile % 16 != 0) return MXFP4_ERR_ARG;
+    if (lda < K || !token_blocks_layout(M, K, m_tile, &mt, &need)) return MXFP4_ERR_SHAPE;
+    if (!a || !blocks) return MXFP4_ERR_ARG;
+    if (!aligned(a, 16) || lda % 8 != 0 || !aligned(blocks, 256)) return MXFP4_ERR_ALIGN;
+    if (blocks_bytes < need) return MXFP4_ERR_WORKSPACE;
+    DeviceInfo di;
+    int st = device_info(&di);
+    if (st != MXFP4_OK) return st;
+    const int nmc = (mt + 127) / 128;
+    const uint32_t a_block = static_cast<uint32_t>(mt) * 128u + static_cast<uint32_t>(nmc) * 2u * kSfChunk;
+    cudaError_t e = launch_quantize_blocks(static_cast<const uint16_t*>(a), M, K, lda, static_cast<uint8_t*>(blocks),
+                                           mt, static_cast<int>(cdiv(M, mt)), static_cast<int>(cdiv(K, kAtomK)),
+                                           a_block, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+}
+
+int mxfp4_gemm_tokens(const void* blocks, size_t blocks_bytes, int64_t M, int64_t K, int m_tile,
+                      const void* packed_b, int64_t N, void* c, int64_t ldc, int splits, void* stream) {
+    if (m_tile < 0 || splits < 0) return MXFP4_ERR_ARG;
+    if (m_tile > kMaxMTile || m_tile % 16 != 0) return MXFP4_ERR_ARG;
+    // the GEMM's checks, with the token blocks standing where A's rows would be checked
+    int st = check_gemm_args(blocks, M, K, K, packed_b, N, c, ldc);
+    if (st != MXFP4_OK || M == 0 || N == 0) return st;
+    int mt = 0;
+    size_t need = 0;
+    if (!token_blocks_layout(M, K, m_tile, &mt, &need)) return MXFP4_ERR_SHAPE;
+    if (!aligned(blocks, 256)) return MXFP4_ERR_ALIGN;
+    if (blocks_bytes < need) return MXFP4_ERR_WORKSPACE;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MXFP4_OK) return st;
+    GemmPlan plan;
+    st = cached_plan(di, M, N, K, 2, splits, mt, &plan);
+    if (st != MXFP4_OK) return st;
+    if (plan.path != 2 || plan.m_tile != mt || plan.ws_total != need) return MXFP4_ERR_SHAPE;   // never expected
+    return run_gemm(plan, di, nullptr, M, K, K, packed_b, N, c, ldc,
+                    static_cast<uint8_t*>(const_cast<void*>(blocks)), static_cast<cudaStream_t>(stream), false);
 }
 
 int mxfp4_device_status(void* stream) {
@@ -744,7 +855,7 @@ extern "C" int mxfp4_gemm_noalloc(const void* a, int64_t M, int64_t K, int64_t l
     if (st != MXFP4_OK) return st;
     // the automatic plan, whose scratch must fit the array
     GemmPlan plan;
-    st = make_plan(M, N, K, 0, 0, 0, di.sm_count, &plan);
+    st = cached_plan(di, M, N, K, 0, 0, 0, &plan);
     if (st != MXFP4_OK) return st;
     if (plan.ws_total > MXFP4_NOALLOC_SCRATCH_BYTES) return MXFP4_ERR_WORKSPACE;
     uint8_t* ws = nullptr;

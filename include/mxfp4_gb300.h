@@ -62,7 +62,8 @@ const char *mxfp4_status_string(int status);
  * on this host thread, 0 if none. */
 int mxfp4_last_cuda_error(void);
 
-/* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64). */
+/* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64).
+ * 2.02: token-block entry points (mxfp4_quantize_tokens, mxfp4_gemm_tokens). */
 int mxfp4_version(void);
 
 /*
@@ -207,6 +208,61 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
 int mxfp4_gemm_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const void *packed_b, int64_t N,
                     void *c_host, int64_t ldc, void *a_dev, void *c_dev, void *workspace, size_t ws_bytes,
                     void *stream);
+
+/*
+ * Token blocks: A quantized once into the layout the GEMM's tensor cores read, for callers that
+ * feed the same activation to several GEMMs or keep it between calls. The pages do this for their
+ * large-M path (submission 711914, `_run_aiter_large_m_gemm`: `_fast_mxfp4_quant` writes the e2m1
+ * codes and a pre-shuffled scale buffer once, and the GEMM takes them as they are); the GEMM's
+ * two-kernel plan uses the same layout in its workspace.
+ *
+ * Layout: the M tokens in tiles of m_tile rows, K in steps of 256; tile t, step j is one block of
+ * m_tile*128 + ceil(m_tile/128)*1024 bytes at offset (t*ceil(K/256) + j) * that size. In a block,
+ * row r's 128 code bytes (the step's 256 e2m1 values, even element in the low nibble) start at
+ * r*128, its eight 16-byte chunks stored at chunk (c ^ r%8) (the 128-byte swizzle of the MMA's
+ * shared-memory operand); then per 128 rows two 512-byte scale chunks, the scale of 1x32 block b
+ * (0..7) of row r at m_tile*128 + (r/128*2 + b/4)*512 + (r%32)*16 + (r/32%4)*4 + b%4 (in a tile
+ * of under 128 rows the scale slots of the rows it lacks are not part of the layout: never
+ * written, never read). Rows past M and K past the end hold zero codes and zero scale bytes.
+ * Codes and scales are bit-identical to mxfp4_quantize's.
+ *
+ * m_tile arguments: 0 = the tile the GEMM's two-kernel plan picks for M and K, else a multiple of
+ * 16 in [16, 256]; either way cut to M rounded up to 16 (mxfp4_token_tile returns the result).
+ * Blocks written with one (M, K, m_tile) must be read with the same.
+ */
+
+/* The token tile of the layout for (M, K, m_tile); 0 for invalid arguments (M < 1, K not a
+ * positive multiple of 8, m_tile not 0 or a multiple of 16 up to 256, or a size limit). */
+int mxfp4_token_tile(int64_t M, int64_t K, int m_tile);
+
+/* Bytes of the token blocks of M tokens of depth K; 0 for invalid arguments. */
+size_t mxfp4_token_blocks_size(int64_t M, int64_t K, int m_tile);
+
+/*
+ * mxfp4_quantize_tokens -- quantize A into token blocks (the quantization of mxfp4_quantize).
+ *   a      : bf16 [M, K], row stride lda (lda >= K, lda % 8 == 0), 16-byte aligned.
+ *   blocks : out, blocks_bytes >= mxfp4_token_blocks_size(M, K, m_tile), 256-byte aligned. Every
+ *            byte of the layout is written (padding included).
+ * M == 0 is a no-op. Ordering as mxfp4_gemm: A is read, and the blocks written, only after the
+ * work before it on `stream` has finished. MXFP4_ERR_WORKSPACE if blocks_bytes is too small.
+ */
+int mxfp4_quantize_tokens(const void *a, int64_t M, int64_t K, int64_t lda, int m_tile,
+                          void *blocks, size_t blocks_bytes, void *stream);
+
+/*
+ * mxfp4_gemm_tokens -- C = A . MXFP4(B)^T for A already in token blocks: the GEMM of the
+ * two-kernel plan alone (mxfp4_gemm with the option path = 2 runs mxfp4_quantize_tokens and then
+ * this; the results are bit-identical).
+ *   blocks   : written by mxfp4_quantize_tokens for the same M, K and m_tile; blocks_bytes its
+ *              size (checked against mxfp4_token_blocks_size); 256-byte aligned.
+ *   packed_b, N, c, ldc: as for mxfp4_gemm.
+ *   splits   : 0 = automatic, else the number of K slices per output tile (as in
+ *              mxfp4_gemm_options).
+ * No workspace is needed. Ordering as mxfp4_gemm (the blocks are read after the work before it on
+ * `stream` has finished). Errors: as mxfp4_gemm; MXFP4_ERR_WORKSPACE if blocks_bytes is too small.
+ */
+int mxfp4_gemm_tokens(const void *blocks, size_t blocks_bytes, int64_t M, int64_t K, int m_tile,
+                      const void *packed_b, int64_t N, void *c, int64_t ldc, int splits, void *stream);
 
 /* Everything the planner decided for one call. */
 typedef struct mxfp4_plan_info {

@@ -99,3 +99,34 @@ REDUCTION_CASES = [
     (33, 200, 512, 1, 2, (3, 1)),
     (40, 200, 512, 2, 2, (3, 1)),
 ]
+
+
+def expected_token_blocks(rq: np.ndarray, rs: np.ndarray, M: int, K: int, m_tile: int):
+    """Token blocks (the two-kernel path's workspace, mxfp4_quantize_tokens' output) laid out
+    from the oracle's bytes: per (token tile, 256-K step) a block of the tile's rows (row r at
+    r*128, its eight 16-byte chunks at (c ^ r%8)*16), then per 128 rows two 512-byte scale
+    chunks (row r at (r%32)*16 + ((r/32)%4)*4 + block%4).
+    Rows past M and K past the end are zero. Returns (bytes, mask of the defined bytes): the
+    scale slots of rows past the tile (a tile of < 128 rows) are not part of the layout."""
+    nmc = (m_tile + 127) // 128
+    a_block = m_tile * 128 + nmc * 1024
+    m_tiles = -(-M // m_tile)
+    k_atoms = -(-K // 256)
+    out = np.zeros((m_tiles, k_atoms, a_block), dtype=np.uint8)
+    defined = np.zeros((m_tiles, k_atoms, a_block), dtype=bool)
+    nblk = (K + 31) // 32
+    for mt in range(m_tiles):
+        for r in range(m_tile):
+            row = mt * m_tile + r
+            for j in range(k_atoms):
+                defined[mt, j, r * 128:(r + 1) * 128] = True
+                for c in range(8):
+                    sf = m_tile * 128 + ((r >> 7) * 2 + (c >> 2)) * 512 + (r % 32) * 16 + ((r >> 5) & 3) * 4 + (c & 3)
+                    defined[mt, j, sf] = True
+                    kb = j * 8 + c
+                    if row >= M or kb >= nblk:
+                        continue
+                    off = r * 128 + ((c ^ (r % 8)) * 16)
+                    out[mt, j, off:off + 16] = rq[row, kb * 16:kb * 16 + 16]
+                    out[mt, j, sf] = rs[row, kb]
+    return out.reshape(-1), defined.reshape(-1)

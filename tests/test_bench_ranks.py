@@ -44,7 +44,7 @@ def test_traffic_is_dropped_when_kernel_sources_or_plan_change(monkeypatch):
     plan = {"path": 1, "splits": 6, "m_tile": 16, "ctas": 102, "stages": 5, "issuers": 2, "reduction": 2,
             "recv_dedicated": 1}
     sig = bench.plan_signature(plan)
-    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, 45, bench.kernel_source_hash(), sig))
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, 45, bench.kernel_source_hash(1), sig))
     assert bench.measured_traffic(name, plan) == (123, 45)
     assert bench.measured_traffic(name, dict(plan, splits=5)) is None          # another launch plan
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, name, (123, 45, "0000000000000000", sig))
@@ -59,9 +59,10 @@ def test_recorded_traffic_matches_the_current_sources_and_plans():
     from block_scaled_mxfp4_bf16_gb300 import workloads
     from test_planner import CLUSTER_CAPS, SM_COUNT
     for name, (gemm, quant, h, sig) in bench.MEASURED_TRAFFIC.items():
-        assert h == bench.kernel_source_hash(), name
         w = workloads.by_name(name)
-        assert bench.plan_signature(mx.mxfp4_gemm_plan_model(w.M, w.N, w.K, SM_COUNT, CLUSTER_CAPS)) == sig, name
+        plan = mx.mxfp4_gemm_plan_model(w.M, w.N, w.K, SM_COUNT, CLUSTER_CAPS)
+        assert h == bench.kernel_source_hash(plan["path"]), name
+        assert bench.plan_signature(plan) == sig, name
         assert 0.95 * w.algorithmic_bytes - 2 * w.M * w.N <= gemm + (quant or 0) <= 1.3 * w.algorithmic_bytes, name
 
 

@@ -25,7 +25,7 @@ class _Lib:
     """The real library for size queries; compute calls are recorded and succeed."""
 
     COMPUTE = ("mxfp4_quantize", "mxfp4_prepack_b", "mxfp4_gemm_ex", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
-               "mxfp4_workspace_init")
+               "mxfp4_workspace_init", "mxfp4_quantize_tokens", "mxfp4_gemm_tokens")
 
     def __init__(self, real):
         self.real = real
@@ -176,3 +176,93 @@ def test_prepack_checks(lib):
         with pytest.raises(ValueError):
             mx.mxfp4_prepack_b(*args, stream=0)
     assert len(lib.calls) == 1
+
+
+def test_prepared_calls_pass_the_same_arguments(lib):
+    # a prepared call checks its tensors once and then passes exactly what the plain call passes
+    a, packed, N = _gemm_operands()
+    c = dev(torch.zeros(8, N, dtype=torch.bfloat16))
+    mx.mxfp4_gemm(a, packed, N, c=c, stream=0)
+    call = mx.prepare_gemm(a, packed, N, c, stream=0)
+    assert len(lib.calls) == 1                       # preparing calls nothing
+    call()
+    call()
+    assert lib.calls[1] == lib.calls[0] and lib.calls[2] == lib.calls[0]
+    M, K = 4, 512
+    _, packed, _ = _gemm_operands(M, N, K)
+    a_host = torch.zeros(M, K, dtype=torch.bfloat16)
+    c_host = torch.zeros(M, N, dtype=torch.bfloat16)
+    a_dev = dev(torch.zeros(M, K, dtype=torch.bfloat16))
+    c_dev = dev(torch.zeros(M, N, dtype=torch.bfloat16))
+    mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0)
+    host_call = mx.prepare_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0)
+    host_call()
+    assert lib.calls[3][0] == "mxfp4_gemm_host" and lib.calls[4] == lib.calls[3]
+
+
+def test_prepared_calls_check_when_prepared(lib):
+    a, packed, N = _gemm_operands()
+    with pytest.raises(ValueError):   # C on another device
+        mx.prepare_gemm(a, packed, N, _meta(8, N, dtype=torch.bfloat16), stream=0)
+    with pytest.raises(ValueError):   # packed weights too small
+        mx.prepare_gemm(a, packed[:1024], N, dev(torch.zeros(8, N, dtype=torch.bfloat16)), stream=0)
+    with pytest.raises(ValueError):   # host staging buffer where a device one belongs
+        mx.prepare_gemm_host(torch.zeros(8, 512, dtype=torch.bfloat16), packed, N,
+                             torch.zeros(8, N, dtype=torch.bfloat16), torch.zeros(8, 512, dtype=torch.bfloat16),
+                             dev(torch.zeros(8, N, dtype=torch.bfloat16)), stream=0)
+    assert lib.calls == []
+
+
+def test_prepared_call_raises_the_library_status():
+    # the status word the C entry point returns becomes the binding's exception
+    seen = []
+    call = mx.PreparedCall(lambda *args: seen.append(args) or 4, (1, 2, 3), "mxfp4_gemm", ())
+    with pytest.raises(mx.Mxfp4Error):
+        call()
+    assert seen == [(1, 2, 3)]
+    mx.PreparedCall(lambda *args: 0, (), "mxfp4_gemm", ())()
+
+
+def test_token_layout_sizes():
+    # the library's token tile and layout size against the layout's definition: tiles of m_tile
+    # rows (cut to M rounded up to 16), 256-K steps, m_tile*128 code bytes plus two 512-byte
+    # scale chunks per 128 rows
+    def size(M, K, mt):
+        return -(-M // mt) * -(-K // 256) * (mt * 128 + -(-mt // 128) * 1024)
+    for M, K, m_tile, mt in [(64, 2048, 0, 64), (256, 7168, 0, 128), (600, 512, 0, 256), (8, 7168, 0, 16),
+                             (24, 512, 0, 16), (24, 1024, 0, 32), (5, 72, 256, 16), (300, 520, 64, 64),
+                             (129, 264, 256, 144), (1, 8, 0, 16)]:
+        assert mx.mxfp4_token_tile(M, K, m_tile) == mt, (M, K, m_tile)
+        assert mx.mxfp4_token_blocks_size(M, K, m_tile) == size(M, K, mt), (M, K, m_tile)
+    for M, K, m_tile in [(0, 512, 0), (8, 100, 0), (8, 512, 24), (8, 512, 272), (8, 512, -16), (8, 0, 0)]:
+        assert mx.mxfp4_token_tile(M, K, m_tile) == 0 and mx.mxfp4_token_blocks_size(M, K, m_tile) == 0
+
+
+def test_token_calls_pass_pointers_and_check_buffers(lib):
+    M, K, N = 40, 512, 256
+    a = dev(torch.zeros(M, K + 8, dtype=torch.bfloat16))[:, :K]
+    size = mx.mxfp4_token_blocks_size(M, K, 32)
+    out = dev(torch.zeros(size + 256, dtype=torch.uint8))
+    out = out[(-out.data_ptr()) % 256:][:size]
+    tokens = mx.mxfp4_quantize_tokens(a, 32, out=out, stream=0)
+    (name, args), = lib.calls
+    assert name == "mxfp4_quantize_tokens"
+    assert args[:7] == (a.data_ptr(), M, K, K + 8, 32, out.data_ptr(), size)
+    assert tokens.data is out and (tokens.M, tokens.K, tokens.m_tile) == (M, K, 32)
+    _, packed, _ = _gemm_operands(M, N, K)
+    c = dev(torch.zeros(M, N + 4, dtype=torch.bfloat16))[:, :N]
+    mx.mxfp4_gemm_tokens(tokens, packed, N, c=c, splits=2, stream=0)
+    name, args = lib.calls[-1]
+    assert name == "mxfp4_gemm_tokens"
+    assert args[:10] == (out.data_ptr(), size, M, K, 32, packed.data_ptr(), N, c.data_ptr(), N + 4, 2)
+    with pytest.raises(ValueError):   # output buffer one byte short
+        mx.mxfp4_quantize_tokens(a, 32, out=out[:-1], stream=0)
+    with pytest.raises(ValueError):   # output buffer on another device
+        mx.mxfp4_quantize_tokens(a, 32, out=_meta(size), stream=0)
+    with pytest.raises(ValueError):   # no layout for this token tile
+        mx.mxfp4_quantize_tokens(a, 24, stream=0)
+    with pytest.raises(ValueError):   # packed weights too small
+        mx.mxfp4_gemm_tokens(tokens, packed[:1024], N, stream=0)
+    with pytest.raises(ValueError):   # C of the wrong shape
+        mx.mxfp4_gemm_tokens(tokens, packed, N, c=dev(torch.zeros(M, N - 1, dtype=torch.bfloat16)), stream=0)
+    assert len(lib.calls) == 2

@@ -346,6 +346,34 @@ def test_gemm_host_buffers_match_device_call():
     assert torch.all(c_host == 5.0)
 
 
+def test_prepared_calls_match_plain_calls():
+    # prepared calls on fixed buffers, replayed with new contents in those buffers, give the
+    # plain calls' bits every time; the host-buffer form returns C through pinned memory
+    mx = _mx()
+    M, N, K = 8, 2112, 7168
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=31).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    a_host = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
+    c_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    call = mx.prepare_gemm(a, packed, N, c)
+    host_call = mx.prepare_gemm_host(a_host, packed, N, c_host, a_dev, c_dev)
+    for seed in (1, 2, 3):
+        x = workloads.random_bf16(M, K, seed=seed)
+        a.copy_(x)
+        a_host.copy_(x)
+        call()
+        host_call()
+        torch.cuda.synchronize()
+        want = mx.mxfp4_gemm(x.cuda(), packed, N)
+        assert torch.equal(c.view(torch.int16), want.view(torch.int16)), seed
+        assert torch.equal(c_host.view(torch.int16), want.cpu().view(torch.int16)), seed
+    assert mx.mxfp4_device_status() == 0
+
+
 @pytest.mark.parametrize("M,N,K,splits,m_tile", [(600, 200, 512, 1, 0), (600, 200, 1024, 2, 0), (300, 384, 768, 1, 256)])
 def test_gemm_256_token_tiles_vs_oracle(M, N, K, splits, m_tile):
     # 256-token tiles (M > 512 by default, or forced): two 128-row scale chunks per token block,

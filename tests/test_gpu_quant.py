@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from block_scaled_mxfp4_bf16_gb300 import workloads
-from mxfp4_testlib import assert_bytes_equal, quantize_both, to_np_u8
+from mxfp4_testlib import assert_bytes_equal, expected_token_blocks, quantize_both, to_np_u8
 
 pytestmark = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden", "hand_blocks.json")
@@ -119,36 +119,6 @@ def test_quantize_rejects_bad_arguments():
     assert L.mxfp4_quantize(x.data_ptr(), 0, 64, 64, q.data_ptr(), s.data_ptr(), st) == 0    # empty no-op
 
 
-def _expected_token_blocks(rq: np.ndarray, rs: np.ndarray, M: int, K: int, m_tile: int):
-    """The two-kernel path's workspace, laid out from the oracle's bytes: per (token tile, 256-K
-    step) a block of the tile's rows (row r at r*128, its eight 16-byte chunks at (c ^ r%8)*16),
-    then per 128 rows two 512-byte scale chunks (row r at (r%32)*16 + ((r/32)%4)*4 + block%4).
-    Rows past M and K past the end are zero. Returns (bytes, mask of the defined bytes): the
-    scale slots of rows past the tile (a tile of < 128 rows) are not part of the layout."""
-    nmc = (m_tile + 127) // 128
-    a_block = m_tile * 128 + nmc * 1024
-    m_tiles = -(-M // m_tile)
-    k_atoms = -(-K // 256)
-    out = np.zeros((m_tiles, k_atoms, a_block), dtype=np.uint8)
-    defined = np.zeros((m_tiles, k_atoms, a_block), dtype=bool)
-    nblk = (K + 31) // 32
-    for mt in range(m_tiles):
-        for r in range(m_tile):
-            row = mt * m_tile + r
-            for j in range(k_atoms):
-                defined[mt, j, r * 128:(r + 1) * 128] = True
-                for c in range(8):
-                    sf = m_tile * 128 + ((r >> 7) * 2 + (c >> 2)) * 512 + (r % 32) * 16 + ((r >> 5) & 3) * 4 + (c & 3)
-                    defined[mt, j, sf] = True
-                    kb = j * 8 + c
-                    if row >= M or kb >= nblk:
-                        continue
-                    off = r * 128 + ((c ^ (r % 8)) * 16)
-                    out[mt, j, off:off + 16] = rq[row, kb * 16:kb * 16 + 16]
-                    out[mt, j, sf] = rs[row, kb]
-    return out.reshape(-1), defined.reshape(-1)
-
-
 @pytest.mark.parametrize("M,K,m_tile", [(40, 768, 0), (300, 512, 0), (33, 320, 0), (100, 1024, 64), (200, 7168, 0),
                                          (40, 776, 0), (33, 344, 0), (7, 8, 0), (200, 7176, 0)])
 def test_two_kernel_token_blocks_bit_exact(M, K, m_tile):
@@ -172,7 +142,7 @@ def test_two_kernel_token_blocks_bit_exact(M, K, m_tile):
     torch.cuda.synchronize()
     assert mx.mxfp4_device_status() == 0
     rq, rs = oracle.quantize(workloads.bf16_bits(a))
-    want, defined = _expected_token_blocks(rq, rs, M, K, plan["m_tile"])
+    want, defined = expected_token_blocks(rq, rs, M, K, plan["m_tile"])
     got = to_np_u8(ws)
     assert got.size == want.size, (got.size, want.size)
     bad = np.flatnonzero((got != want) & defined)
