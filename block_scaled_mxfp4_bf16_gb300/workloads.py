@@ -15,6 +15,7 @@ leaderboard harness itself is not available, so these stand in for its inputs):
 """
 from __future__ import annotations
 
+import re
 from dataclasses import dataclass
 
 import torch
@@ -58,10 +59,15 @@ EXTRA_WORKLOADS = [
 
 
 def by_name(name: str) -> Workload:
+    """A listed workload by name, else any shape named ``M<m>_N<n>_K<k>`` (B with sigma 1, no
+    outlier blocks), e.g. a large token count to time the compute-bound regime."""
     for w in WORKLOADS + EXTRA_WORKLOADS:
         if w.name == name:
             return w
-    raise KeyError(name)
+    m = re.fullmatch(r"M(\d+)_N(\d+)_K(\d+)", name)
+    if m is None or min(int(v) for v in m.groups()) < 1:
+        raise KeyError(name)
+    return Workload(name, int(m.group(1)), int(m.group(2)), int(m.group(3)))
 
 
 def make_inputs(w: Workload, seed: int = 0) -> tuple[torch.Tensor, torch.Tensor]:

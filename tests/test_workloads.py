@@ -49,3 +49,14 @@ def test_weight_scale_of_the_wide_shape():
     a, b = workloads.make_inputs(w, seed=0)
     assert abs(float(b.float().std()) - 0.02) < 0.001
     assert abs(float(a.float().std()) - 1.0) < 0.02
+
+
+def test_workloads_named_by_shape():
+    # any M<m>_N<n>_K<k> names a plain workload of that shape (sigma 1, no outliers); listed
+    # names keep their own recipes; anything else is unknown
+    w = workloads.by_name("M2048_N4096_K7168")
+    assert (w.M, w.N, w.K, w.b_sigma, w.outlier_blocks) == (2048, 4096, 7168, 1.0, False)
+    assert workloads.by_name("M64_N7168_K2048").b_sigma == 0.02
+    for bad in ("M0_N128_K256", "M8_N2112", "foo", "M8_N2112_K7168x"):
+        with pytest.raises(KeyError):
+            workloads.by_name(bad)
