@@ -38,15 +38,15 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2590460, None, "08a99b7e175208b7",
+    "M16_N3072_K1536": (2590976, None, "e21d41521596b8f8",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8435712, None, "08a99b7e175208b7",
-                       "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=2,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1180930, None, "08a99b7e175208b7",
+    "M8_N2112_K7168": (8435968, None, "e21d41521596b8f8",
+                       "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
+    "M32_N4096_K512": (1181696, None, "e21d41521596b8f8",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7937280, 271104, "dcc610032c44da12",
+    "M64_N7168_K2048": (7937280, 271104, "5d639cf83e8de0a3",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=2,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16649728, 3679232, "dcc610032c44da12",
+    "M256_N4096_K7168": (16637440, 3679488, "5d639cf83e8de0a3",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against

@@ -143,6 +143,7 @@ struct ResidentArgs {
     uint32_t* status;      // device error word
     int M, N, K;
     int m_tile, m_tiles, n_tiles, splits, k_atoms;
+    int issuers;           // MMA-issuing warps: 2, or 3 (16-token tiles of at least three steps)
     uint32_t a_block;      // bytes of one token block
     uint32_t off_a, off_recv, off_bar;   // shared-memory offsets from the 1 KB-aligned base
     uint32_t tmem_cols;

@@ -183,7 +183,7 @@ static int plan_resident_layout(GemmPlan& p, bool one_per_sm) {
     p.nmc = 1;
     p.a_block = static_cast<uint32_t>(p.m_tile) * 128u + 2u * kSfChunk;
     p.stages = p.atoms_max;
-    p.issuers = 2;
+    p.issuers = p.m_tile == 16 && p.atoms_max >= 3 ? 3 : 2;
     p.off_a = static_cast<uint32_t>(p.atoms_max) * kWBlock;
     p.off_araw = 0;
     p.off_recv = p.off_a + static_cast<uint32_t>(p.atoms_max) * p.a_block;
@@ -197,7 +197,7 @@ static int plan_resident_layout(GemmPlan& p, bool one_per_sm) {
     if (one_per_sm && end + 2048 < one_only) end = one_only - 2048;
     p.smem_bytes = align_up(end, 16) + 1024;      // + the 1 KB alignment of the base
     if (p.smem_bytes > kSmemLimit) return MXFP4_ERR_SHAPE;
-    const uint32_t cols = 2u * static_cast<uint32_t>(p.m_tile) + 16u * static_cast<uint32_t>(p.atoms_max);
+    const uint32_t cols = static_cast<uint32_t>(p.issuers * p.m_tile) + 16u * static_cast<uint32_t>(p.atoms_max);
     p.tmem_cols = 32;
     while (p.tmem_cols < cols) p.tmem_cols <<= 1;
     p.recv_dedicated = p.splits > 1 ? 1 : 0;
@@ -423,6 +423,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
         r.n_tiles = plan.n_tiles;
         r.splits = plan.splits;
         r.k_atoms = plan.k_atoms;
+        r.issuers = plan.issuers;
         r.a_block = plan.a_block;
         r.off_a = plan.off_a;
         r.off_recv = plan.off_recv;

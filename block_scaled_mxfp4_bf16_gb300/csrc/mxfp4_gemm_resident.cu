@@ -157,7 +157,7 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
     if (threadIdx.x == 0) {
         for (int j = 0; j < na; ++j) mbar_init(&full[j], 1);
         mbar_init(a_ready, kResQuantThreads / 32);
-        mbar_init(acc_full, 2);                       // one commit per MMA issuer
+        mbar_init(acc_full, static_cast<uint32_t>(p.issuers));   // one commit per MMA issuer
         mbar_init(red_bar, 1);
         if (S > 1 && own_rows > 0)    // (S - 1) peers x owned rows x words
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * own_rows * words) * 4u);
@@ -178,101 +178,9 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         }
     }
 
-    if (warp == 1 || warp == 2) {
-        // ------------------------------------------------ tensor memory and the MMAs (2 warps)
-        // Warp 1 allocates the columns once the previous grid has finished (so a CTA never holds
-        // columns that a CTA of the previous grid still waits for) and publishes them to warp 2
-        // and the epilogue. Lane 0 of each warp issues the MMAs of alternate 256-K steps into an
-        // accumulator of its own: one thread's tcgen05 issue chain is the limit of this phase.
-        const int issuer = warp - 1;
-        if (warp == 1) {
-            pdl_wait_prior_grid();
-            tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
-            tmem_relinquish();
-            tc_fence_before_sync();
-            named_barrier_arrive(4, 64);              // to warp 2
-            named_barrier_arrive(1, 32 + 128);        // to the epilogue
-            __syncwarp();
-        } else {
-            named_barrier(4, 64);
-        }
-        tc_fence_after_sync();
-        const uint32_t tmem_base = *tmem_slot;
-        if (lane == 0) {
-            // columns: accumulators [0, 2*m_tile), weight scales 8 per step, token scales 8 per step
-            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
-            const uint32_t t_sfw = tmem_base + 2u * static_cast<uint32_t>(p.m_tile);
-            const uint32_t t_sft = t_sfw + 8u * static_cast<uint32_t>(atoms_max);
-            const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
-            const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
-            const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
-            const uint64_t w_desc0 = desc_sw128(smem_addr(sB));
-            const uint64_t t_desc0 = desc_sw128(smem_addr(sA));
-            const uint64_t sfw_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
-            const uint64_t sft_desc0 = desc_sf(smem_addr(sA + a_rows));
-            const uint32_t w_step = kWBlock >> 4, t_step = p.a_block >> 4, chunk_step = kSfChunk >> 4;
-            bool ok = true;
-            // While A is being quantized, copy the scale factors of this issuer's weight steps
-            // that have landed; afterwards each step's MMAs go out as soon as that step is in.
-            int wsf = issuer;                         // next of this issuer's steps without scales
-            {
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_test_wait(a_ready, 0)) {
-                    if (wsf < na && mbar_test_wait(&full[wsf], 0)) {
-                        tc_fence_after_sync();
-                        const uint64_t sd = sfw_desc0 + static_cast<uint32_t>(wsf) * w_step;
-                        tc_copy_sf(t_sfw + 8u * wsf, sd);
-                        tc_copy_sf(t_sfw + 8u * wsf + 4u, sd + chunk_step);
-                        wsf += 2;
-                    } else if (global_timer_ns() - t0 > lim) {
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            if (threadIdx.x == 32) RES_PHASE(5);
-            if (ok) {
-                tc_fence_after_sync();
-#pragma unroll 1
-                for (int j = issuer; j < na; j += 2) {
-                    const uint32_t sfw = t_sfw + 8u * j, sft = t_sft + 8u * j;
-                    if (j >= wsf) {
-                        if (!mbar_wait(&full[j], 0, lim)) { ok = false; break; }
-                        tc_fence_after_sync();
-                        const uint64_t sd = sfw_desc0 + static_cast<uint32_t>(j) * w_step;
-                        tc_copy_sf(sfw, sd);
-                        tc_copy_sf(sfw + 4u, sd + chunk_step);
-                    }
-                    const uint64_t sd = sft_desc0 + static_cast<uint32_t>(j) * t_step;
-                    tc_copy_sf(sft, sd);
-                    tc_copy_sf(sft + 4u, sd + chunk_step);
-                    const uint64_t wd = w_desc0 + static_cast<uint32_t>(j) * w_step;
-                    const uint64_t td = t_desc0 + static_cast<uint32_t>(j) * t_step;
-                    // K step kk of the 256: +32 bytes in both operands (descriptor +2)
-                    mma_mxf4(t_acc, wd + 0, td + 0, idesc0, sfw, sft, j != issuer);
-                    mma_mxf4(t_acc, wd + 2, td + 2, idesc1, sfw, sft, 1);
-                    mma_mxf4(t_acc, wd + 4, td + 4, idesc0, sfw + 4u, sft + 4u, 1);
-                    mma_mxf4(t_acc, wd + 6, td + 6, idesc1, sfw + 4u, sft + 4u, 1);
-                }
-            }
-            if (!ok) res_fail(p, abort_flag);
-            tc_commit(acc_full);                      // one arrival per issuer
-            if (threadIdx.x == 32) RES_PHASE(6);
-            // never leave copies in flight into shared memory that is about to be freed
-            for (int j = issuer; j < na; j += 2) mbar_wait(&full[j], 0, lim);
-        }
-        __syncwarp();
-        if (S > 1) cluster_wait();
-        if (warp == 1) {
-            named_barrier(2, 32 + 128);               // the epilogue has read the accumulators
-            tc_fence_after_sync();
-            tmem_dealloc(tmem_base, p.tmem_cols);
-        }
-        return;
-    }
 
     // ------------------------------------------------------------ A quantization (10 warps)
-    {
+    if (warp != 1 && warp != 2) {
         const int qt = warp == 0 ? lane : static_cast<int>(threadIdx.x) - 64;
         const int nb8 = na * 8;                       // 1x32 blocks of the slice per token row
         const int items = m_valid * nb8;
@@ -305,6 +213,104 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         __syncwarp();
         if (lane == 0) mbar_arrive(a_ready);
         if (threadIdx.x == 0) RES_PHASE(4);
+    }
+    const int NI = p.issuers;
+    if (warp == 1 || warp == 2 || (warp == 3 && NI == 3)) {
+        // ------------------------------------------------ tensor memory and the MMAs (2-3 warps)
+        // Warp 1 allocates the columns once the previous grid has finished (so a CTA never holds
+        // columns that a CTA of the previous grid still waits for) and publishes them to the other
+        // issuing warps and the epilogue. Lane 0 of each issuing warp issues the MMAs of every
+        // NI-th 256-K step into an accumulator of its own: one thread's tcgen05 issue chain is the
+        // limit of this phase. Warps 1-2 issue from the start; with a third issuer, warp 3 joins
+        // once it has quantized its share of A.
+        const int issuer = warp - 1;
+        if (warp == 1) {
+            pdl_wait_prior_grid();
+            tmem_alloc(const_cast<uint32_t*>(tmem_slot), p.tmem_cols);
+            tmem_relinquish();
+            tc_fence_before_sync();
+            named_barrier_arrive(4, 64);              // to warp 2
+            if (NI == 3) named_barrier_arrive(6, 64); // to warp 3
+            named_barrier_arrive(1, 32 + 128);        // to the epilogue
+            __syncwarp();
+        } else if (warp == 2) {
+            named_barrier(4, 64);
+        } else {
+            named_barrier(6, 64);
+        }
+        tc_fence_after_sync();
+        const uint32_t tmem_base = *tmem_slot;
+        if (lane == 0) {
+            // columns: accumulators [0, NI*m_tile), weight scales 8 per step, token scales 8 per step
+            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
+            const uint32_t t_sfw = tmem_base + static_cast<uint32_t>(NI * p.m_tile);
+            const uint32_t t_sft = t_sfw + 8u * static_cast<uint32_t>(atoms_max);
+            const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
+            const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
+            const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
+            const uint64_t w_desc0 = desc_sw128(smem_addr(sB));
+            const uint64_t t_desc0 = desc_sw128(smem_addr(sA));
+            const uint64_t sfw_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
+            const uint64_t sft_desc0 = desc_sf(smem_addr(sA + a_rows));
+            const uint32_t w_step = kWBlock >> 4, t_step = p.a_block >> 4, chunk_step = kSfChunk >> 4;
+            bool ok = true;
+            // While A is being quantized, copy the scale factors of this issuer's weight steps
+            // that have landed; afterwards each step's MMAs go out as soon as that step is in.
+            int wsf = issuer;                         // next of this issuer's steps without scales
+            {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_test_wait(a_ready, 0)) {
+                    if (wsf < na && mbar_test_wait(&full[wsf], 0)) {
+                        tc_fence_after_sync();
+                        const uint64_t sd = sfw_desc0 + static_cast<uint32_t>(wsf) * w_step;
+                        tc_copy_sf(t_sfw + 8u * wsf, sd);
+                        tc_copy_sf(t_sfw + 8u * wsf + 4u, sd + chunk_step);
+                        wsf += NI;
+                    } else if (global_timer_ns() - t0 > lim) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (threadIdx.x == 32) RES_PHASE(5);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int j = issuer; j < na; j += NI) {
+                    const uint32_t sfw = t_sfw + 8u * j, sft = t_sft + 8u * j;
+                    if (j >= wsf) {
+                        if (!mbar_wait(&full[j], 0, lim)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint64_t sd = sfw_desc0 + static_cast<uint32_t>(j) * w_step;
+                        tc_copy_sf(sfw, sd);
+                        tc_copy_sf(sfw + 4u, sd + chunk_step);
+                    }
+                    const uint64_t sd = sft_desc0 + static_cast<uint32_t>(j) * t_step;
+                    tc_copy_sf(sft, sd);
+                    tc_copy_sf(sft + 4u, sd + chunk_step);
+                    const uint64_t wd = w_desc0 + static_cast<uint32_t>(j) * w_step;
+                    const uint64_t td = t_desc0 + static_cast<uint32_t>(j) * t_step;
+                    // K step kk of the 256: +32 bytes in both operands (descriptor +2)
+                    mma_mxf4(t_acc, wd + 0, td + 0, idesc0, sfw, sft, j != issuer);
+                    mma_mxf4(t_acc, wd + 2, td + 2, idesc1, sfw, sft, 1);
+                    mma_mxf4(t_acc, wd + 4, td + 4, idesc0, sfw + 4u, sft + 4u, 1);
+                    mma_mxf4(t_acc, wd + 6, td + 6, idesc1, sfw + 4u, sft + 4u, 1);
+                }
+            }
+            if (!ok) res_fail(p, abort_flag);
+            tc_commit(acc_full);                      // one arrival per issuer
+            if (threadIdx.x == 32) RES_PHASE(6);
+            // never leave copies in flight into shared memory that is about to be freed
+            for (int j = issuer; j < na; j += NI) mbar_wait(&full[j], 0, lim);
+        }
+        __syncwarp();
+        if (S > 1) cluster_wait();
+        if (warp == 1) {
+            named_barrier(2, 32 + 128);               // the epilogue has read the accumulators
+            tc_fence_after_sync();
+            tmem_dealloc(tmem_base, p.tmem_cols);
+        }
+        return;
     }
     if (warp < 4 || warp >= 8) {
         if (S > 1) cluster_wait();
@@ -352,6 +358,12 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             tmem_load_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(u[i]));
+            if (NI == 3 && na >= 3) {   // a third issuer only with 16-token tiles
+                tmem_load_16(trow + 2u * acc2, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+                tmem_load_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(u[i]));
+            }
         } else {
             tmem_load_wait();
         }
