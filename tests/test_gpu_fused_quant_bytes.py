@@ -82,6 +82,7 @@ def _signed_zero_a(M: int, K: int, seed: int) -> torch.Tensor:
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
     (8, 2112, 7168, 3, 0, 0),        # the benchmark's weight-streaming shape, automatic plan
     (16, 384, 1536, 3, 3, 16),
+    (8, 256, 2048, 3, 1, 16),        # eight steps: three MMA-issuing warps, one of them a quantizer
     (32, 256, 512, 3, 1, 16),        # two 16-token tiles
     (24, 300, 2072, 3, 4, 32),       # a 32-token tile with 24 tokens; K cuts the last step
     (5, 200, 520, 3, 2, 16),         # K cuts a 1x32 block

@@ -37,6 +37,13 @@ CASES = [
     (13, 257, 1800, 7, 16),
     (24, 130, 768, 3, 32),
     (2, 512, 4096, 8, 0),
+    # 16-token tiles of 3 to 8 steps a slice: a quantizing warp joins as the third MMA issuer
+    (7, 128, 768, 1, 16),
+    (3, 140, 1024, 1, 16),
+    (10, 384, 1288, 1, 16),
+    (6, 300, 1792, 1, 16),
+    (4, 256, 2048, 1, 16),
+    (9, 200, 3840, 2, 16),
 ]
 
 
