@@ -80,8 +80,12 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(max_stages), static_cast<size_t>(p.atoms_max),
                                                   (budget - fixed) / per_stage}));
     // two MMA issuers (one accumulator each) while their columns fit; a 256-token MMA keeps the
-    // tensor core busy from one issuer
+    // tensor core busy from one issuer. On the two-kernel path, when every step has a stage of its
+    // own (no refills), an epilogue warp (idle during the MMAs there) is a third issuer: the issue
+    // chain is then the whole MMA phase (64x7168x2048 1.32 -> 1.02 us); with refills the ring's
+    // round trip is the limit and a third issuer gained nothing (256x4096x7168).
     p.issuers = p.m_tile <= 128 ? std::min(2, p.atoms_max) : 1;
+    if (p.path == 2 && p.m_tile <= 128 && p.atoms_max >= 3 && p.stages == p.atoms_max) p.issuers = 3;
     auto sf_cols = [&]() { return static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc); };
     while (p.issuers > 1 && static_cast<uint32_t>(p.issuers * p.m_tile) + sf_cols() > 512u) --p.issuers;
     // An issuer tells a stage's fills apart only by the parity of its full barrier, so it must

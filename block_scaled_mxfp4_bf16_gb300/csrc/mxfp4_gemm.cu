@@ -67,16 +67,23 @@ __device__ __forceinline__ bool et_first_lane(int warp, int lane) { return warp 
 
 // 32 accumulator columns of this thread's lane (the second 16 only if `upper`), plus the
 // matching columns of the second accumulator `acc2` columns further when `two`.
-__device__ __forceinline__ void load_acc32(uint32_t taddr, bool upper, bool two, uint32_t acc2, uint32_t (&r)[32]) {
+__device__ __forceinline__ void load_acc32(uint32_t taddr, bool upper, int nacc, uint32_t acc2, uint32_t (&r)[32]) {
     tmem_load_16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
     if (upper) tmem_load_16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-    if (two) {
+    if (nacc >= 2) {
         uint32_t q[32];
         tmem_load_16(taddr + acc2, *reinterpret_cast<uint32_t(*)[16]>(&q[0]));
         if (upper) tmem_load_16(taddr + acc2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&q[16]));
         tmem_load_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(q[i]));
+        if (nacc >= 3) {   // the third issuer's accumulator, added last
+            tmem_load_16(taddr + 2u * acc2, *reinterpret_cast<uint32_t(*)[16]>(&q[0]));
+            if (upper) tmem_load_16(taddr + 2u * acc2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&q[16]));
+            tmem_load_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(q[i]));
+        }
     } else {
         tmem_load_wait();
     }
@@ -269,6 +276,68 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const uint8_t* asrc = p.ablk + (static_cast<size_t>(mt) * p.k_atoms + a0) * a_block;
     const uint32_t tx_bytes = kWBlock + (fused ? 0u : a_block);
     const int npro = na < stages ? na : stages;
+    // One MMA-issuing thread: the MMAs of every issuers-th 256-K step into an accumulator of its
+    // own, each step's stage released with a commit, then one commit on acc_full.
+    auto issue_mmas = [&](const int issuer) {
+        // The issue loop is kept to integer adds: a shared-memory descriptor's start-address
+        // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
+        const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
+        const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
+        const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
+        const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);      // columns per stage
+        const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
+        const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
+        const uint64_t b_desc0 = desc_sw128(smem_addr(sB));
+        const uint64_t a_desc0 = desc_sw128(smem_addr(sA));
+        const uint64_t sfb_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
+        const uint64_t sfa_desc0 = desc_sf(smem_addr(sA + a_rows));
+        const uint32_t b_step = kWBlock >> 4, a_step = a_block >> 4, chunk_step = kSfChunk >> 4;
+        const bool two_chunks = p.nmc == 2;
+        bool mok = true;
+        if (fused) mok = mbar_wait(a_full, 0, lim);
+        if (issuer == 0) MXFP4_PHASE(3);
+        tc_fence_after_sync();
+        int s = issuer;
+        uint32_t phase = 0;
+        while (s >= stages) { s -= stages; phase ^= 1u; }
+#pragma unroll 1
+        for (int j = issuer; mok && j < na; j += p.issuers) {
+            if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
+            if (j == 0) MXFP4_PHASE(4);
+            if (j == na - 1) MXFP4_PHASE(5);
+            tc_fence_after_sync();
+            const uint32_t slot = static_cast<uint32_t>(fused ? j : s);
+            const uint64_t bd = b_desc0 + static_cast<uint32_t>(s) * b_step;
+            const uint64_t ad = a_desc0 + slot * a_step;
+            const uint64_t sfbd = sfb_desc0 + static_cast<uint32_t>(s) * b_step;
+            const uint64_t sfad = sfa_desc0 + slot * a_step;
+            const uint32_t sfb_cols = t_sfb0 + static_cast<uint32_t>(s) * 8u;
+            const uint32_t sfa_cols = t_sfa0 + static_cast<uint32_t>(s) * sfa_step;
+            // scale factors: weight groups 2j, 2j+1 -> 4 columns each; token chunks likewise
+            tc_copy_sf(sfb_cols, sfbd);
+            tc_copy_sf(sfb_cols + 4u, sfbd + chunk_step);
+            if (!two_chunks) {
+                tc_copy_sf(sfa_cols, sfad);
+                tc_copy_sf(sfa_cols + 4u, sfad + chunk_step);
+            } else {   // 256 tokens: chunks (c, g) at 512 * (2c + g), columns 4 * (2g + c)
+                tc_copy_sf(sfa_cols, sfad);
+                tc_copy_sf(sfa_cols + 4u, sfad + 2 * chunk_step);
+                tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
+                tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
+            }
+            const uint32_t sfa_g1 = sfa_cols + 4u * static_cast<uint32_t>(p.nmc);
+            // K step kk of the atom: +32 bytes in both operands (descriptor +2)
+            mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != issuer);
+            mma_mxf4(t_acc, bd + 2, ad + 2, idesc1, sfb_cols, sfa_cols, 1);
+            mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
+            mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
+            tc_commit(&empty[s]);
+            s += p.issuers;
+            while (s >= stages) { s -= stages; phase ^= 1u; }
+        }
+        if (!mok) fail(p, flags);
+        tc_commit(acc_full);
+    };
     // ------------------------------------------------------------------------ set-up
     if (warp == 0) {
         // The weight ring's first stages go before the dependency wait (the weights never depend
@@ -378,66 +447,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         const int issuer = warp - 1;
         tc_fence_after_sync();
         tmem_base = *tmem_slot;
-        if (lane == 0 && issuer < p.issuers) {
-            // The issue loop is kept to integer adds: a shared-memory descriptor's start-address
-            // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
-            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
-            const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
-            const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
-            const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);      // columns per stage
-            const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
-            const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
-            const uint64_t b_desc0 = desc_sw128(smem_addr(sB));
-            const uint64_t a_desc0 = desc_sw128(smem_addr(sA));
-            const uint64_t sfb_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
-            const uint64_t sfa_desc0 = desc_sf(smem_addr(sA + a_rows));
-            const uint32_t b_step = kWBlock >> 4, a_step = a_block >> 4, chunk_step = kSfChunk >> 4;
-            const bool two_chunks = p.nmc == 2;
-            bool mok = true;
-            if (fused) mok = mbar_wait(a_full, 0, lim);
-            if (issuer == 0) MXFP4_PHASE(3);
-            tc_fence_after_sync();
-            int s = issuer;
-            uint32_t phase = 0;
-            while (s >= stages) { s -= stages; phase ^= 1u; }
-#pragma unroll 1
-            for (int j = issuer; mok && j < na; j += p.issuers) {
-                if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
-                if (j == 0) MXFP4_PHASE(4);
-                if (j == na - 1) MXFP4_PHASE(5);
-                tc_fence_after_sync();
-                const uint32_t slot = static_cast<uint32_t>(fused ? j : s);
-                const uint64_t bd = b_desc0 + static_cast<uint32_t>(s) * b_step;
-                const uint64_t ad = a_desc0 + slot * a_step;
-                const uint64_t sfbd = sfb_desc0 + static_cast<uint32_t>(s) * b_step;
-                const uint64_t sfad = sfa_desc0 + slot * a_step;
-                const uint32_t sfb_cols = t_sfb0 + static_cast<uint32_t>(s) * 8u;
-                const uint32_t sfa_cols = t_sfa0 + static_cast<uint32_t>(s) * sfa_step;
-                // scale factors: weight groups 2j, 2j+1 -> 4 columns each; token chunks likewise
-                tc_copy_sf(sfb_cols, sfbd);
-                tc_copy_sf(sfb_cols + 4u, sfbd + chunk_step);
-                if (!two_chunks) {
-                    tc_copy_sf(sfa_cols, sfad);
-                    tc_copy_sf(sfa_cols + 4u, sfad + chunk_step);
-                } else {   // 256 tokens: chunks (c, g) at 512 * (2c + g), columns 4 * (2g + c)
-                    tc_copy_sf(sfa_cols, sfad);
-                    tc_copy_sf(sfa_cols + 4u, sfad + 2 * chunk_step);
-                    tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
-                    tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
-                }
-                const uint32_t sfa_g1 = sfa_cols + 4u * static_cast<uint32_t>(p.nmc);
-                // K step kk of the atom: +32 bytes in both operands (descriptor +2)
-                mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != issuer);
-                mma_mxf4(t_acc, bd + 2, ad + 2, idesc1, sfb_cols, sfa_cols, 1);
-                mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
-                mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
-                tc_commit(&empty[s]);
-                s += p.issuers;
-                while (s >= stages) { s -= stages; phase ^= 1u; }
-            }
-            if (!mok) fail(p, flags);
-            tc_commit(acc_full);
-        }
+        if (lane == 0 && issuer < p.issuers) issue_mmas(issuer);
         __syncwarp();
         if (cluster_posts) cluster_wait();
     } else {
@@ -446,6 +456,13 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         named_barrier(1, 32 + kEpiThreads);       // the column base, published by warp 1 long ago
         tmem_base = *tmem_slot;
         if (cluster_posts) cluster_wait();         // every peer's red_bar exists (long since)
+        // A third issuer on the two-kernel path: warp 3, idle there until the accumulators are
+        // ready, takes every third step (its own accumulator), then joins the epilogue.
+        if (warp == 3 && p.issuers == 3) {
+            tc_fence_after_sync();
+            if (lane == 0) issue_mmas(2);
+            __syncwarp();
+        }
         const bool waited = mbar_wait(acc_full, 0, lim);
         tc_fence_after_sync();
         if (et == 0) MXFP4_PHASE(6);
@@ -458,7 +475,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // Accumulator D = C^T: tensor-memory lane = weight row n, column = token m. Epilogue warp w
     // reads the lanes of quadrant w % 4 and every other 32-column chunk (two warps per quadrant).
     const int half = ((warp - 3) >> 2) & 1;
-    const bool two_acc = p.issuers == 2 && na >= 2;     // the second accumulator holds data
+    const int nacc = min(p.issuers, na);             // accumulators that hold data
     const uint32_t acc2 = static_cast<uint32_t>(p.m_tile);
     const int nl = (warp & 3) * 32 + lane;
     const int n = n0 + nl;
@@ -469,7 +486,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         if (warp >= 3 && ok) {
             for (int cb = half * 32; cb < m_valid; cb += 64) {
                 uint32_t r[32];
-                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                load_acc32(trow + cb, cb + 16 < m_valid, nacc, acc2, r);
                 if (n < p.N) {
                     uint16_t* cp = p.c + static_cast<int64_t>(m0 + cb) * p.ldc + n;
                     const int cnt = min(32, m_valid - cb);
@@ -508,7 +525,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         if (warp >= 3 && ok) {
             for (int cb = half * 32; cb < m_valid; cb += 64) {
                 uint32_t r[32];
-                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                load_acc32(trow + cb, cb + 16 < m_valid, nacc, acc2, r);
                 const int cnt = min(32, m_valid - cb);
                 float* dst = sStage + cb * kTileN + nl;
 #pragma unroll
@@ -526,14 +543,19 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             tc_fence_after_sync();
             tmem_dealloc(tmem_base, p.tmem_cols);
         }
-        if (threadIdx.x == 96 && ok) {
+        if (warp == 3 && ok) {
+            // one copy per 4 rows, issued by the lanes of warp 3 side by side
             const uint32_t slot_off = smem_addr(sRecv) + static_cast<uint32_t>(split * rows_per) * kTileN * 4u;
             for (int o = 0; o < S; ++o) {
                 const int o0 = min(m_valid, o * rows_per), o1 = min(m_valid, o0 + rows_per);
                 if (o == split || o1 <= o0) continue;
-                bulk_copy_to_peer(map_to_rank(slot_off, static_cast<uint32_t>(o)), sStage + o0 * kTileN,
-                                  static_cast<uint32_t>(o1 - o0) * kTileN * 4u,
-                                  map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(o)));
+                const uint32_t dst = map_to_rank(slot_off, static_cast<uint32_t>(o));
+                const uint32_t bar = map_to_rank(smem_addr(red_bar), static_cast<uint32_t>(o));
+                for (int r = o0 + 4 * lane; r < o1; r += 128) {
+                    const int rows = min(4, o1 - r);
+                    bulk_copy_to_peer(dst + static_cast<uint32_t>(r - o0) * kTileN * 4u, sStage + r * kTileN,
+                                      static_cast<uint32_t>(rows) * kTileN * 4u, bar);
+                }
             }
         }
         // An owner whose rows did not all arrive in time skips its sum and stores (the status
@@ -622,7 +644,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                                 static_cast<uint32_t>(lm) * 4u;
                 uint32_t peer_bar = map_to_rank(bar_addr, static_cast<uint32_t>(owner));
                 uint32_t r[32];
-                load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+                load_acc32(trow + cb, cb + 16 < m_valid, nacc, acc2, r);
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     if (cb + i < m_valid) {   // rows past M in this group of 4 carry padding, never stored
@@ -699,7 +721,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             uint32_t peer = map_to_rank(recv_addr, static_cast<uint32_t>(owner)) + own_off +
                             static_cast<uint32_t>(lm) * kTileN * 4u;
             uint32_t r[32];
-            load_acc32(trow + cb, cb + 16 < m_valid, two_acc, acc2, r);
+            load_acc32(trow + cb, cb + 16 < m_valid, nacc, acc2, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 if (cb + i < m_valid) {

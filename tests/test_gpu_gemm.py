@@ -270,7 +270,7 @@ def test_plan_invariants_over_a_shape_grid():
                         continue
                     checked += 1
                     steps = -(-(-(-K // 256)) // pl["splits"])      # 256-K steps of the longest slice
-                    assert 1 <= pl["issuers"] <= (3 if pl["path"] == 3 else 2), pl
+                    assert 1 <= pl["issuers"] <= (3 if pl["path"] in (2, 3) else 2), pl
                     if steps > pl["stages"]:
                         assert pl["stages"] % pl["issuers"] == 0, (M, K, path, splits, pl)
                     t = pl["tmem_cols"]

@@ -54,7 +54,7 @@ def test_invariants_over_a_grid(mx):
                             continue
                         checked += 1
                         steps = -(-(-(-K // 256)) // p["splits"])     # 256-K steps of the longest slice
-                        assert 1 <= p["issuers"] <= (3 if p["path"] == 3 else 2) and 1 <= p["stages"] <= 8, p
+                        assert 1 <= p["issuers"] <= (3 if p["path"] in (2, 3) else 2) and 1 <= p["stages"] <= 8, p
                         if p["path"] == 3:    # the whole slice resident, two A blocks per thread at most
                             assert p["stages"] == steps and p["m_tile"] in (16, 32), p
                             # a third issuing warp only for 16-token tiles of three or more steps
@@ -62,6 +62,8 @@ def test_invariants_over_a_grid(mx):
                             assert p["issuers"] * p["m_tile"] + 16 * steps <= p["tmem_cols"], p
                             assert min(M, p["m_tile"]) * steps * 8 <= 640, (M, N, K, p)
                             assert p["smem_bytes"] <= 227 * 1024, p
+                        if p["issuers"] == 3 and p["path"] == 2:   # the lent epilogue warp: only without refills
+                            assert p["stages"] == steps and p["m_tile"] <= 128, p
                         if steps > p["stages"]:   # refilled stages: one MMA thread per stage
                             assert p["stages"] % p["issuers"] == 0, (M, N, K, path, splits, p)
                         t = p["tmem_cols"]
