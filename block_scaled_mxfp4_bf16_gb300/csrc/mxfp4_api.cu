@@ -312,6 +312,26 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
         }
         return st;
     };
+    // 129..512 tokens: 64-token tiles instead of 128 when that is still one wave of CTAs, unsplit,
+    // with every 256-K step in a stage of its own. Twice the CTAs share the 128-token MMAs' tensor
+    // time; past one wave, or with a refilled ring (long K), the 128-token plan stays faster.
+    // Same-box graph replay, 128 -> 64: 256x3072x1536 5.85 -> 5.36 us, 256x2048x1024 6.72 -> 4.60,
+    // 512x2048x2048 6.97 -> 6.73, 200x4096x512 4.48 -> 4.23, 384x2880x1024 5.50 -> 5.47; against:
+    // 160x7168x2048 (168 CTAs) 7.03 -> 9.41, 256x4096x7168 (28 steps) 11.92 -> 12.69.
+    if (path_req != 1 && splits_req == 0 && mtile_req == 0 && p.path == 2 && M > 128 && M <= 512) {
+        GemmPlan q = p;
+        q.m_tile = 64;
+        q.nmc = 1;
+        q.m_tiles = static_cast<int>(cdiv(M, q.m_tile));
+        q.a_block = static_cast<uint32_t>(q.m_tile) * 128u + 2u * kSfChunk;
+        q.raw_rows = q.m_tile;
+        q.splits = 1;
+        if (static_cast<int64_t>(q.m_tiles) * q.n_tiles <= sm_count && layout_once(q) == MXFP4_OK &&
+            q.stages == q.atoms_max) {
+            *P = q;
+            return MXFP4_OK;
+        }
+    }
     if (splits_req > 0) {
         p.splits = std::max(1, std::min({splits_req, p.k_atoms, kMaxSplits}));
         const int st = layout(p);

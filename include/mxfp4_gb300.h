@@ -226,8 +226,11 @@ int mxfp4_gemm_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const
  * written, never read). Rows past M and K past the end hold zero codes and zero scale bytes.
  * Codes and scales are bit-identical to mxfp4_quantize's.
  *
- * m_tile arguments: 0 = the tile the GEMM's two-kernel plan picks for M and K, else a multiple of
- * 16 in [16, 256]; either way cut to M rounded up to 16 (mxfp4_token_tile returns the result).
+ * m_tile arguments: 0 = a default from M and K alone (M rounded up to 16 up to 128 tokens, 128 up
+ * to 512, 256 beyond; 16 for 17..32 tokens of at most two 256-K steps), else a multiple of 16 in
+ * [16, 256]; either way cut to M rounded up to 16 (mxfp4_token_tile returns the result). The
+ * GEMM's own two-kernel plan may pick another tile (it also weighs N and the SM count: see
+ * mxfp4_gemm_plan_info).
  * Blocks written with one (M, K, m_tile) must be read with the same.
  */
 

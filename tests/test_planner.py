@@ -33,6 +33,9 @@ def plan(mx, M, N, K, **kw):
     (32, 2880, 512, 3, 1, 16),
     (24, 2112, 7168, 2, 5, 32),      # too many A blocks per thread for the resident kernel
     (1, 128, 65536, 1, 8, 16),       # slices too long for the resident kernel: fused path
+    (256, 3072, 1536, 2, 1, 64),     # 129..512 tokens: 64-token tiles while one wave, unsplit, no refill
+    (512, 2048, 2048, 2, 1, 64),
+    (160, 7168, 2048, 2, 1, 128),    # 64-token tiles would be 168 CTAs: more than one wave
 ])
 def test_workload_plans(mx, M, N, K, path, splits, m_tile):
     p = plan(mx, M, N, K)
