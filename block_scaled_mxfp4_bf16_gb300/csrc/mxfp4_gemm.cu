@@ -19,15 +19,16 @@
 //   warps 1-2 : tensor-memory allocation (warp 1) and two MMA-issuing threads (alternate 256-K
 //               steps, two accumulators): per 256-K step a thread copies the scale factors into
 //               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs.
-//   warps 3-10: the epilogue: they move the accumulator out of tensor memory. In the fused path
+//   warps 3-10: the epilogue: they move the accumulators out of tensor memory. In the fused path
 //               they first warm L2 with the CTA's A rows while the previous grid finishes and
-//               zero the staged bytes past K of a 1x32 block that K cuts.
+//               zero the staged bytes past K of a 1x32 block that K cuts. On the two-kernel path,
+//               when every step has a stage of its own, warp 3 is a third MMA issuer first.
 // In the fused path every warp first quantizes the staged slice into the token-block layout (the
 // pages' in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`): the copy
 // and MMA warps have nothing else to do until those blocks exist.
 // Reduction: each output row has an owner CTA in the cluster; the K slices send their fp32 rows
-// into the owner's shared memory -- short runs as st.async stores, long runs as one bulk copy per
-// owner, both counted on the owner's mbarrier (where neither fits, posted stores and a cluster
+// into the owner's shared memory -- short runs as st.async stores, long runs as bulk copies of
+// four rows each, both counted on the owner's mbarrier (where neither fits, posted stores and a cluster
 // barrier) -- and the owner sums them in slice order (run-to-run identical) and stores bf16 C.
 // Every wait on an mbarrier is bounded; on timeout the kernel records an error in the device
 // status word and unwinds (outputs undefined, no hang, tensor memory released).

@@ -7,16 +7,18 @@
 // slice, so the CTA asks for all of its weight blocks (the prepacked shared-memory images, one
 // bulk copy each) the moment it starts, before it waits for the previous grid: the weights
 // never depend on it. After that wait:
-//   warps 0, 2..11: each thread loads its 1x32 blocks of bf16 A straight from global memory
+//   warps 0, 3..11: each thread loads its 1x32 blocks of bf16 A straight from global memory
 //                   into registers (the addresses are computed, and the lines prefetched into
 //                   L2, before the wait), quantizes them (the pages' in-register A
 //                   quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel` with
 //                   `_mxfp4_quant_tile`) and writes the token blocks into shared memory;
-//   warp 1:         allocates tensor memory, copies each weight step's scale factors into it as
-//                   the step lands, then, once A is quantized, issues every block-scaled MMA of
-//                   the slice from one thread (tcgen05.mma kind::mxf4, D = C^T: one weight row
-//                   per lane, one token per column);
-//   warps 4..7:     read the accumulator (one lane quadrant each) and reduce the K slices: rank o
+//   warps 1, 2:     warp 1 allocates tensor memory; lane 0 of each copies its 256-K steps' weight
+//                   scale factors into it as they land, then, once A is quantized, issues those
+//                   steps' block-scaled MMAs into an accumulator of its own (tcgen05.mma
+//                   kind::mxf4, D = C^T: one weight row per lane, one token per column);
+//                   warp 3 joins as a third issuer, once it has quantized its share of A, for
+//                   16-token tiles of three or more steps;
+//   warps 4..7:     add the accumulators (one lane quadrant each) and reduce the K slices: rank o
 //                   of the cluster owns weight rows [o*R, (o+1)*R) of the tile and every CTA
 //                   sends it those rows as 16-byte st.async stores counted on the owner's
 //                   mbarrier; the owner adds the slices in rank order (run-to-run identical)
@@ -177,7 +179,6 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             bulk_load(sB + j * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[j], pol);
         }
     }
-
 
     // ------------------------------------------------------------ A quantization (10 warps)
     if (warp != 1 && warp != 2) {
