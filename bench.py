@@ -38,11 +38,11 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2590976, None, "e21d41521596b8f8",
+    "M16_N3072_K1536": (2594560, None, "b15f87ec57e72f86",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8435968, None, "e21d41521596b8f8",
+    "M8_N2112_K7168": (8439552, None, "b15f87ec57e72f86",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1181696, None, "e21d41521596b8f8",
+    "M32_N4096_K512": (1185536, None, "b15f87ec57e72f86",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
     "M64_N7168_K2048": (7941120, 271104, "8a4857ccbcd82441",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),

@@ -313,6 +313,58 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         }
         return;
     }
+    // The owner's sum over the K slices: thread t of `sum_threads` sums owned row t % own_rows,
+    // tokens 4g..4g+3 with g = t / own_rows, over the sources in rank order (consecutive threads:
+    // consecutive rows, contiguous in C). Always waited for (bounded) before leaving: peers may
+    // still be posting into this CTA. Warps 8..11, done with A, join the epilogue warps in it when
+    // the owned (row, group) pairs outnumber the epilogue's 128 threads.
+    const int G = words / 4;                          // groups of 4 tokens
+    const bool sum_helpers = S > 1 && own_rows * G > 128;
+    const int sum_threads = sum_helpers ? 256 : 128;
+    auto owner_sum = [&](const int t0, const bool ok_in) {
+        const bool got = mbar_wait_cluster(red_bar, 0, lim);
+        if (!got) res_fail(p, abort_flag);
+        if (threadIdx.x == 128) RES_PHASE(9);
+        if (got && ok_in) {
+            const float4* rv = reinterpret_cast<const float4*>(sRecv);
+            for (int t = t0; t < own_rows * G; t += sum_threads) {
+                const int g = t / own_rows;
+                const int r = t - g * own_rows;
+                const int n = n0 + own0 + r;
+                float4 acc = rv[g * R + r];
+                for (int s0 = 1; s0 < S; s0 += 8) {
+                    float4 x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (s0 + i < S) x[i] = rv[((s0 + i) * G + g) * R + r];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (s0 + i < S) {
+                            acc.x += x[i].x;
+                            acc.y += x[i].y;
+                            acc.z += x[i].z;
+                            acc.w += x[i].w;
+                        }
+                    }
+                }
+                if (n < p.N) {
+                    uint16_t* cp = p.c + static_cast<int64_t>(m0 + 4 * g) * p.ldc + n;
+                    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (4 * g + i < m_valid) *cp = __bfloat16_as_ushort(__float2bfloat16_rn(vals[i]));
+                        cp += p.ldc;
+                    }
+                }
+            }
+        }
+    };
+    if (warp >= 8 && sum_helpers) {
+        cluster_wait();
+        named_barrier(3, 256);                        // the epilogue has put this rank's own rows in place
+        if (own_rows > 0) owner_sum(128 + static_cast<int>(threadIdx.x) - 256, abort_flag[0] == 0u);
+        return;
+    }
     if (warp < 4 || warp >= 8) {
         if (S > 1) cluster_wait();
         return;
@@ -326,7 +378,6 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
     // destinations of this thread's split-K posts
     const int q = warp & 3;                           // lane quadrant this warp may read
     const int nl = q * 32 + lane;                     // weight row of the tile
-    const int G = words / 4;                          // groups of 4 tokens
     uint32_t dst = 0u, bar = 0u;
     int owner = 0;
     if (S > 1) {
@@ -406,48 +457,8 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         }
     }
     if (threadIdx.x == 128) RES_PHASE(8);
-    named_barrier(3, 128);                            // this rank's own rows are in place
-    if (own_rows > 0) {
-        // always wait (bounded) before leaving: peers may still be posting into this CTA
-        const bool got = mbar_wait_cluster(red_bar, 0, lim);
-        if (!got) res_fail(p, abort_flag);
-        if (threadIdx.x == 128) RES_PHASE(9);
-        if (got && ok) {
-            // thread t sums owned row t % own_rows, tokens 4g..4g+3 with g = t / own_rows, over
-            // the sources in rank order (consecutive threads: consecutive rows, contiguous in C)
-            const float4* rv = reinterpret_cast<const float4*>(sRecv);
-            for (int t = static_cast<int>(threadIdx.x) - 128; t < own_rows * G; t += 128) {
-                const int g = t / own_rows;
-                const int r = t - g * own_rows;
-                const int n = n0 + own0 + r;
-                float4 acc = rv[g * R + r];
-                for (int s0 = 1; s0 < S; s0 += 8) {
-                    float4 x[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (s0 + i < S) x[i] = rv[((s0 + i) * G + g) * R + r];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (s0 + i < S) {
-                            acc.x += x[i].x;
-                            acc.y += x[i].y;
-                            acc.z += x[i].z;
-                            acc.w += x[i].w;
-                        }
-                    }
-                }
-                if (n < p.N) {
-                    uint16_t* cp = p.c + static_cast<int64_t>(m0 + 4 * g) * p.ldc + n;
-                    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (4 * g + i < m_valid) *cp = __bfloat16_as_ushort(__float2bfloat16_rn(vals[i]));
-                        cp += p.ldc;
-                    }
-                }
-            }
-        }
-    }
+    named_barrier(3, sum_helpers ? 256 : 128);        // this rank's own rows are in place
+    if (own_rows > 0) owner_sum(static_cast<int>(threadIdx.x) - 128, ok);
 #ifdef MXFP4_TRACE
     if (threadIdx.x == 128) {
         trace_buffer[trace_row][11] = sm_clock();
