@@ -79,21 +79,31 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     if (fixed + per_stage > budget) return MXFP4_ERR_SHAPE;
     p.stages = static_cast<int>(std::min<size_t>({static_cast<size_t>(max_stages), static_cast<size_t>(p.atoms_max),
                                                   (budget - fixed) / per_stage}));
-    // two MMA issuers (one accumulator each) while their columns fit; a 256-token MMA keeps the
-    // tensor core busy from one issuer. On the two-kernel path, when every step has a stage of its
-    // own (no refills), an epilogue warp (idle during the MMAs there) is a third issuer: the issue
-    // chain is then the whole MMA phase (64x7168x2048 1.32 -> 1.02 us); with refills the ring's
-    // round trip is the limit and a third issuer gained nothing (256x4096x7168).
-    p.issuers = p.m_tile <= 128 ? std::min(2, p.atoms_max) : 1;
-    if (p.path == 2 && p.m_tile <= 128 && p.atoms_max >= 3 && p.stages == p.atoms_max) p.issuers = 3;
-    auto sf_cols = [&]() { return static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc); };
-    while (p.issuers > 1 && static_cast<uint32_t>(p.issuers * p.m_tile) + sf_cols() > 512u) --p.issuers;
+    // Two MMA issuers (one accumulator each, alternate steps) while their columns fit. On the
+    // two-kernel path, when every step has a stage of its own (no refills), an epilogue warp
+    // (idle during the MMAs there) is a third issuer: the issue chain is then the whole MMA phase
+    // (64x7168x2048 1.32 -> 1.02 us); with refills the ring's round trip is the limit and a third
+    // issuer gained nothing (256x4096x7168). A tile of more than 128 tokens has two issuers that
+    // each take one part of every step's tokens (the first 128, the rest), with scale columns of
+    // their own and one accumulator between them: one thread's ten tcgen05 instructions per step,
+    // not the tensor core, set the pace there.
+    const bool wide = p.m_tile > 128;
+    p.issuers = wide ? 2 : std::min(2, p.atoms_max);
+    if (p.path == 2 && !wide && p.atoms_max >= 3 && p.stages == p.atoms_max) p.issuers = 3;
+    auto halves = [&]() { return wide && p.issuers == 2; };
+    auto sf_cols = [&]() {
+        return halves() ? static_cast<uint32_t>(p.stages) * 32u : static_cast<uint32_t>(p.stages) * 8u * (1u + p.nmc);
+    };
+    auto acc_cols = [&]() { return static_cast<uint32_t>(halves() ? p.m_tile : p.issuers * p.m_tile); };
+    while (p.issuers > 1 && acc_cols() + sf_cols() > 512u) --p.issuers;
     // An issuer tells a stage's fills apart only by the parity of its full barrier, so it must
     // never wait for a stage's next fill before the previous fill of that stage has landed. That
     // holds when each stage has a single consumer (stages a multiple of the issuers, each issuer
     // taking every issuers-th step) or when no stage is refilled. Otherwise drop stages to a
     // multiple of the issuers, or issuers to a divisor of the stages.
-    if (p.atoms_max > p.stages && p.stages % p.issuers != 0) {
+    // (In halves every issuer consumes every fill, and a stage is refilled only once both
+    // have released it.)
+    if (!halves() && p.atoms_max > p.stages && p.stages % p.issuers != 0) {
         if (p.stages >= 2 * p.issuers) p.stages -= p.stages % p.issuers;
         else
             while (p.stages % p.issuers != 0) --p.issuers;
@@ -102,7 +112,7 @@ static int plan_layout(GemmPlan& p, int max_stages) {
     const int a_slots = p.path == 1 ? p.atoms_max : p.stages;
     p.off_araw = p.off_a + static_cast<uint32_t>(a_slots) * p.a_block;
     size_t end = align_up(p.off_araw + raw_bytes, 1024);
-    const uint32_t cols = static_cast<uint32_t>(p.issuers * p.m_tile) + sf_cols();
+    const uint32_t cols = acc_cols() + sf_cols();
     p.tmem_cols = 32;
     while (p.tmem_cols < cols) p.tmem_cols <<= 1;
     // CTAs of this kernel that may share an SM: as many as tensor memory holds without any

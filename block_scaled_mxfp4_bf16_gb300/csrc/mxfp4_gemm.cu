@@ -170,9 +170,10 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
     if (lane == 0) mbar_arrive(q.a_full);   // one arrival per warp
 }
 
-// kTwoKernel: an instantiation that only runs the two-kernel path (no quantizer code in it);
-// the other takes the path from its arguments.
-template <bool kTwoKernel>
+// kTwoKernel: an instantiation that only runs the two-kernel path (no quantizer code in it),
+// kWide (with it): its tiles of more than 128 tokens, two issuers sharing every step (below);
+// the other instantiation takes the path and the issue scheme from its arguments.
+template <bool kTwoKernel, bool kWide>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mxfp4_gemm_kernel(const GemmArgs p) {
     const bool fused = kTwoKernel ? false : p.fused != 0;
@@ -209,6 +210,10 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const int na = base + (split < rem ? 1 : 0);
     const int m_valid = (p.M - m0) < p.m_tile ? (p.M - m0) : p.m_tile;
     const int stages = p.stages;
+    // Tiles of more than 128 tokens with two issuers ("halves"): the first issuer takes tokens
+    // 0..127 of every step, the second the rest, each into its columns of one accumulator; both
+    // release every stage.
+    const bool halves = kTwoKernel ? kWide : (p.m_tile > 128 && p.issuers == 2);
     const uint32_t a_block = p.a_block;
     const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
     const uint64_t lim = p.wait_limit_ns;
@@ -251,7 +256,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], halves ? 2 : 1);   // halves: both issuers release every stage
         }
         mbar_init(a_full, kGemmThreads / 32);
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
@@ -278,31 +283,42 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     const uint32_t tx_bytes = kWBlock + (fused ? 0u : a_block);
     const int npro = na < stages ? na : stages;
     // One MMA-issuing thread: the MMAs of every issuers-th 256-K step into an accumulator of its
-    // own, each step's stage released with a commit, then one commit on acc_full.
+    // own (or, in halves, of every step for its tokens), each step's stage released with a
+    // commit, then one commit on acc_full.
     auto issue_mmas = [&](const int issuer) {
         // The issue loop is kept to integer adds: a shared-memory descriptor's start-address
         // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
-        const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * p.m_tile);
-        const uint32_t t_sfb0 = tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
+        const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * (halves ? 128 : p.m_tile));
+        // scale columns: per issuer in halves (weights, then its tokens), else shared per stage
+        const uint32_t t_sfb0 = halves ? tmem_base + static_cast<uint32_t>(p.m_tile + issuer * 16 * stages)
+                                       : tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
         const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
-        const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);      // columns per stage
-        const uint32_t idesc0 = idesc_mxf4(static_cast<uint32_t>(p.m_tile));
+        const uint32_t mc = halves ? 1u : static_cast<uint32_t>(p.nmc);  // token row blocks per MMA
+        const uint32_t sfa_step = 8u * mc;                                // columns per stage
+        // halves: the first issuer's MMAs take tokens 0..127, the second's the rest of the tile
+        const uint32_t n_mma = halves ? (issuer == 0 ? 128u : static_cast<uint32_t>(p.m_tile - 128))
+                                      : static_cast<uint32_t>(p.m_tile);
+        const uint32_t idesc0 = idesc_mxf4(n_mma);
         const uint32_t idesc1 = idesc0 | (2u << 29) | (2u << 4);         // scale bytes {2,3}
         const uint64_t b_desc0 = desc_sw128(smem_addr(sB));
-        const uint64_t a_desc0 = desc_sw128(smem_addr(sA));
+        // halves: token rows 128h.. start 128 rows (16 KB, a whole number of swizzle atoms) in,
+        // their scale chunks are (h, 0) and (h, 1)
+        const uint32_t half = halves ? static_cast<uint32_t>(issuer) : 0u;
+        const uint64_t a_desc0 = desc_sw128(smem_addr(sA)) + half * ((128u * 128u) >> 4);
         const uint64_t sfb_desc0 = desc_sf(smem_addr(sB + kBRowsBytes));
-        const uint64_t sfa_desc0 = desc_sf(smem_addr(sA + a_rows));
+        const uint64_t sfa_desc0 = desc_sf(smem_addr(sA + a_rows)) + half * 2u * (kSfChunk >> 4);
         const uint32_t b_step = kWBlock >> 4, a_step = a_block >> 4, chunk_step = kSfChunk >> 4;
-        const bool two_chunks = p.nmc == 2;
+        const bool two_chunks = mc == 2;
+        const int first = halves ? 0 : issuer, stride = halves ? 1 : p.issuers;
         bool mok = true;
         if (fused) mok = mbar_wait(a_full, 0, lim);
         if (issuer == 0) MXFP4_PHASE(3);
         tc_fence_after_sync();
-        int s = issuer;
+        int s = first;
         uint32_t phase = 0;
         while (s >= stages) { s -= stages; phase ^= 1u; }
 #pragma unroll 1
-        for (int j = issuer; mok && j < na; j += p.issuers) {
+        for (int j = first; mok && j < na; j += stride) {
             if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
             if (j == 0) MXFP4_PHASE(4);
             if (j == na - 1) MXFP4_PHASE(5);
@@ -326,14 +342,14 @@ mxfp4_gemm_kernel(const GemmArgs p) {
                 tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
                 tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
             }
-            const uint32_t sfa_g1 = sfa_cols + 4u * static_cast<uint32_t>(p.nmc);
+            const uint32_t sfa_g1 = sfa_cols + 4u * mc;
             // K step kk of the atom: +32 bytes in both operands (descriptor +2)
-            mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != issuer);
+            mma_mxf4(t_acc, bd + 0, ad + 0, idesc0, sfb_cols, sfa_cols, j != first);
             mma_mxf4(t_acc, bd + 2, ad + 2, idesc1, sfb_cols, sfa_cols, 1);
             mma_mxf4(t_acc, bd + 4, ad + 4, idesc0, sfb_cols + 4u, sfa_g1, 1);
             mma_mxf4(t_acc, bd + 6, ad + 6, idesc1, sfb_cols + 4u, sfa_g1, 1);
             tc_commit(&empty[s]);
-            s += p.issuers;
+            s += stride;
             while (s >= stages) { s -= stages; phase ^= 1u; }
         }
         if (!mok) fail(p, flags);
@@ -476,7 +492,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // Accumulator D = C^T: tensor-memory lane = weight row n, column = token m. Epilogue warp w
     // reads the lanes of quadrant w % 4 and every other 32-column chunk (two warps per quadrant).
     const int half = ((warp - 3) >> 2) & 1;
-    const int nacc = min(p.issuers, na);             // accumulators that hold data
+    const int nacc = halves ? 1 : min(p.issuers, na);   // accumulators that hold data
     const uint32_t acc2 = static_cast<uint32_t>(p.m_tile);
     const int nl = (warp & 3) * 32 + lane;
     const int n = n0 + nl;
@@ -798,7 +814,8 @@ static cudaError_t set_kernel_attributes() {
     if (attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        for (auto* kernel : {mxfp4_gemm_kernel<false>, mxfp4_gemm_kernel<true>}) {
+        for (auto* kernel : {mxfp4_gemm_kernel<false, false>, mxfp4_gemm_kernel<true, false>,
+                             mxfp4_gemm_kernel<true, true>}) {
             cudaFuncAttributes fa = {};
             e = cudaFuncGetAttributes(&fa, kernel);
             if (e != cudaSuccess) return e;
@@ -826,13 +843,17 @@ int max_active_clusters(int cluster_size, size_t smem_bytes) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0, m = 0;   // the same resources either way; the smaller count if they ever differ
-    if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_kernel<true>, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&m, mxfp4_gemm_kernel<false>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
+    int best = -1;   // the same resources in every instantiation; the smallest count if they ever differ
+    for (auto* kernel : {mxfp4_gemm_kernel<false, false>, mxfp4_gemm_kernel<true, false>,
+                         mxfp4_gemm_kernel<true, true>}) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        best = best < 0 || n < best ? n : best;
     }
-    return n < m ? n : m;
+    return best;
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t s) {
@@ -852,8 +873,9 @@ cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = plan.splits > 1 ? 2 : 1;
-    return args.fused ? cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<false>, args)
-                      : cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true>, args);
+    if (args.fused) return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<false, false>, args);
+    return args.m_tile > 128 && args.issuers == 2 ? cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, true>, args)
+                                                  : cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, false>, args);
 }
 
 cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

@@ -271,7 +271,8 @@ def test_plan_invariants_over_a_shape_grid():
                     checked += 1
                     steps = -(-(-(-K // 256)) // pl["splits"])      # 256-K steps of the longest slice
                     assert 1 <= pl["issuers"] <= (3 if pl["path"] in (2, 3) else 2), pl
-                    if steps > pl["stages"]:
+                    halves = pl["m_tile"] > 128 and pl["issuers"] == 2   # both issuers take every stage
+                    if steps > pl["stages"] and not halves:
                         assert pl["stages"] % pl["issuers"] == 0, (M, K, path, splits, pl)
                     t = pl["tmem_cols"]
                     assert 32 <= t <= 512 and t & (t - 1) == 0, pl
@@ -374,22 +375,31 @@ def test_prepared_calls_match_plain_calls():
     assert mx.mxfp4_device_status() == 0
 
 
-@pytest.mark.parametrize("M,N,K,splits,m_tile", [(600, 200, 512, 1, 0), (600, 200, 1024, 2, 0), (300, 384, 768, 1, 256)])
-def test_gemm_256_token_tiles_vs_oracle(M, N, K, splits, m_tile):
-    # 256-token tiles (M > 512 by default, or forced): two 128-row scale chunks per token block,
-    # four token-scale copies per step, one MMA issuer; ragged last tile
+@pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
+    (600, 200, 512, 2, 1, 0), (600, 200, 1024, 2, 2, 0), (300, 384, 768, 2, 1, 256),
+    (600, 200, 2048, 2, 1, 0),       # 8 steps over 4 stages: both issuers release every refilled stage
+    (700, 300, 3072, 2, 1, 0),       # 12 steps, three tiles, the last one ragged (188 tokens)
+    (300, 384, 1536, 2, 1, 192),     # 6 steps over 5 stages; the second issuer's MMAs take 64 tokens
+    (200, 256, 1024, 2, 2, 160),     # split-K over a 160-token tile: 32-token MMAs for the second issuer
+    (300, 256, 256, 1, 1, 256),      # the fused path with a 256-token tile
+])
+def test_gemm_wide_token_tiles_vs_oracle(M, N, K, path, splits, m_tile):
+    # Tiles of more than 128 tokens (M > 512 by default, or forced): two 128-row scale chunks per
+    # token block, and two MMA issuers, the first taking tokens 0..127 of every step, the second
+    # the rest, into one accumulator; ragged last tiles
     mx = _mx()
-    plan = mx.mxfp4_gemm_plan(M, N, K, 2, splits, m_tile)
-    assert plan["m_tile"] == 256 and plan["issuers"] == 1, plan
+    plan = mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)
+    assert plan["m_tile"] == (m_tile or 256) and plan["issuers"] == 2, plan
+    assert plan["tmem_cols"] >= plan["m_tile"] + 32 * plan["stages"], plan
     a = workloads.random_bf16(M, K, seed=M + K + 256)
     b = workloads.random_bf16(N, K, seed=N + K + 256, scale=0.5)
     bq, bs = mx.mxfp4_quantize(b.cuda())
     packed = mx.mxfp4_prepack_b(bq, bs)
-    c = mx.mxfp4_gemm(a.cuda(), packed, N, path=2, splits=splits, m_tile=m_tile)
+    c = mx.mxfp4_gemm(a.cuda(), packed, N, path=path, splits=splits, m_tile=m_tile)
     torch.cuda.synchronize()
     assert mx.mxfp4_device_status() == 0
     ref = oracle_c(a, to_np_u8(bq), to_np_u8(bs))
-    check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} splits {splits} m_tile 256")
+    check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} path {path} splits {splits} m_tile {plan['m_tile']}")
 
 
 @pytest.mark.parametrize("M,K,path,splits", [(8, 512, 1, 1), (16, 1536, 1, 3), (5, 1280, 1, 2), (13, 2048, 1, 4),

@@ -67,7 +67,10 @@ def test_invariants_over_a_grid(mx):
                             assert p["smem_bytes"] <= 227 * 1024, p
                         if p["issuers"] == 3 and p["path"] == 2:   # the lent epilogue warp: only without refills
                             assert p["stages"] == steps and p["m_tile"] <= 128, p
-                        if steps > p["stages"]:   # refilled stages: one MMA thread per stage
+                        if p["m_tile"] > 128:   # two issuers, each with part of every step's tokens
+                            assert p["issuers"] == 2, p
+                            assert p["m_tile"] + 32 * p["stages"] <= p["tmem_cols"], p
+                        elif steps > p["stages"]:   # refilled stages: one MMA thread per stage
                             assert p["stages"] % p["issuers"] == 0, (M, N, K, path, splits, p)
                         t = p["tmem_cols"]
                         assert 32 <= t <= 512 and t & (t - 1) == 0, p
