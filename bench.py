@@ -48,6 +48,14 @@ MEASURED_TRAFFIC = {
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
     "M256_N4096_K7168": (16641024, 3679488, "a89c62df1467f413",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
+    "M4_N2880_K512": (844032, None, "b15f87ec57e72f86",
+                      "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
+    "M32_N2880_K512": (872192, None, "b15f87ec57e72f86",
+                       "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
+    "M16_N2112_K7168": (8554496, None, "b15f87ec57e72f86",
+                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
+    "M256_N3072_K1536": (2796288, 795392, "a89c62df1467f413",
+                         "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against
 STEADY_STEPS = 1000                  # calls in a steady-state region
