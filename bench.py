@@ -38,23 +38,23 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2594560, None, "b15f87ec57e72f86",
+    "M16_N3072_K1536": (2594560, None, "4abfb55dc0d6dad9",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8439552, None, "b15f87ec57e72f86",
+    "M8_N2112_K7168": (8439552, None, "4abfb55dc0d6dad9",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1185536, None, "b15f87ec57e72f86",
+    "M32_N4096_K512": (1185536, None, "4abfb55dc0d6dad9",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7940864, 271616, "a89c62df1467f413",
+    "M64_N7168_K2048": (7940864, 271616, "a99a3ac1d18b2b36",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16641024, 3679488, "a89c62df1467f413",
+    "M256_N4096_K7168": (16641024, 3679488, "a99a3ac1d18b2b36",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
-    "M4_N2880_K512": (844032, None, "b15f87ec57e72f86",
+    "M4_N2880_K512": (844032, None, "4abfb55dc0d6dad9",
                       "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M32_N2880_K512": (872192, None, "b15f87ec57e72f86",
+    "M32_N2880_K512": (872192, None, "4abfb55dc0d6dad9",
                        "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M16_N2112_K7168": (8554496, None, "b15f87ec57e72f86",
+    "M16_N2112_K7168": (8554496, None, "4abfb55dc0d6dad9",
                         "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M256_N3072_K1536": (2796288, 795392, "a89c62df1467f413",
+    "M256_N3072_K1536": (2796288, 795392, "a99a3ac1d18b2b36",
                          "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against
@@ -75,19 +75,39 @@ KERNEL_SOURCES = {
 }
 
 
+def product_code_lines(text: str) -> list[str]:
+    """The lines of a CUDA source that the product build compiles: comments, blank lines and the
+    timing build's `#ifdef MXFP4_TRACE` branches (up to their `#else` or `#endif`) left out."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out, skip, depth = [], False, 0
+    for ln in (ln.split("//", 1)[0].rstrip() for ln in text.splitlines()):
+        d = ln.strip()
+        if not skip:
+            if d == "#ifdef MXFP4_TRACE":
+                skip, depth = True, 0
+            elif ln:
+                out.append(ln)
+            continue
+        if d.startswith("#if"):
+            depth += 1
+        elif d == "#endif" and depth > 0:
+            depth -= 1
+        elif depth == 0 and d in ("#else", "#endif"):
+            skip = False
+    return out
+
+
 def kernel_source_hash(path: int) -> str:
     """Hash of the device code a call on plan path `path` launches (the kernels' source files and
-    the headers they include), with comments and blank lines left out so that editing a comment
-    keeps the measured traffic."""
+    the headers they include, as the product build compiles them), so that editing a comment or
+    the timing build's stamps keeps the measured traffic."""
     import hashlib
-    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[path]:
         h.update(name.encode())
         with open(os.path.join(ROOT, "block_scaled_mxfp4_bf16_gb300", "csrc", name)) as fh:
-            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
-        code = [ln.split("//", 1)[0].rstrip() for ln in text.splitlines()]
-        h.update("\n".join(ln for ln in code if ln).encode())
+            h.update("\n".join(product_code_lines(fh.read())).encode())
     return h.hexdigest()[:16]
 
 

@@ -50,6 +50,9 @@ namespace mxfp4 {
 // other phase.
 #ifdef MXFP4_TRACE
 static __shared__ unsigned int g_trace_row;
+// Per-step stamps of the same row (SM clock): [j] when step j's stage was seen full by its MMA
+// thread, [32 + j] when the copy thread saw the stage it refills for step j released (j < 32).
+static __device__ unsigned long long ring_buffer[4096][64];
 __device__ __forceinline__ void trace_phase(int slot) {
     const unsigned int row = g_trace_row;
     if (slot == 0 || slot == 10 || slot == 13 || slot == 12) return;
@@ -320,6 +323,9 @@ mxfp4_gemm_kernel(const GemmArgs p) {
 #pragma unroll 1
         for (int j = first; mok && j < na; j += stride) {
             if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
+#ifdef MXFP4_TRACE
+            if (j < 32) ring_buffer[g_trace_row][j] = sm_clock();
+#endif
             if (j == 0) MXFP4_PHASE(4);
             if (j == na - 1) MXFP4_PHASE(5);
             tc_fence_after_sync();
@@ -443,6 +449,9 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             for (int j = npro; j < na; ++j) {
                 const int s = j % stages;
                 if (!mbar_wait(&empty[s], ((j / stages) - 1) & 1, lim)) { fail(p, flags); break; }
+#ifdef MXFP4_TRACE
+                if (j < 32) ring_buffer[g_trace_row][32 + j] = sm_clock();
+#endif
                 mbar_arrive_expect_tx(&full[s], tx_bytes);
                 bulk_load(sB + s * kWBlock, bsrc + static_cast<size_t>(j) * kWBlock, kWBlock, &full[s], pol_b);
                 if (!fused)
@@ -888,6 +897,9 @@ cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStr
 #ifdef MXFP4_TRACE
 extern "C" int mxfp4_trace_read(void* host, size_t bytes) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, mxfp4::trace_buffer, bytes));
+}
+extern "C" int mxfp4_ring_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, mxfp4::ring_buffer, bytes));
 }
 extern "C" int mxfp4_trace_clusters(int size, size_t smem) { return mxfp4::max_active_clusters(size, smem); }
 #endif

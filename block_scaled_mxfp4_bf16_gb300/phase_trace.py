@@ -10,6 +10,11 @@ clock at each phase. Phases are reported per call as the median over the call's 
 since that CTA's dependency wait returned (SM clock deltas, converted with each call's measured
 clock rate), plus the gap from the previous call's last C store to this call's median wait.
 Prints one JSON line per workload.
+
+With --steps (streaming-kernel plans), also the weight and token ring step by step: when each
+256-K step's stage was seen full by its MMA thread, when the copy thread saw the stage it
+refills for a step released (the MMAs of the step `stages` earlier complete), and the refill's
+latency from that release to the step's stage being full again.
 """
 from __future__ import annotations
 
@@ -37,7 +42,7 @@ def _library():
     path = _build.build_variant("trace", ["-DMXFP4_TRACE"])
     L = ctypes.CDLL(path)
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
-    for name in ("mxfp4_trace_read", "mxfp4_trace_read_resident"):
+    for name in ("mxfp4_trace_read", "mxfp4_trace_read_resident", "mxfp4_ring_read"):
         getattr(L, name).argtypes = [vp, ctypes.c_size_t]
         getattr(L, name).restype = ctypes.c_int
     L.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, vp]
@@ -52,7 +57,8 @@ class _Opts(ctypes.Structure):
                 ("reserved", ctypes.c_int * 5)]
 
 
-def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0, calls: int = 60) -> dict:
+def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0, calls: int = 60,
+          steps: bool = False) -> dict:
     import block_scaled_mxfp4_bf16_gb300 as mx
     L = _library()
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
@@ -92,7 +98,7 @@ def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0
     buf = np.zeros((4096, 16), dtype=np.uint64)
     read = L.mxfp4_trace_read_resident if plan["path"] == 3 else L.mxfp4_trace_read
     assert read(buf.ctypes.data, buf.nbytes) == 0
-    t = buf.astype(np.int64)
+    t = np.concatenate([buf.astype(np.int64), np.arange(4096, dtype=np.int64)[:, None]], axis=1)   # [16]: row
     t = t[(t[:, 0] > 0) & (t[:, 13] > 0)]
     grids: dict = {}
     for row in t:
@@ -117,9 +123,46 @@ def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0
         if prev_end is not None:
             agg["gap_from_previous_call"].append(float(np.median(wait_ns)) - prev_end)
         prev_end = float(np.max(rows[:, 13]))
-    return {"workload": w.name, "plan": plan, "calls": len(steady),
-            "ns_after_dependency_wait": {k: round(float(np.median(v)), 0 if k != "sm_ghz" else 3)
-                                         for k, v in agg.items() if v}}
+    out = {"workload": w.name, "plan": plan, "calls": len(steady),
+           "ns_after_dependency_wait": {k: round(float(np.median(v)), 0 if k != "sm_ghz" else 3)
+                                        for k, v in agg.items() if v}}
+    if steps and plan["path"] != 3:
+        out["ring"] = _ring(L, grids, steady, plan, w)
+    return out
+
+
+def _ring(L, grids: dict, steady: list, plan: dict, w: workloads.Workload) -> dict:
+    ring = np.zeros((4096, 64), dtype=np.uint64)
+    assert L.mxfp4_ring_read(ring.ctypes.data, ring.nbytes) == 0
+    return ring_summary(ring.astype(np.int64), grids, steady, plan, w.K)
+
+
+def ring_summary(r: np.ndarray, grids: dict, steady: list, plan: dict, K: int) -> dict:
+    """Per-step medians (ns after each CTA's dependency wait) of the ring stamps `r` [row][64] of
+    the steady calls' CTAs, whose trace rows (`grids[gid]`, 17 columns: the 16 trace slots and
+    the row index) give the clock base and rate."""
+    na = min(32, -(-(-(-K // 256)) // plan["splits"]))   # steps of the longest slice (stamped up to 32)
+    stages = plan["stages"]
+    ready: dict = {j: [] for j in range(na)}
+    released: dict = {j: [] for j in range(stages, na)}
+    latency: dict = {j: [] for j in range(stages, na)}
+    for gid in steady:
+        rows = np.array(grids[gid])
+        ghz = float(np.median((rows[:, 11] - rows[:, 10]) / np.maximum(1, rows[:, 13] - rows[:, 0])))
+        for row in rows:
+            tr = r[int(row[16])]
+            for j in range(na):
+                if tr[j] >= row[10]:   # stamped by this launch
+                    ready[j].append((tr[j] - row[2]) / ghz)
+            for j in range(stages, na):
+                if tr[32 + j] >= row[10] and tr[j] >= row[10]:
+                    released[j].append((tr[32 + j] - row[2]) / ghz)
+                    latency[j].append((tr[j] - tr[32 + j]) / ghz)
+
+    def med(d):
+        return [round(float(np.median(v))) for _, v in sorted(d.items()) if v]
+    return {"step_ready": med(ready), "refill_released_from_step": stages, "refill_released": med(released),
+            "refill_latency": med(latency)}
 
 
 def main():
@@ -128,10 +171,13 @@ def main():
     ap.add_argument("--path", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--m-tile", type=int, default=0)
+    ap.add_argument("--steps", action="store_true", help="also the ring, step by step (streaming plans)")
+    ap.add_argument("--calls", type=int, default=60)
     args = ap.parse_args()
     torch.cuda.set_device(0)
     for name in args.workload:
-        print(json.dumps(trace(workloads.by_name(name), args.path, args.splits, args.m_tile)), flush=True)
+        print(json.dumps(trace(workloads.by_name(name), args.path, args.splits, args.m_tile, args.calls,
+                               args.steps)), flush=True)
 
 
 if __name__ == "__main__":

@@ -51,6 +51,17 @@ def test_traffic_is_dropped_when_kernel_sources_or_plan_change(monkeypatch):
     assert bench.measured_traffic(name, plan) is None                          # other device code
 
 
+def test_source_hash_sees_only_the_product_build():
+    # comments, blank lines and the timing build's stamps leave the hash alone; code in the
+    # product build (including an #else branch of the timing guard) changes it
+    import bench
+    base = "int a;\n#ifdef MXFP4_TRACE\nstamp();\n#if 1\nmore();\n#endif\n#else\nnop();\n#endif\nint b;\n"
+    same = base.replace("stamp();", "stamp(); other_stamp();  // note") + "\n/* c */\n"
+    assert bench.product_code_lines(base) == bench.product_code_lines(same) == ["int a;", "nop();", "#endif", "int b;"]
+    assert bench.product_code_lines(base.replace("nop();", "op();")) != bench.product_code_lines(base)
+    assert bench.product_code_lines(base.replace("int b;", "int c;")) != bench.product_code_lines(base)
+
+
 def test_recorded_traffic_matches_the_current_sources_and_plans():
     # every recorded capture belongs to the device code in the tree and to the plan the planner
     # makes for that workload on a GB300 (152 SMs; the cluster limits of the planner tests)
