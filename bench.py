@@ -38,23 +38,23 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2594560, None, "4abfb55dc0d6dad9",
+    "M16_N3072_K1536": (2594816, None, "f8c444d4e8fd2ac8",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8439552, None, "4abfb55dc0d6dad9",
+    "M8_N2112_K7168": (8439552, None, "f8c444d4e8fd2ac8",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1185536, None, "4abfb55dc0d6dad9",
+    "M32_N4096_K512": (1185792, None, "f8c444d4e8fd2ac8",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7940864, 271616, "a99a3ac1d18b2b36",
+    "M64_N7168_K2048": (7940864, 271104, "3e9aa5eb50763ce4",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16641024, 3679488, "a99a3ac1d18b2b36",
+    "M256_N4096_K7168": (16642560, 3679488, "3e9aa5eb50763ce4",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
-    "M4_N2880_K512": (844032, None, "4abfb55dc0d6dad9",
+    "M4_N2880_K512": (844032, None, "f8c444d4e8fd2ac8",
                       "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M32_N2880_K512": (872192, None, "4abfb55dc0d6dad9",
+    "M32_N2880_K512": (871936, None, "f8c444d4e8fd2ac8",
                        "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M16_N2112_K7168": (8554496, None, "4abfb55dc0d6dad9",
+    "M16_N2112_K7168": (8554240, None, "f8c444d4e8fd2ac8",
                         "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M256_N3072_K1536": (2796288, 795392, "a99a3ac1d18b2b36",
+    "M256_N3072_K1536": (2800384, 794880, "3e9aa5eb50763ce4",
                          "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against

@@ -472,11 +472,11 @@ def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch
 
 
 _PLAN_FIELDS = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated",
-                "smem_bytes", "tmem_cols")
+                "smem_bytes", "tmem_cols", "scale_stores")
 
 
 class _PlanInfo(ctypes.Structure):
-    _fields_ = [(name, ctypes.c_int) for name in _PLAN_FIELDS] + [("reserved", ctypes.c_int * 6)]
+    _fields_ = [(name, ctypes.c_int) for name in _PLAN_FIELDS] + [("reserved", ctypes.c_int * 5)]
 
 
 def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> dict:

@@ -94,7 +94,8 @@ struct GemmPlan {
     int atoms_max;     // most atoms any split gets
     int raw_rows;      // fused path: token rows staged as bf16 (the real rows of a tile)
     int stages;
-    int issuers;       // MMA-issuing threads (1 or 2), one accumulator each
+    int issuers;       // MMA-issuing threads (1 to 3); one accumulator each, or halves of one
+    int sf_stores;     // two-kernel path: scale factors written into tensor memory by epilogue warps
     int ctas;
     uint32_t a_block;  // bytes of one token block
     // shared-memory layout (bytes from a 1 KB-aligned base): weight stages at 0, token blocks
@@ -127,6 +128,7 @@ struct GemmArgs {
     uint32_t off_stage;
     uint32_t tmem_cols;
     int fused;
+    int sf_stores;         // scale factors into tensor memory by epilogue warps (two-kernel path)
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)
     uint64_t wait_limit_ns;
 #ifdef MXFP4_TEST_HOOKS

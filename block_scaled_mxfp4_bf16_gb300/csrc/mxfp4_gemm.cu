@@ -174,11 +174,13 @@ __device__ __forceinline__ void quantize_slice(const QuantSlice& q, int qt, cons
 }
 
 // kTwoKernel: an instantiation that only runs the two-kernel path (no quantizer code in it),
-// kWide (with it): its tiles of more than 128 tokens, two issuers sharing every step (below);
+// kWide (with it): its tiles of more than 128 tokens, two issuers sharing every step (below),
+// kSfStores (with it): scale factors written into tensor memory by epilogue warps (below);
 // the other instantiation takes the path and the issue scheme from its arguments.
-template <bool kTwoKernel, bool kWide>
+template <bool kTwoKernel, bool kWide, bool kSfStores>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mxfp4_gemm_kernel(const GemmArgs p) {
+    static_assert(kTwoKernel || (!kWide && !kSfStores), "the fused path copies its own scale factors");
     const bool fused = kTwoKernel ? false : p.fused != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -193,6 +195,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     uint64_t* red_bar = a_raw + 1;                // split-K: the peers' rows have landed here
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
     volatile uint32_t* flags = tmem_slot + 1;    // [0] abort
+    uint64_t* sf_full = red_bar + 2;              // [kMaxStages] a stage's scale factors in tensor memory
 
     // The warp index broadcast from lane 0, so the compiler treats it (and the MMA operands
     // derived from it) as warp-uniform: tcgen05 instructions take their operands from uniform
@@ -217,6 +220,12 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     // 0..127 of every step, the second the rest, each into its columns of one accumulator; both
     // release every stage.
     const bool halves = kTwoKernel ? kWide : (p.m_tile > 128 && p.issuers == 2);
+    // kSfStores: epilogue warps 4..7 (one per lane quarter) write each stage's scale factors
+    // into tensor memory (tcgen05.st) and the MMA threads wait for that instead of the stage
+    // itself, so the tensor pipe runs MMAs only (no tcgen05.cp); scale columns then hold one copy
+    // per stage shared by every issuer. The planner takes it where the pipe is the limit.
+    constexpr bool sf_st = kSfStores;
+    const uint32_t sf_col0 = static_cast<uint32_t>(halves ? p.m_tile : p.issuers * p.m_tile);   // first scale column
     const uint32_t a_block = p.a_block;
     const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
     const uint64_t lim = p.wait_limit_ns;
@@ -265,6 +274,8 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         mbar_init(acc_full, static_cast<uint32_t>(p.issuers));
         mbar_init(a_raw, 1 + kEpiWarps);   // the copy thread + the epilogue warps (tail zeroing)
         mbar_init(red_bar, 1);
+        if (sf_st)
+            for (int s = 0; s < stages; ++s) mbar_init(&sf_full[s], 4);   // one arrival per writing warp
         if (S > 1 && p.red_bulk && r1 > r0)   // (S - 1) peers x owned rows x 512 bytes
             mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * (r1 - r0)) * kTileN * 4u);
         else if (S > 1 && vec && r1 > r0)     // (S - 1) peers x 128 weight rows x 16 bytes per 4 rows
@@ -293,11 +304,15 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         // field (bits 0..13, address / 16) moves by (bytes / 16) from one buffer to the next.
         const uint32_t t_acc = tmem_base + static_cast<uint32_t>(issuer * (halves ? 128 : p.m_tile));
         // scale columns: per issuer in halves (weights, then its tokens), else shared per stage
-        const uint32_t t_sfb0 = halves ? tmem_base + static_cast<uint32_t>(p.m_tile + issuer * 16 * stages)
-                                       : tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
+        const uint32_t t_sfb0 = sf_st ? tmem_base + sf_col0
+                                : halves ? tmem_base + static_cast<uint32_t>(p.m_tile + issuer * 16 * stages)
+                                         : tmem_base + static_cast<uint32_t>(p.issuers * p.m_tile);
         const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
-        const uint32_t mc = halves ? 1u : static_cast<uint32_t>(p.nmc);  // token row blocks per MMA
+        const uint32_t mc = halves && !sf_st ? 1u : static_cast<uint32_t>(p.nmc);  // token row blocks per copy
         const uint32_t sfa_step = 8u * mc;                                // columns per stage
+        // shared scale columns (sf_st): a token row block's 4 columns sit at 4 * block, so the
+        // second issuer of halves starts 4 columns in (its K groups 8 columns apart, as for N = 256)
+        const uint32_t tok_col = sf_st && halves ? 4u * static_cast<uint32_t>(issuer) : 0u;
         // halves: the first issuer's MMAs take tokens 0..127, the second's the rest of the tile
         const uint32_t n_mma = halves ? (issuer == 0 ? 128u : static_cast<uint32_t>(p.m_tile - 128))
                                       : static_cast<uint32_t>(p.m_tile);
@@ -322,7 +337,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         while (s >= stages) { s -= stages; phase ^= 1u; }
 #pragma unroll 1
         for (int j = first; mok && j < na; j += stride) {
-            if (!mbar_wait(&full[s], phase, lim)) { mok = false; break; }
+            if (!mbar_wait(sf_st ? &sf_full[s] : &full[s], phase, lim)) { mok = false; break; }
 #ifdef MXFP4_TRACE
             if (j < 32) ring_buffer[g_trace_row][j] = sm_clock();
 #endif
@@ -335,18 +350,20 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             const uint64_t sfbd = sfb_desc0 + static_cast<uint32_t>(s) * b_step;
             const uint64_t sfad = sfa_desc0 + slot * a_step;
             const uint32_t sfb_cols = t_sfb0 + static_cast<uint32_t>(s) * 8u;
-            const uint32_t sfa_cols = t_sfa0 + static_cast<uint32_t>(s) * sfa_step;
+            const uint32_t sfa_cols = t_sfa0 + static_cast<uint32_t>(s) * sfa_step + tok_col;
             // scale factors: weight groups 2j, 2j+1 -> 4 columns each; token chunks likewise
-            tc_copy_sf(sfb_cols, sfbd);
-            tc_copy_sf(sfb_cols + 4u, sfbd + chunk_step);
-            if (!two_chunks) {
-                tc_copy_sf(sfa_cols, sfad);
-                tc_copy_sf(sfa_cols + 4u, sfad + chunk_step);
-            } else {   // 256 tokens: chunks (c, g) at 512 * (2c + g), columns 4 * (2g + c)
-                tc_copy_sf(sfa_cols, sfad);
-                tc_copy_sf(sfa_cols + 4u, sfad + 2 * chunk_step);
-                tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
-                tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
+            if (!sf_st) {
+                tc_copy_sf(sfb_cols, sfbd);
+                tc_copy_sf(sfb_cols + 4u, sfbd + chunk_step);
+                if (!two_chunks) {
+                    tc_copy_sf(sfa_cols, sfad);
+                    tc_copy_sf(sfa_cols + 4u, sfad + chunk_step);
+                } else {   // 256 tokens: chunks (c, g) at 512 * (2c + g), columns 4 * (2g + c)
+                    tc_copy_sf(sfa_cols, sfad);
+                    tc_copy_sf(sfa_cols + 4u, sfad + 2 * chunk_step);
+                    tc_copy_sf(sfa_cols + 8u, sfad + chunk_step);
+                    tc_copy_sf(sfa_cols + 12u, sfad + 3 * chunk_step);
+                }
             }
             const uint32_t sfa_g1 = sfa_cols + 4u * mc;
             // K step kk of the atom: +32 bytes in both operands (descriptor +2)
@@ -488,6 +505,46 @@ mxfp4_gemm_kernel(const GemmArgs p) {
             tc_fence_after_sync();
             if (lane == 0) issue_mmas(2);
             __syncwarp();
+        }
+        if (sf_st && warp >= 4 && warp < 8) {
+            // Each stage's scale factors into its columns, every lane quarter the same words (what
+            // a 32x128b.warpx4 copy writes): lane r of a 512-byte chunk holds the 4 K blocks of
+            // rows r, 32 + r, 64 + r, 96 + r, one column each. Weights: 2 chunks -> 8 columns;
+            // tokens: 2 chunks, or 4 for 256-token tiles ((c, g) at 512 * (2c + g) -> columns
+            // 4 * (2g + c)).
+            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t t_sfb0 = tmem_base + lane_base + sf_col0;
+            const uint32_t t_sfa0 = t_sfb0 + static_cast<uint32_t>(stages) * 8u;
+            const uint32_t sfa_step = 8u * static_cast<uint32_t>(p.nmc);
+            int s = 0;
+            uint32_t phase = 0;
+#pragma unroll 1
+            for (int j = 0; j < na; ++j) {
+                if (!mbar_wait(&full[s], phase, lim)) { fail(p, flags); break; }
+                const uint8_t* wsf = sB + s * kWBlock + kBRowsBytes + lane * 16;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(wsf);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(wsf + kSfChunk);
+                const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                tmem_store_8(t_sfb0 + static_cast<uint32_t>(s) * 8u, wv);
+                const uint8_t* tsf = sA + s * a_block + a_rows + lane * 16;
+                const uint4 t0 = *reinterpret_cast<const uint4*>(tsf);
+                const uint4 t1 = *reinterpret_cast<const uint4*>(tsf + kSfChunk);
+                if (p.nmc == 1) {
+                    const uint32_t tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                    tmem_store_8(t_sfa0 + static_cast<uint32_t>(s) * sfa_step, tv);
+                } else {
+                    const uint4 t2 = *reinterpret_cast<const uint4*>(tsf + 2 * kSfChunk);
+                    const uint4 t3 = *reinterpret_cast<const uint4*>(tsf + 3 * kSfChunk);
+                    const uint32_t tv[16] = {t0.x, t0.y, t0.z, t0.w, t2.x, t2.y, t2.z, t2.w,
+                                             t1.x, t1.y, t1.z, t1.w, t3.x, t3.y, t3.z, t3.w};
+                    tmem_store_16(t_sfa0 + static_cast<uint32_t>(s) * sfa_step, tv);
+                }
+                tmem_store_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[s]);
+                if (++s == stages) { s = 0; phase ^= 1u; }
+            }
         }
         const bool waited = mbar_wait(acc_full, 0, lim);
         tc_fence_after_sync();
@@ -823,8 +880,8 @@ static cudaError_t set_kernel_attributes() {
     if (attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        for (auto* kernel : {mxfp4_gemm_kernel<false, false>, mxfp4_gemm_kernel<true, false>,
-                             mxfp4_gemm_kernel<true, true>}) {
+        for (auto* kernel : {mxfp4_gemm_kernel<false, false, false>, mxfp4_gemm_kernel<true, false, false>,
+                             mxfp4_gemm_kernel<true, false, true>, mxfp4_gemm_kernel<true, true, true>}) {
             cudaFuncAttributes fa = {};
             e = cudaFuncGetAttributes(&fa, kernel);
             if (e != cudaSuccess) return e;
@@ -853,8 +910,8 @@ int max_active_clusters(int cluster_size, size_t smem_bytes) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int best = -1;   // the same resources in every instantiation; the smallest count if they ever differ
-    for (auto* kernel : {mxfp4_gemm_kernel<false, false>, mxfp4_gemm_kernel<true, false>,
-                         mxfp4_gemm_kernel<true, true>}) {
+    for (auto* kernel : {mxfp4_gemm_kernel<false, false, false>, mxfp4_gemm_kernel<true, false, false>,
+                         mxfp4_gemm_kernel<true, false, true>, mxfp4_gemm_kernel<true, true, true>}) {
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
             cudaGetLastError();
@@ -882,9 +939,10 @@ cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, cudaStream_t
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = plan.splits > 1 ? 2 : 1;
-    if (args.fused) return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<false, false>, args);
-    return args.m_tile > 128 && args.issuers == 2 ? cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, true>, args)
-                                                  : cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, false>, args);
+    if (args.fused) return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<false, false, false>, args);
+    if (args.m_tile > 128 && args.issuers == 2) return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, true, true>, args);
+    return args.sf_stores ? cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, false, true>, args)
+                          : cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<true, false, false>, args);
 }
 
 cudaError_t launch_timeout_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

@@ -282,7 +282,9 @@ typedef struct mxfp4_plan_info {
                             the pipeline buffers (one more cluster barrier before the posts) */
     int smem_bytes;      /* dynamic shared memory per CTA */
     int tmem_cols;       /* tensor-memory columns allocated per CTA */
-    int reserved[6];
+    int scale_stores;    /* 1: epilogue warps write each stage's scale factors into tensor memory
+                            (the tensor pipe then runs MMAs only); 0: the MMA threads copy them */
+    int reserved[5];
 } mxfp4_plan_info;
 
 /* The full plan mxfp4_gemm_ex would run on the current device (superset of mxfp4_gemm_plan).

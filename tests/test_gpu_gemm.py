@@ -375,6 +375,31 @@ def test_prepared_calls_match_plain_calls():
     assert mx.mxfp4_device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,path,splits,m_tile,stores", [
+    (200, 384, 4096, 2, 1, 128, 1),   # 16 steps over 6 stages: refilled, scale factors stored by warps
+    (100, 300, 5128, 2, 2, 64, 1),    # split-K, K tail, ragged weight tile, 11 steps over 8 stages
+    (40, 256, 12288, 2, 3, 48, 1),    # three slices of 16 steps, 48-token tiles
+    (40, 256, 2304, 2, 3, 48, 0),     # three steps per slice, a stage each: the MMA threads copy them
+    (64, 256, 2048, 2, 1, 64, 0),     # the same unsplit, three issuers
+])
+def test_gemm_scale_factor_stores_vs_oracle(M, N, K, path, splits, m_tile, stores):
+    # On the two-kernel path with a refilling ring, epilogue warps 4..7 write each stage's weight
+    # and token scale factors into tensor memory (one lane quarter each) instead of the MMA
+    # threads copying them; both forms against the oracle
+    mx = _mx()
+    plan = mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)
+    assert plan["scale_stores"] == stores and plan["m_tile"] == m_tile, plan
+    a = workloads.random_bf16(M, K, seed=M + K + 7)
+    b = workloads.random_bf16(N, K, seed=N + K + 7, scale=0.5)
+    bq, bs = mx.mxfp4_quantize(b.cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    c = mx.mxfp4_gemm(a.cuda(), packed, N, path=path, splits=splits, m_tile=m_tile)
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0
+    ref = oracle_c(a, to_np_u8(bq), to_np_u8(bs))
+    check_tolerance(bf16_to_f64(c.cpu()), ref, f"{M}x{N}x{K} splits {splits} m_tile {m_tile} stores {stores}")
+
+
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
     (600, 200, 512, 2, 1, 0), (600, 200, 1024, 2, 2, 0), (300, 384, 768, 2, 1, 256),
     (600, 200, 2048, 2, 1, 0),       # 8 steps over 4 stages: both issuers release every refilled stage
@@ -390,6 +415,7 @@ def test_gemm_wide_token_tiles_vs_oracle(M, N, K, path, splits, m_tile):
     mx = _mx()
     plan = mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile)
     assert plan["m_tile"] == (m_tile or 256) and plan["issuers"] == 2, plan
+    assert plan["scale_stores"] == (1 if path == 2 else 0), plan
     assert plan["tmem_cols"] >= plan["m_tile"] + 32 * plan["stages"], plan
     a = workloads.random_bf16(M, K, seed=M + K + 256)
     b = workloads.random_bf16(N, K, seed=N + K + 256, scale=0.5)

@@ -67,6 +67,10 @@ def test_invariants_over_a_grid(mx):
                             assert p["smem_bytes"] <= 227 * 1024, p
                         if p["issuers"] == 3 and p["path"] == 2:   # the lent epilogue warp: only without refills
                             assert p["stages"] == steps and p["m_tile"] <= 128, p
+                        # scale factors by tensor-memory stores on the two-kernel path, where the
+                        # tensor pipe is the limit: two issuers sharing each step, or a refilled ring
+                        wide = p["m_tile"] > 128 and p["issuers"] == 2
+                        assert p["scale_stores"] == int(p["path"] == 2 and (wide or steps > p["stages"])), p
                         if p["m_tile"] > 128:   # two issuers, each with part of every step's tokens
                             assert p["issuers"] == 2, p
                             assert p["m_tile"] + 32 * p["stages"] <= p["tmem_cols"], p
