@@ -106,6 +106,17 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_quantize_tokens.restype = _int
             L.mxfp4_gemm_tokens.argtypes = [_vp, _sz, _i64, _i64, _int, _vp, _i64, _vp, _i64, _int, _vp]
             L.mxfp4_gemm_tokens.restype = _int
+            _pp = ctypes.POINTER(_vp)
+            L.mxfp4_call_create.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _sz,
+                                            ctypes.POINTER(_Options), _pp]
+            L.mxfp4_call_create.restype = _int
+            L.mxfp4_call_create_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _sz,
+                                                 ctypes.c_uint, _pp]
+            L.mxfp4_call_create_host.restype = _int
+            L.mxfp4_call_run.argtypes = [_vp, _vp]
+            L.mxfp4_call_run.restype = _int
+            L.mxfp4_call_destroy.argtypes = [_vp]
+            L.mxfp4_call_destroy.restype = None
             _LIB = L
     return _LIB
 
@@ -368,15 +379,6 @@ def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor 
     return c
 
 
-def prepare_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor,
-                 workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
-                 stream=None, m_tile: int = 0) -> PreparedCall:
-    """mxfp4_gemm prepared for repeated calls on the same buffers (see PreparedCall); `c` is
-    required, the other arguments are those of mxfp4_gemm."""
-    c, args, ws = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
-    return PreparedCall(load_library().mxfp4_gemm_ex, args, "mxfp4_gemm", (a, packed_b, c, ws))
-
-
 def _host_call_args(a_host, packed_b, N, c_host, a_dev, c_dev, workspace, stream) -> tuple:
     """The checked arguments of one mxfp4_gemm_host call, in C order."""
     L = load_library()
@@ -423,31 +425,54 @@ def mxfp4_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host
 
 class PreparedCall:
     """A GEMM call whose buffers stay the same from one call to the next (a serving loop with
-    fixed input and output buffers): the tensors are checked once, when the call is prepared,
-    and each call passes the saved pointers and sizes straight to the C entry point. The
-    tensors are kept alive by this object; the caller must not resize or replace their storage
-    while it is in use. Calling it enqueues one call on the stream given when it was prepared
-    and raises Mxfp4Error if the library refuses it."""
+    fixed input and output buffers), prepared in the library (mxfp4_call_create*): its checks,
+    plan and host-buffer queries are done once, and each call only enqueues its kernels and
+    copies on the stream given when it was prepared. The tensors are kept alive by this object;
+    the caller must not resize or replace their storage while it is in use. Calling it raises
+    Mxfp4Error if the library refuses the run."""
 
-    __slots__ = ("_fn", "_args", "_where", "_keep")
+    __slots__ = ("_run", "_handle", "_stream", "_where", "_keep", "_destroy")
 
-    def __init__(self, fn, args: tuple, where: str, keep: tuple):
-        self._fn, self._args, self._where, self._keep = fn, args, where, keep
+    def __init__(self, create, args: tuple, stream: int, where: str, keep: tuple):
+        L = load_library()
+        handle = ctypes.c_void_p()
+        _check(create(*args, ctypes.byref(handle)), where)
+        self._run, self._destroy = L.mxfp4_call_run, L.mxfp4_call_destroy
+        self._handle, self._stream, self._where, self._keep = handle.value, stream, where, keep
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        st = self._run(self._handle, self._stream)
         if st != 0:
             raise Mxfp4Error(st, self._where)
+
+    def __del__(self):
+        handle, self._handle = getattr(self, "_handle", None), None
+        if handle:
+            self._destroy(handle)
+
+
+def prepare_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor,
+                 workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
+                 stream=None, m_tile: int = 0) -> PreparedCall:
+    """mxfp4_gemm prepared for repeated calls on the same buffers (see PreparedCall); `c` is
+    required, the other arguments are those of mxfp4_gemm."""
+    c, args, ws = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
+    return PreparedCall(load_library().mxfp4_call_create, args[:-1], args[-1], "mxfp4_call_create",
+                        (a, packed_b, c, ws))
 
 
 def prepare_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_host: torch.Tensor,
                       a_dev: torch.Tensor, c_dev: torch.Tensor, workspace: torch.Tensor | None = None,
-                      stream=None) -> PreparedCall:
+                      stream=None, a_host_written: bool = False) -> PreparedCall:
     """mxfp4_gemm_host prepared for repeated calls on the same buffers (see PreparedCall); the
-    arguments are those of mxfp4_gemm_host."""
+    arguments are those of mxfp4_gemm_host. a_host_written: the caller guarantees that a_host is
+    written by the host only, never by device work (MXFP4_CALL_A_HOST_WRITTEN), so A crosses the
+    link while the work before the call still runs."""
     args = _host_call_args(a_host, packed_b, N, c_host, a_dev, c_dev, workspace, stream)
     keep = (a_host, packed_b, c_host, a_dev, c_dev, workspace)
-    return PreparedCall(load_library().mxfp4_gemm_host, args, "mxfp4_gemm_host", keep)
+    flags = 1 if a_host_written else 0
+    return PreparedCall(load_library().mxfp4_call_create_host, args[:-1] + (flags,), args[-1],
+                        "mxfp4_call_create_host", keep)
 
 
 def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,

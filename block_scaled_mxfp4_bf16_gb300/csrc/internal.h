@@ -204,7 +204,9 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
                                    int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s);
 // bf16 rows [rows, K] at row stride lda (elements; 16-byte aligned rows, K % 8 == 0) from
 // device-accessible host memory -> packed device rows [rows, K]; PDL-chained (see the kernel).
-cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, cudaStream_t s);
+// early: read src before waiting for the previous grid (the caller declared it host-written only)
+cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, bool early,
+                              cudaStream_t s);
 // Pre-quantized B (natural layout) -> weight blocks [n_tiles][k_atoms][kWBlock].
 cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out,
                            cudaStream_t s);

@@ -4,6 +4,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <new>
 #include <tuple>
 
 #include "../../include/mxfp4_gb300.h"
@@ -566,7 +567,7 @@ const char* mxfp4_status_string(int status) {
 
 int mxfp4_last_cuda_error(void) { return t_last_cuda_error; }
 
-int mxfp4_version(void) { return 202; }
+int mxfp4_version(void) { return 203; }
 
 int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, void* scales, void* stream) {
     if (rows < 0 || K < 0) return MXFP4_ERR_ARG;
@@ -678,23 +679,145 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
     return MXFP4_OK;
 }
 
-int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
-                  int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts, void* stream) {
+}  // extern "C"
+
+// A call with everything checked and resolved: the plan, the device, and for host buffers where
+// A comes from and where C goes. mxfp4_gemm_ex / mxfp4_gemm_host resolve one per call; a
+// prepared call (mxfp4_call_create*) keeps one and only enqueues at each run.
+struct mxfp4_call {
+    mxfp4::DeviceInfo di;
+    mxfp4::GemmPlan plan;
+    bool empty;              // M == 0 or N == 0: nothing to enqueue
+    // the GEMM itself
+    const void* a;           // the device A the GEMM reads (a_dev for host buffers)
+    int64_t M, K, lda, N;
+    const void* packed_b;
+    void* c;                 // where the GEMM stores C: the caller's C, mapped c_host, or c_dev
+    int64_t ldc;
+    uint8_t* ws;
+    // host buffers: A arrives from a_host (mapped: staged by a kernel), C leaves to c_host
+    bool host;
+    const void* a_host;
+    const void* a_mapped;    // device address of mapped page-locked a_host, or null (copied)
+    bool a_early;            // a_host is written by the host only: staged without waiting first
+    int64_t a_host_ld;
+    void* a_dev;
+    void* c_host;            // copy-out target when C goes through c_dev (else null)
+    int64_t c_host_ld;
+    void* c_dev;
+};
+
+namespace mxfp4 {
+
+// mxfp4_gemm_ex's checks and plan, into `call`.
+static int resolve_device_call(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
+                               void* c, int64_t ldc, void* workspace, size_t ws_bytes,
+                               const mxfp4_gemm_options* opts, mxfp4_call* call) {
     if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    *call = mxfp4_call{};
     int st = check_gemm_args(a, M, K, lda, packed_b, N, c, ldc);
-    if (st != MXFP4_OK || M == 0 || N == 0) return st;
-    DeviceInfo di;
-    st = device_info(&di);
     if (st != MXFP4_OK) return st;
-    GemmPlan plan;
-    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
+    call->empty = M == 0 || N == 0;
+    if (call->empty) return MXFP4_OK;
+    st = device_info(&call->di);
     if (st != MXFP4_OK) return st;
-    if (plan.ws_total > 0) {
-        if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
+    st = cached_plan(call->di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0,
+                     &call->plan);
+    if (st != MXFP4_OK) return st;
+    if (call->plan.ws_total > 0) {
+        if (!workspace || ws_bytes < call->plan.ws_total) return MXFP4_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
     }
-    return run_gemm(plan, di, a, M, K, lda, packed_b, N, c, ldc, static_cast<uint8_t*>(workspace),
-                    static_cast<cudaStream_t>(stream));
+    call->a = a;
+    call->M = M;
+    call->K = K;
+    call->lda = lda;
+    call->packed_b = packed_b;
+    call->N = N;
+    call->c = c;
+    call->ldc = ldc;
+    call->ws = static_cast<uint8_t*>(workspace);
+    return MXFP4_OK;
+}
+
+// mxfp4_gemm_host's checks and plan, and where A comes from and C goes, into `call`.
+static int resolve_host_call(const void* a_host, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
+                             void* c_host, int64_t ldc, void* a_dev, void* c_dev, void* workspace, size_t ws_bytes,
+                             unsigned flags, mxfp4_call* call) {
+    if (flags & ~static_cast<unsigned>(MXFP4_CALL_A_HOST_WRITTEN)) return MXFP4_ERR_ARG;
+    // everything the device-side call checks is checked first, so nothing is copied on an error
+    int st = resolve_device_call(a_dev, M, K, K, packed_b, N, c_dev, N, workspace, ws_bytes, nullptr, call);
+    if (st != MXFP4_OK || call->empty) return st;
+    if (!a_host || !c_host) return MXFP4_ERR_ARG;
+    if (lda < K || ldc < N) return MXFP4_ERR_SHAPE;
+    call->host = true;
+    call->a_host = a_host;
+    call->a_host_ld = lda;
+    call->a_dev = a_dev;
+    call->c_dev = c_dev;
+    // A: page-locked host memory mapped into the device's address space (16-byte aligned rows)
+    // is staged by a kernel that reads it in place, so the launch chain from the previous call's
+    // GEMM to this one is never broken by a copy-engine transfer; anything else is copied.
+    cudaPointerAttributes a_attr = {};
+    if (cudaPointerGetAttributes(&a_attr, a_host) == cudaSuccess && a_attr.type == cudaMemoryTypeHost)
+        call->a_mapped = a_attr.devicePointer;
+    else
+        cudaGetLastError();   // clear the error an unregistered pointer leaves behind
+    if (call->a_mapped && !(aligned(call->a_mapped, 16) && lda % 8 == 0)) call->a_mapped = nullptr;
+    call->a_early = (flags & MXFP4_CALL_A_HOST_WRITTEN) != 0;
+    // Page-locked host memory mapped into the device's address space takes C straight from the
+    // epilogue's stores (no separate device -> host copy) when it is aligned for bf16 stores;
+    // anything else goes through c_dev.
+    cudaPointerAttributes attr = {};
+    void* c_mapped = nullptr;
+    if (cudaPointerGetAttributes(&attr, c_host) == cudaSuccess && attr.type == cudaMemoryTypeHost)
+        c_mapped = attr.devicePointer;
+    else
+        cudaGetLastError();   // clear the error an unregistered pointer leaves behind
+    if (c_mapped && aligned(c_mapped, 2)) {
+        call->c = c_mapped;
+        call->ldc = ldc;
+    } else {
+        call->c_host = c_host;
+        call->c_host_ld = ldc;
+    }
+    return MXFP4_OK;
+}
+
+// Enqueue a resolved call on `s`.
+static int run_call(const mxfp4_call& call, cudaStream_t s) {
+    if (call.empty) return MXFP4_OK;
+    const size_t a_row = static_cast<size_t>(call.K) * 2, c_row = static_cast<size_t>(call.N) * 2;
+    cudaError_t e;
+    if (call.host) {
+        if (call.a_mapped)
+            e = launch_stage_rows(call.a_mapped, call.a_host_ld, call.a_dev, call.M, call.K, call.a_early, s);
+        else   // one linear copy when the host rows are contiguous, a strided one otherwise
+            e = call.a_host_ld == call.K
+                    ? cudaMemcpyAsync(call.a_dev, call.a_host, a_row * call.M, cudaMemcpyHostToDevice, s)
+                    : cudaMemcpy2DAsync(call.a_dev, a_row, call.a_host, static_cast<size_t>(call.a_host_ld) * 2,
+                                        a_row, static_cast<size_t>(call.M), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const int st = run_gemm(call.plan, call.di, call.a, call.M, call.K, call.lda, call.packed_b, call.N, call.c,
+                            call.ldc, call.ws, s);
+    if (st != MXFP4_OK || !call.c_host) return st;
+    e = call.c_host_ld == call.N
+            ? cudaMemcpyAsync(call.c_host, call.c_dev, c_row * call.M, cudaMemcpyDeviceToHost, s)
+            : cudaMemcpy2DAsync(call.c_host, static_cast<size_t>(call.c_host_ld) * 2, call.c_dev, c_row, c_row,
+                                static_cast<size_t>(call.M), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+}
+
+}  // namespace mxfp4
+
+extern "C" {
+
+int mxfp4_gemm_ex(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
+                  int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts, void* stream) {
+    mxfp4_call call;
+    const int st = resolve_device_call(a, M, K, lda, packed_b, N, c, ldc, workspace, ws_bytes, opts, &call);
+    return st != MXFP4_OK ? st : run_call(call, static_cast<cudaStream_t>(stream));
 }
 
 int mxfp4_gemm(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
@@ -705,58 +828,47 @@ int mxfp4_gemm(const void* a, int64_t M, int64_t K, int64_t lda, const void* pac
 int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
                     void* c_host, int64_t ldc, void* a_dev, void* c_dev, void* workspace, size_t ws_bytes,
                     void* stream) {
-    // everything the device-side call checks is checked first, so nothing is copied on an error
-    int st = check_gemm_args(a_dev, M, K, K, packed_b, N, c_dev, N);
-    if (st != MXFP4_OK || M == 0 || N == 0) return st;
-    if (!a_host || !c_host) return MXFP4_ERR_ARG;
-    if (lda < K || ldc < N) return MXFP4_ERR_SHAPE;
-    DeviceInfo di;
-    st = device_info(&di);
-    if (st != MXFP4_OK) return st;
-    GemmPlan plan;
-    st = cached_plan(di, M, N, K, 0, 0, 0, &plan);
-    if (st != MXFP4_OK) return st;
-    if (plan.ws_total > 0) {
-        if (!workspace || ws_bytes < plan.ws_total) return MXFP4_ERR_WORKSPACE;
-        if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t a_row = static_cast<size_t>(K) * 2, c_row = static_cast<size_t>(N) * 2;
-    // A: page-locked host memory mapped into the device's address space (16-byte aligned rows)
-    // is staged by a kernel that reads it in place, so the launch chain from the previous call's
-    // GEMM to this one is never broken by a copy-engine transfer; anything else is copied.
-    cudaPointerAttributes a_attr = {};
-    const void* a_mapped = nullptr;
-    if (cudaPointerGetAttributes(&a_attr, a_host) == cudaSuccess && a_attr.type == cudaMemoryTypeHost)
-        a_mapped = a_attr.devicePointer;
-    else
-        cudaGetLastError();   // clear the error an unregistered pointer leaves behind
-    cudaError_t e;
-    if (a_mapped && aligned(a_mapped, 16) && lda % 8 == 0)
-        e = launch_stage_rows(a_mapped, lda, a_dev, M, K, s);
-    else   // one linear copy when the host rows are contiguous, a strided one otherwise
-        e = lda == K ? cudaMemcpyAsync(a_dev, a_host, a_row * M, cudaMemcpyHostToDevice, s)
-                     : cudaMemcpy2DAsync(a_dev, a_row, a_host, static_cast<size_t>(lda) * 2, a_row,
-                                         static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    // Page-locked host memory mapped into the device's address space takes C straight from the
-    // epilogue's stores (no separate device -> host copy) when it is aligned for bf16 stores;
-    // anything else goes through c_dev.
-    cudaPointerAttributes attr = {};
-    void* c_mapped = nullptr;
-    if (cudaPointerGetAttributes(&attr, c_host) == cudaSuccess && attr.type == cudaMemoryTypeHost)
-        c_mapped = attr.devicePointer;
-    else
-        cudaGetLastError();   // clear the error an unregistered pointer leaves behind
-    if (c_mapped && aligned(c_mapped, 2))
-        return run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_mapped, ldc, static_cast<uint8_t*>(workspace), s);
-    st = run_gemm(plan, di, a_dev, M, K, K, packed_b, N, c_dev, N, static_cast<uint8_t*>(workspace), s);
-    if (st != MXFP4_OK) return st;
-    e = ldc == N ? cudaMemcpyAsync(c_host, c_dev, c_row * M, cudaMemcpyDeviceToHost, s)
-                 : cudaMemcpy2DAsync(c_host, static_cast<size_t>(ldc) * 2, c_dev, c_row, c_row,
-                                     static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
-    return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
+    mxfp4_call call;
+    const int st = resolve_host_call(a_host, M, K, lda, packed_b, N, c_host, ldc, a_dev, c_dev, workspace, ws_bytes,
+                                     0u, &call);
+    return st != MXFP4_OK ? st : run_call(call, static_cast<cudaStream_t>(stream));
 }
+
+int mxfp4_call_create(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
+                      int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts,
+                      mxfp4_call** out) {
+    if (!out) return MXFP4_ERR_ARG;
+    *out = nullptr;
+    mxfp4_call call;
+    const int st = resolve_device_call(a, M, K, lda, packed_b, N, c, ldc, workspace, ws_bytes, opts, &call);
+    if (st != MXFP4_OK) return st;
+    *out = new (std::nothrow) mxfp4_call(call);
+    return *out ? MXFP4_OK : MXFP4_ERR_ARG;
+}
+
+int mxfp4_call_create_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
+                           void* c_host, int64_t ldc, void* a_dev, void* c_dev, void* workspace, size_t ws_bytes,
+                           unsigned flags, mxfp4_call** out) {
+    if (!out) return MXFP4_ERR_ARG;
+    *out = nullptr;
+    mxfp4_call call;
+    const int st = resolve_host_call(a_host, M, K, lda, packed_b, N, c_host, ldc, a_dev, c_dev, workspace, ws_bytes,
+                                     flags, &call);
+    if (st != MXFP4_OK) return st;
+    *out = new (std::nothrow) mxfp4_call(call);
+    return *out ? MXFP4_OK : MXFP4_ERR_ARG;
+}
+
+int mxfp4_call_run(const mxfp4_call* call, void* stream) {
+    if (!call) return MXFP4_ERR_ARG;
+    if (!call->empty) {   // a call runs on the device it was prepared on
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev != call->di.device) return MXFP4_ERR_ARG;
+    }
+    return run_call(*call, static_cast<cudaStream_t>(stream));
+}
+
+void mxfp4_call_destroy(mxfp4_call* call) { delete call; }
 
 // Token-block layout of M tokens of depth K in tiles of m_tile tokens: (tiles, bytes).
 static bool token_blocks_layout(int64_t M, int64_t K, int m_tile, int* m_tile_out, size_t* bytes) {

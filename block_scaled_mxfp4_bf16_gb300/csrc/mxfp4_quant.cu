@@ -182,23 +182,27 @@ prepack_kernel(const uint8_t* __restrict__ bq, const uint8_t* __restrict__ bs, i
 }
 
 // Host rows -> device rows for the host-buffer GEMM: one 16-byte piece per thread, read from
-// page-locked host memory mapped into the device's address space (zero-copy). Both the read and
-// the store come after the wait on the previous grid: that grid may still read the destination,
-// and it may also be writing the source (a chained call whose C, stored into mapped host memory,
-// is this call's A), so the stream order a copy would give is kept. Unlike a copy-engine
-// transfer, a kernel keeps the programmatic-dependent-launch chain from the previous GEMM
-// through this copy to the next GEMM, so their launches still overlap.
+// page-locked host memory mapped into the device's address space (zero-copy). The store comes
+// after the wait on the previous grid, which may still read the destination. So does the read,
+// unless the caller has declared the source written by the host only (kEarly): otherwise that
+// grid may be writing it (a chained call whose C, stored into mapped host memory, is this
+// call's A), and the stream order a copy would give is kept. With kEarly the read crosses the
+// link while the previous grid still runs. Unlike a copy-engine transfer, a kernel keeps the
+// programmatic-dependent-launch chain from the previous GEMM through this copy to the next
+// GEMM, so their launches still overlap.
+template <bool kEarly>
 __global__ void __launch_bounds__(256)
 stage_rows_kernel(const uint4* __restrict__ src, int64_t src_row16, uint4* __restrict__ dst, int64_t row16,
                   int64_t pieces) {
     pdl_launch_dependents();
-    pdl_wait_prior_grid();
+    if (!kEarly) pdl_wait_prior_grid();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < pieces) {
-        const int64_t r = i / row16;
-        const int64_t c = i - r * row16;
-        dst[r * row16 + c] = src[r * src_row16 + c];
-    }
+    const int64_t r = i / row16;
+    const int64_t c = i - r * row16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (i < pieces) v = src[r * src_row16 + c];
+    if (kEarly) pdl_wait_prior_grid();
+    if (i < pieces) dst[r * row16 + c] = v;
 }
 
 constexpr int64_t kQuantFourLaneMaxBlocks = 16384;
@@ -237,13 +241,18 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
                       ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
 }
 
-cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, cudaStream_t s) {
+cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, bool early,
+                              cudaStream_t s) {
     const int threads = 256;
     const int64_t row16 = K / 8, pieces = rows * row16;
     const int64_t blocks = (pieces + threads - 1) / threads;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    return launch_pdl(stage_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
-                      static_cast<const uint4*>(src), lda / 8, static_cast<uint4*>(dst), row16, pieces);
+    const auto* in = static_cast<const uint4*>(src);
+    auto* out = static_cast<uint4*>(dst);
+    return early ? launch_pdl(stage_rows_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, in,
+                              lda / 8, out, row16, pieces)
+                 : launch_pdl(stage_rows_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, in,
+                              lda / 8, out, row16, pieces);
 }
 
 cudaError_t launch_prepack(const uint8_t* bq, const uint8_t* bs, int64_t N, int64_t K, uint8_t* out, cudaStream_t s) {

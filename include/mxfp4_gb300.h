@@ -63,7 +63,9 @@ const char *mxfp4_status_string(int status);
 int mxfp4_last_cuda_error(void);
 
 /* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64).
- * 2.02: token-block entry points (mxfp4_quantize_tokens, mxfp4_gemm_tokens). */
+ * 2.02: token-block entry points (mxfp4_quantize_tokens, mxfp4_gemm_tokens). 2.03: prepared
+ * calls (mxfp4_call_create, mxfp4_call_create_host, mxfp4_call_run, mxfp4_call_destroy) and the
+ * scale_stores field of mxfp4_plan_info. */
 int mxfp4_version(void);
 
 /*
@@ -208,6 +210,43 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *o
 int mxfp4_gemm_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const void *packed_b, int64_t N,
                     void *c_host, int64_t ldc, void *a_dev, void *c_dev, void *workspace, size_t ws_bytes,
                     void *stream);
+
+/*
+ * Prepared calls -- for a serving loop whose buffers stay the same from one call to the next.
+ * mxfp4_call_create (the arguments of mxfp4_gemm_ex) and mxfp4_call_create_host (those of
+ * mxfp4_gemm_host) do all of that call's checks, its planning and, for host buffers, the queries
+ * of where A comes from and where C goes, once, on the current device; each mxfp4_call_run then
+ * only enqueues the call's kernels and copies on `stream`: exactly what the unprepared call would
+ * enqueue with the same arguments (same results, bit for bit).
+ *   out    : receives a handle owned by the caller, released with mxfp4_call_destroy (NULL is a
+ *            no-op there). On an error *out is NULL and nothing is allocated.
+ *   Buffers: every pointer given at creation must stay valid, with the same size and (for host
+ *            memory) the same page-locked / mapped state, until the last run has completed on
+ *            its stream; their contents may change freely between runs.
+ * Runs of one call share its workspace (and a_dev / c_dev): order them (one stream, or events),
+ * as for repeated unprepared calls. mxfp4_call_run must be made on the device the call was
+ * created on (MXFP4_ERR_ARG otherwise) and returns MXFP4_OK or MXFP4_ERR_CUDA if a launch or copy
+ * fails to enqueue.
+ * Errors at creation: those of mxfp4_gemm_ex / mxfp4_gemm_host; MXFP4_ERR_ARG also if `out` is
+ * NULL or the handle cannot be allocated.
+ */
+typedef struct mxfp4_call mxfp4_call;
+int mxfp4_call_create(const void *a, int64_t M, int64_t K, int64_t lda, const void *packed_b, int64_t N,
+                      void *c, int64_t ldc, void *workspace, size_t ws_bytes, const mxfp4_gemm_options *opts,
+                      mxfp4_call **out);
+/* flags: 0, or MXFP4_CALL_A_HOST_WRITTEN -- the caller guarantees that a_host is written by the
+ * host only, never by device work (in particular it is not the C of an earlier call, and no
+ * device-to-host copy into it is pending). A staged from mapped page-locked a_host is then read
+ * over the link as soon as the call's first kernel starts, while the work before it on the
+ * stream still runs, instead of after that work; as always, the host must have written A
+ * before the run is enqueued. Without the flag (and in mxfp4_gemm_host) A is read only once
+ * the work before it has completed. Other bits: MXFP4_ERR_ARG. */
+#define MXFP4_CALL_A_HOST_WRITTEN 1u
+int mxfp4_call_create_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const void *packed_b,
+                           int64_t N, void *c_host, int64_t ldc, void *a_dev, void *c_dev, void *workspace,
+                           size_t ws_bytes, unsigned flags, mxfp4_call **out);
+int mxfp4_call_run(const mxfp4_call *call, void *stream);
+void mxfp4_call_destroy(mxfp4_call *call);
 
 /*
  * Token blocks: A quantized once into the layout the GEMM's tensor cores read, for callers that

@@ -91,3 +91,26 @@ def test_plan_info_layout_and_null_check(lib):
                                          ctypes.c_void_p]
     assert lib.mxfp4_gemm_plan_info(8, 2112, 7168, None, None) == 1      # MXFP4_ERR_ARG, no device needed
 
+
+
+def test_prepared_call_null_checks(lib):
+    # a prepared call's entry points refuse a missing handle or output slot before touching a
+    # device, and destroying no handle is a no-op
+    vp = ctypes.c_void_p
+    lib.mxfp4_call_run.argtypes = [vp, vp]
+    lib.mxfp4_call_run.restype = ctypes.c_int
+    lib.mxfp4_call_destroy.argtypes = [vp]
+    lib.mxfp4_call_destroy.restype = None
+    i64, sz = ctypes.c_int64, ctypes.c_size_t
+    lib.mxfp4_call_create.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, sz, vp, vp]
+    lib.mxfp4_call_create.restype = ctypes.c_int
+    lib.mxfp4_call_create_host.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, vp, vp, sz, ctypes.c_uint, vp]
+    lib.mxfp4_call_create_host.restype = ctypes.c_int
+    assert lib.mxfp4_call_run(None, None) == 1          # MXFP4_ERR_ARG
+    lib.mxfp4_call_destroy(None)
+    assert lib.mxfp4_call_create(None, 8, 512, 512, None, 256, None, 256, None, 0, None, None) == 1
+    assert lib.mxfp4_call_create_host(None, 8, 512, 512, None, 256, None, 256, None, None, None, 0, 0, None) == 1
+    out = vp(1234)
+    # a null A is refused by the argument checks and leaves no handle behind
+    assert lib.mxfp4_call_create(None, 8, 512, 512, None, 256, None, 256, None, 0, None, ctypes.byref(out)) == 1
+    assert out.value is None

@@ -22,16 +22,29 @@ def dev(t: torch.Tensor) -> torch.Tensor:
 
 
 class _Lib:
-    """The real library for size queries; compute calls are recorded and succeed."""
+    """The real library for size queries; compute calls are recorded and succeed (a prepared
+    call's creation hands out handle 1000 + its index among the calls, its runs return `run_status`)."""
 
     COMPUTE = ("mxfp4_quantize", "mxfp4_prepack_b", "mxfp4_gemm_ex", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
-               "mxfp4_workspace_init", "mxfp4_quantize_tokens", "mxfp4_gemm_tokens")
+               "mxfp4_workspace_init", "mxfp4_quantize_tokens", "mxfp4_gemm_tokens", "mxfp4_call_run",
+               "mxfp4_call_destroy")
+    CREATE = ("mxfp4_call_create", "mxfp4_call_create_host")
 
     def __init__(self, real):
         self.real = real
         self.calls = []
+        self.run_status = 0
+
+    def _create(self, name, *args):
+        args[-1]._obj.value = 1000 + len(self.calls)   # the handle, written through the out pointer
+        self.calls.append((name, args[:-1]))
+        return 0
 
     def __getattr__(self, name):
+        if name in self.CREATE:
+            return lambda *args: self._create(name, *args)
+        if name == "mxfp4_call_run":
+            return lambda *args: self.calls.append((name, args)) or self.run_status
         if name in self.COMPUTE:
             return lambda *args: self.calls.append((name, args)) or 0
         if name == "mxfp4_gemm_workspace_size_ex":
@@ -179,15 +192,19 @@ def test_prepack_checks(lib):
 
 
 def test_prepared_calls_pass_the_same_arguments(lib):
-    # a prepared call checks its tensors once and then passes exactly what the plain call passes
+    # a prepared call hands the library, once, exactly what the plain call passes (without the
+    # stream); each call then runs the library's handle on the stream it was prepared with, and
+    # dropping the call releases the handle
     a, packed, N = _gemm_operands()
     c = dev(torch.zeros(8, N, dtype=torch.bfloat16))
     mx.mxfp4_gemm(a, packed, N, c=c, stream=0)
     call = mx.prepare_gemm(a, packed, N, c, stream=0)
-    assert len(lib.calls) == 1                       # preparing calls nothing
+    assert lib.calls[1] == ("mxfp4_call_create", lib.calls[0][1][:-1])
     call()
     call()
-    assert lib.calls[1] == lib.calls[0] and lib.calls[2] == lib.calls[0]
+    assert lib.calls[2] == lib.calls[3] == ("mxfp4_call_run", (1001, 0))
+    del call
+    assert lib.calls[4] == ("mxfp4_call_destroy", (1001,))
     M, K = 4, 512
     _, packed, _ = _gemm_operands(M, N, K)
     a_host = torch.zeros(M, K, dtype=torch.bfloat16)
@@ -197,7 +214,11 @@ def test_prepared_calls_pass_the_same_arguments(lib):
     mx.mxfp4_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0)
     host_call = mx.prepare_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0)
     host_call()
-    assert lib.calls[3][0] == "mxfp4_gemm_host" and lib.calls[4] == lib.calls[3]
+    assert lib.calls[5][0] == "mxfp4_gemm_host"
+    assert lib.calls[6] == ("mxfp4_call_create_host", lib.calls[5][1][:-1] + (0,))
+    assert lib.calls[7] == ("mxfp4_call_run", (1006, 0))
+    mx.prepare_gemm_host(a_host, packed, N, c_host, a_dev, c_dev, stream=0, a_host_written=True)
+    assert lib.calls[8] == ("mxfp4_call_create_host", lib.calls[5][1][:-1] + (1,))   # MXFP4_CALL_A_HOST_WRITTEN
 
 
 def test_prepared_calls_check_when_prepared(lib):
@@ -213,14 +234,16 @@ def test_prepared_calls_check_when_prepared(lib):
     assert lib.calls == []
 
 
-def test_prepared_call_raises_the_library_status():
-    # the status word the C entry point returns becomes the binding's exception
-    seen = []
-    call = mx.PreparedCall(lambda *args: seen.append(args) or 4, (1, 2, 3), "mxfp4_gemm", ())
+def test_prepared_call_raises_the_library_status(lib):
+    # the status word a run returns becomes the binding's exception; so does a refused creation
+    a, packed, N = _gemm_operands()
+    call = mx.prepare_gemm(a, packed, N, dev(torch.zeros(8, N, dtype=torch.bfloat16)), stream=0)
+    call()
+    lib.run_status = 4
     with pytest.raises(mx.Mxfp4Error):
         call()
-    assert seen == [(1, 2, 3)]
-    mx.PreparedCall(lambda *args: 0, (), "mxfp4_gemm", ())()
+    with pytest.raises(mx.Mxfp4Error):
+        mx.PreparedCall(lambda *args: 2, (), 0, "mxfp4_call_create", ())
 
 
 def test_token_layout_sizes():

@@ -375,6 +375,89 @@ def test_prepared_calls_match_plain_calls():
     assert mx.mxfp4_device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
+    (16, 3072, 1536, 0, 0, 0),       # weight-resident, split K
+    (5, 300, 520, 1, 2, 0),          # fused, K tail
+    (64, 7168, 2048, 0, 0, 0),       # two-kernel (workspace)
+    (300, 384, 1536, 2, 1, 192),     # two issuers sharing every step, scale factors stored by warps
+])
+def test_prepared_calls_every_plan(M, N, K, path, splits, m_tile):
+    # the library's prepared calls (created once, run many times) against the plain calls on the
+    # same buffers, for each kind of plan; host buffers both page-locked (A staged by a kernel, C
+    # stored straight into them; A read before or after the work ahead of it) and pageable
+    # (copied both ways)
+    mx = _mx()
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=M + 3).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    call = mx.prepare_gemm(a, packed, N, c, path=path, splits=splits, m_tile=m_tile)
+    a_dev = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    hosts = []
+    for pinned, early in ((True, False), (True, True), (False, False)):
+        a_host = torch.empty(M, K, dtype=torch.bfloat16)
+        c_host = torch.empty(M, N, dtype=torch.bfloat16)
+        if pinned:
+            a_host, c_host = a_host.pin_memory(), c_host.pin_memory()
+        # early: A declared host-written only, staged without waiting for the work before it
+        hosts.append((a_host, c_host, mx.prepare_gemm_host(a_host, packed, N, c_host, a_dev, c_dev,
+                                                           a_host_written=early)))
+    for seed in (5, 6):
+        x = workloads.random_bf16(M, K, seed=seed)
+        want = mx.mxfp4_gemm(x.cuda(), packed, N, path=path, splits=splits, m_tile=m_tile)
+        a.copy_(x)
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(c.view(torch.int16), want.view(torch.int16)), seed
+        auto = mx.mxfp4_gemm(x.cuda(), packed, N)   # host calls run the automatic plan
+        for a_host, c_host, host_call in hosts:
+            a_host.copy_(x)
+            c_host.zero_()
+            host_call()
+            torch.cuda.synchronize()
+            assert torch.equal(c_host.view(torch.int16), auto.cpu().view(torch.int16)), (seed, a_host.is_pinned())
+    assert mx.mxfp4_device_status() == 0
+
+
+def test_prepared_host_calls_chain_through_host_memory():
+    # C of one prepared host call is A of the next (K == N): the second call's staging must read
+    # the first call's C only once it is complete
+    mx = _mx()
+    M, N = 8, 1024
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, N, seed=41, scale=0.05).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    bufs = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    a_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    first = mx.prepare_gemm_host(bufs[0], packed, N, bufs[1], a_dev, c_dev)
+    second = mx.prepare_gemm_host(bufs[1], packed, N, bufs[2], a_dev, c_dev)
+    x = workloads.random_bf16(M, N, seed=42)
+    bufs[0].copy_(x)
+    for _ in range(3):
+        first()
+        second()
+    torch.cuda.synchronize()
+    once = mx.mxfp4_gemm(x.cuda(), packed, N)
+    twice = mx.mxfp4_gemm(once, packed, N)
+    assert torch.equal(bufs[2].view(torch.int16), twice.cpu().view(torch.int16))
+    assert mx.mxfp4_device_status() == 0
+
+
+def test_prepared_call_of_an_empty_product():
+    # M = 0: the call is created and each run enqueues nothing
+    mx = _mx()
+    N, K = 256, 512
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=9).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a = torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
+    call = mx.prepare_gemm(a, packed, N, c)
+    call()
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0
+
+
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile,stores", [
     (200, 384, 4096, 2, 1, 128, 1),   # 16 steps over 6 stages: refilled, scale factors stored by warps
     (100, 300, 5128, 2, 2, 64, 1),    # split-K, K tail, ragged weight tile, 11 steps over 8 stages
