@@ -38,21 +38,21 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2595072, None, "1e7adebd14201fa9",
+    "M16_N3072_K1536": (2594304, None, "b1dd3d1c61387cd9",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8439552, None, "1e7adebd14201fa9",
+    "M8_N2112_K7168": (8440064, None, "b1dd3d1c61387cd9",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1185280, None, "1e7adebd14201fa9",
+    "M32_N4096_K512": (1185280, None, "b1dd3d1c61387cd9",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
     "M64_N7168_K2048": (7941120, 270848, "02b9d32e457a8762",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
     "M256_N4096_K7168": (16640512, 3679744, "02b9d32e457a8762",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
-    "M4_N2880_K512": (843776, None, "1e7adebd14201fa9",
+    "M4_N2880_K512": (844032, None, "b1dd3d1c61387cd9",
                       "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M32_N2880_K512": (872704, None, "1e7adebd14201fa9",
+    "M32_N2880_K512": (872448, None, "b1dd3d1c61387cd9",
                        "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M16_N2112_K7168": (8554240, None, "1e7adebd14201fa9",
+    "M16_N2112_K7168": (8554752, None, "b1dd3d1c61387cd9",
                         "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
     "M256_N3072_K1536": (2796800, 795136, "02b9d32e457a8762",
                          "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),

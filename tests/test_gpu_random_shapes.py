@@ -40,3 +40,28 @@ def test_random_shape_vs_oracle(M, N, K, path, splits, m_tile, lda_pad, ldc_pad)
     assert_bytes_equal(bq, rq, "B e2m1")
     assert_bytes_equal(bs, rs, "B scales")
     check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} path {path} splits {splits} m_tile {m_tile}")
+
+
+def _wide_cases(n: int = 24, seed: int = 20261204):
+    # the two-kernel path where its ring refills (long K) and on tiles of more than 128 tokens:
+    # scale factors written into tensor memory by epilogue warps, two issuers sharing a step
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M = int(rng.choice([129, 144, 200, 256, 300, 384, 513, 600]))
+        N = int(rng.integers(1, 400))
+        K = 8 * int(rng.integers(100, 1100))
+        if M * N * K > 120_000_000:
+            continue
+        splits = int(rng.choice([0, 1, 2, 4]))
+        m_tile = int(rng.choice([0, 64, 128, 144, 192, 256]))
+        out.append((M, N, K, splits, m_tile, 8 * int(rng.integers(0, 3)), int(rng.integers(0, 5))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,splits,m_tile,lda_pad,ldc_pad", _wide_cases())
+def test_random_refilled_and_wide_tiles_vs_oracle(M, N, K, splits, m_tile, lda_pad, ldc_pad):
+    a = workloads.random_bf16(M, K, seed=M * 31 + K)
+    b = workloads.random_bf16(N, K, seed=N * 37 + K, scale=0.5)
+    c, bq, bs = run_gemm(a, b, path=2, splits=splits, lda_pad=lda_pad, ldc_pad=ldc_pad, m_tile=m_tile)
+    check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} two-kernel splits {splits} m_tile {m_tile}")
