@@ -44,9 +44,9 @@ MEASURED_TRAFFIC = {
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
     "M32_N4096_K512": (1185280, None, "b1dd3d1c61387cd9",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7941120, 270848, "02b9d32e457a8762",
+    "M64_N7168_K2048": (7942656, 270848, "aaad18935b674aa8",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16640512, 3679744, "02b9d32e457a8762",
+    "M256_N4096_K7168": (16641024, 3679744, "aaad18935b674aa8",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
     "M4_N2880_K512": (844032, None, "b1dd3d1c61387cd9",
                       "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
@@ -54,7 +54,7 @@ MEASURED_TRAFFIC = {
                        "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
     "M16_N2112_K7168": (8554752, None, "b1dd3d1c61387cd9",
                         "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M256_N3072_K1536": (2796800, 795136, "02b9d32e457a8762",
+    "M256_N3072_K1536": (2796800, 794880, "aaad18935b674aa8",
                          "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against

@@ -232,12 +232,16 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
     if (items <= kQuantFourLaneMaxBlocks)
         return launch_pdl(quantize_blocks4_kernel, dim3(grid_for(items * 4, threads)), dim3(threads), 0, s, x, rows,
                           K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+    // One lane per block in 128-thread blocks: more, smaller blocks than 256-thread ones shorten
+    // the launch's tail (256x4096x7168 11.85 -> 11.65 us per call, 512x4096x7168 14.23 -> 13.60;
+    // the four-lane kernel above measured mixed with 128 threads and keeps 256).
+    const int threads1 = 128;
     // item indices (and the grid-stride overshoot, below one more grid) within 32 bits: FastDiv
-    const int64_t span = items + static_cast<int64_t>(grid_for(items, threads)) * threads;
+    const int64_t span = items + static_cast<int64_t>(grid_for(items, threads1)) * threads1;
     if (span <= static_cast<int64_t>(UINT32_MAX))
-        return launch_pdl(quantize_blocks_kernel<true>, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows,
+        return launch_pdl(quantize_blocks_kernel<true>, dim3(grid_for(items, threads1)), dim3(threads1), 0, s, x, rows,
                           K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
-    return launch_pdl(quantize_blocks_kernel<false>, dim3(grid_for(items, threads)), dim3(threads), 0, s, x, rows, K,
+    return launch_pdl(quantize_blocks_kernel<false>, dim3(grid_for(items, threads1)), dim3(threads1), 0, s, x, rows, K,
                       ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
 }
 
