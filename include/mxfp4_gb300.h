@@ -219,7 +219,8 @@ int mxfp4_gemm_host(const void *a_host, int64_t M, int64_t K, int64_t lda, const
  * only enqueues the call's kernels and copies on `stream`: exactly what the unprepared call would
  * enqueue with the same arguments (same results, bit for bit).
  *   out    : receives a handle owned by the caller, released with mxfp4_call_destroy (NULL is a
- *            no-op there). On an error *out is NULL and nothing is allocated.
+ *            no-op there); a run keeps nothing of it, so it may be destroyed as soon as its last
+ *            run has been enqueued. On an error *out is NULL and nothing is allocated.
  *   Buffers: every pointer given at creation must stay valid, with the same size and (for host
  *            memory) the same page-locked / mapped state, until the last run has completed on
  *            its stream; their contents may change freely between runs.
