@@ -21,7 +21,7 @@ __all__ = [
     "mxfp4_gemm_workspace_size", "mxfp4_workspace_init", "mxfp4_gemm", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
     "mxfp4_gemm_plan", "mxfp4_gemm_plan_model", "mxfp4_device_status", "mxfp4_selftest_timeout", "mxfp4_version",
     "PreparedCall", "prepare_gemm", "prepare_gemm_host", "TokenBlocks", "mxfp4_token_tile", "mxfp4_token_blocks_size",
-    "mxfp4_quantize_tokens", "mxfp4_gemm_tokens",
+    "mxfp4_quantize_tokens", "mxfp4_gemm_tokens", "mxfp4_gemm_unpacked",
 ]
 
 _LOCK = threading.Lock()
@@ -106,6 +106,10 @@ def load_library() -> ctypes.CDLL:
             L.mxfp4_quantize_tokens.restype = _int
             L.mxfp4_gemm_tokens.argtypes = [_vp, _sz, _i64, _i64, _int, _vp, _i64, _vp, _i64, _int, _vp]
             L.mxfp4_gemm_tokens.restype = _int
+            L.mxfp4_gemm_unpacked_workspace_size.argtypes = [_i64, _i64, _i64]
+            L.mxfp4_gemm_unpacked_workspace_size.restype = _sz
+            L.mxfp4_gemm_unpacked.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _i64, _vp, _sz, _vp]
+            L.mxfp4_gemm_unpacked.restype = _int
             _pp = ctypes.POINTER(_vp)
             L.mxfp4_call_create.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _sz,
                                             ctypes.POINTER(_Options), _pp]
@@ -473,6 +477,44 @@ def prepare_gemm_host(a_host: torch.Tensor, packed_b: torch.Tensor, N: int, c_ho
     flags = 1 if a_host_written else 0
     return PreparedCall(load_library().mxfp4_call_create_host, args[:-1] + (flags,), args[-1],
                         "mxfp4_call_create_host", keep)
+
+
+def mxfp4_gemm_unpacked(a: torch.Tensor, bq: torch.Tensor, bs: torch.Tensor, c: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """mxfp4_gemm on B as mxfp4_quantize writes it (e2m1 [N, nblk*16], e8m0 [N, nblk], nblk =
+    ceil(K/32)): the call writes B's packed image into its workspace, then runs the GEMM
+    (mxfp4_gemm_unpacked). `workspace`, if given: a contiguous CUDA byte buffer of at least
+    mxfp4_gemm_unpacked_workspace_size bytes starting 1024-byte aligned."""
+    L = load_library()
+    _dev(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    M, K = a.shape
+    _on(bq, a.device, "bq")
+    _on(bs, a.device, "bs")
+    N = bq.shape[0] if bq.dim() == 2 else -1
+    nblk = -(-K // 32)
+    if (bq.dim() != 2 or tuple(bq.shape) != (N, nblk * 16) or tuple(bs.shape) != (N, nblk)
+            or not bq.is_contiguous() or not bs.is_contiguous() or bq.element_size() != 1 or bs.element_size() != 1):
+        raise ValueError("bq [N, ceil(K/32)*16] and bs [N, ceil(K/32)] must be contiguous byte tensors")
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _on(c, a.device, "c")
+    if c.dtype != torch.bfloat16 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be a bf16 [M, N] tensor with unit column stride")
+    st = _stream(stream)
+    need = L.mxfp4_gemm_unpacked_workspace_size(M, N, K) if M and N else 0
+    if workspace is None:
+        ws = _workspace(a.device, need + 1024, stream, st) if need else None
+        workspace = ws[(-ws.data_ptr()) % 1024:][:need] if ws is not None else None
+    elif (not workspace.is_cuda or not workspace.is_contiguous() or workspace.device != a.device
+          or workspace.nbytes < need):
+        raise ValueError(f"workspace must be a contiguous buffer of at least {need} bytes on {a.device}")
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.nbytes if workspace is not None else 0
+    _check(L.mxfp4_gemm_unpacked(a.data_ptr(), M, K, a.stride(0), bq.data_ptr(), bs.data_ptr(), N, c.data_ptr(),
+                                 c.stride(0), ws_ptr, ws_bytes, st), "mxfp4_gemm_unpacked")
+    return c
 
 
 def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,

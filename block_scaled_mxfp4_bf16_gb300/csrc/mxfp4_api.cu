@@ -834,6 +834,37 @@ int mxfp4_gemm_host(const void* a_host, int64_t M, int64_t K, int64_t lda, const
     return st != MXFP4_OK ? st : run_call(call, static_cast<cudaStream_t>(stream));
 }
 
+size_t mxfp4_gemm_unpacked_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0 || !weight_dims_fit(N, K)) return 0;
+    return align_up(packed_b_bytes(N, K), 1024) + mxfp4_gemm_workspace_size(M, N, K);
+}
+
+int mxfp4_gemm_unpacked(const void* a, int64_t M, int64_t K, int64_t lda, const void* bq, const void* bs,
+                        int64_t N, void* c, int64_t ldc, void* workspace, size_t ws_bytes, void* stream) {
+    // B's packed image goes to the start of the workspace, the GEMM's own workspace after it
+    if (M < 0 || N < 0 || K < 0) return MXFP4_ERR_ARG;
+    if (K == 0 || K % 8 != 0 || (N > 0 && !weight_dims_fit(N, K))) return MXFP4_ERR_SHAPE;
+    const size_t pb = N > 0 ? align_up(packed_b_bytes(N, K), 1024) : 0;
+    const bool empty = M == 0 || N == 0;
+    if (!empty) {
+        if (!bq || !bs) return MXFP4_ERR_ARG;
+        if (!aligned(bq, 16)) return MXFP4_ERR_ALIGN;
+        if (!workspace || ws_bytes < pb) return MXFP4_ERR_WORKSPACE;
+        if (!aligned(workspace, 1024)) return MXFP4_ERR_ALIGN;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mxfp4_call call;
+    const int st = resolve_device_call(a, M, K, lda, empty ? bq : ws, N, c, ldc, empty ? nullptr : ws + pb,
+                                       empty ? 0 : ws_bytes - pb, nullptr, &call);
+    if (st != MXFP4_OK || call.empty) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the prepack kernel never lets dependents start early, so the GEMM's early weight requests
+    // see its whole image (see mxfp4_gemm); the next call's prepack waits for this GEMM
+    const cudaError_t e = launch_prepack(static_cast<const uint8_t*>(bq), static_cast<const uint8_t*>(bs), N, K, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_call(call, s);
+}
+
 int mxfp4_call_create(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N, void* c,
                       int64_t ldc, void* workspace, size_t ws_bytes, const mxfp4_gemm_options* opts,
                       mxfp4_call** out) {

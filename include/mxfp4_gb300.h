@@ -64,8 +64,8 @@ int mxfp4_last_cuda_error(void);
 
 /* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64).
  * 2.02: token-block entry points (mxfp4_quantize_tokens, mxfp4_gemm_tokens). 2.03: prepared
- * calls (mxfp4_call_create, mxfp4_call_create_host, mxfp4_call_run, mxfp4_call_destroy) and the
- * scale_stores field of mxfp4_plan_info. */
+ * calls (mxfp4_call_create, mxfp4_call_create_host, mxfp4_call_run, mxfp4_call_destroy), the
+ * scale_stores field of mxfp4_plan_info, mxfp4_gemm_unpacked. */
 int mxfp4_version(void);
 
 /*
@@ -187,6 +187,24 @@ size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4
  * an argument or shape error, or MXFP4_ERR_ARCH / MXFP4_ERR_CUDA from the device query. */
 int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options *opts,
                     int *path, int *splits, int *m_tile, int *ctas, int *stages);
+
+/*
+ * mxfp4_gemm_unpacked -- mxfp4_gemm for B as mxfp4_quantize writes it: packed e2m1 nibbles
+ * bq [N, nblk*16] and e8m0 scales bs [N, nblk] (nblk = ceil(K/32)), the two arrays the pages'
+ * `custom_kernel` receives with A. The call first writes B's prepacked image (mxfp4_prepack_b)
+ * into the workspace, then runs mxfp4_gemm on it: the same C, bit for bit, at the cost of the
+ * prepack on every call. For weights used more than once, prepack them once and call mxfp4_gemm.
+ *   a, c, M, K, lda, ldc, N: as for mxfp4_gemm.  bq, bs: as for mxfp4_prepack_b.
+ *   workspace: ws_bytes >= mxfp4_gemm_unpacked_workspace_size(M, N, K), 1024-byte aligned:
+ *              B's image first (mxfp4_prepack_b_size rounded up to 1 KB), then mxfp4_gemm's
+ *              workspace. Calls sharing a workspace must be ordered, as for mxfp4_gemm (a call's
+ *              prepack waits for the work before it on `stream`).
+ * Errors: those of mxfp4_gemm and mxfp4_prepack_b, checked before anything is enqueued.
+ * mxfp4_gemm_unpacked_workspace_size returns 0 for invalid sizes.
+ */
+size_t mxfp4_gemm_unpacked_workspace_size(int64_t M, int64_t N, int64_t K);
+int mxfp4_gemm_unpacked(const void *a, int64_t M, int64_t K, int64_t lda, const void *bq, const void *bs,
+                        int64_t N, void *c, int64_t ldc, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * mxfp4_gemm_host -- mxfp4_gemm for A and C in host memory: on `stream`, move A (rows of K

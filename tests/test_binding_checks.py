@@ -27,7 +27,7 @@ class _Lib:
 
     COMPUTE = ("mxfp4_quantize", "mxfp4_prepack_b", "mxfp4_gemm_ex", "mxfp4_gemm_host", "mxfp4_gemm_noalloc",
                "mxfp4_workspace_init", "mxfp4_quantize_tokens", "mxfp4_gemm_tokens", "mxfp4_call_run",
-               "mxfp4_call_destroy")
+               "mxfp4_call_destroy", "mxfp4_gemm_unpacked")
     CREATE = ("mxfp4_call_create", "mxfp4_call_create_host")
 
     def __init__(self, real):
@@ -289,3 +289,34 @@ def test_token_calls_pass_pointers_and_check_buffers(lib):
     with pytest.raises(ValueError):   # C of the wrong shape
         mx.mxfp4_gemm_tokens(tokens, packed, N, c=dev(torch.zeros(M, N - 1, dtype=torch.bfloat16)), stream=0)
     assert len(lib.calls) == 2
+
+
+def test_unpacked_gemm_checks_and_arguments(lib):
+    # B as the quantizer writes it: [N, ceil(K/32)*16] codes and [N, ceil(K/32)] scales; the
+    # workspace handed over is 1024-byte aligned and holds B's image plus the GEMM's workspace
+    M, N, K = 8, 256, 520                                  # K cuts the last 1x32 block
+    nblk = -(-K // 32)
+    a = dev(torch.zeros(M, K, dtype=torch.bfloat16))
+    bq = dev(torch.zeros(N, nblk * 16, dtype=torch.uint8))
+    bs = dev(torch.zeros(N, nblk, dtype=torch.uint8))
+    need = lib.mxfp4_gemm_unpacked_workspace_size(M, N, K)   # B's image (no GEMM workspace without a GPU)
+    assert need >= mx.mxfp4_prepack_b_size(N, K)
+    raw = dev(torch.zeros(need + 1024, dtype=torch.uint8))
+    ws = raw[(-raw.data_ptr()) % 1024:][:need]
+    c = mx.mxfp4_gemm_unpacked(a, bq, bs, workspace=ws, stream=0)
+    (name, args), = lib.calls
+    assert name == "mxfp4_gemm_unpacked" and tuple(c.shape) == (M, N)
+    assert args[:7] == (a.data_ptr(), M, K, K, bq.data_ptr(), bs.data_ptr(), N)
+    assert args[9] == ws.data_ptr() and args[9] % 1024 == 0 and args[10] == need
+    for bad in [
+        (bq[:, :-16], bs),                                              # codes one block short
+        (bq, bs[:, :-1]),                                               # scales one block short
+        (_meta(N, nblk * 16), bs),                                      # codes on another device
+        (dev(torch.zeros(N, nblk * 16, dtype=torch.int16)), bs),        # codes not bytes
+        (bq, dev(torch.zeros(N, 2 * nblk, dtype=torch.uint8))[:, ::2]),  # scales not contiguous
+    ]:
+        with pytest.raises(ValueError):
+            mx.mxfp4_gemm_unpacked(a, *bad, workspace=ws, stream=0)
+    with pytest.raises(ValueError):   # workspace too small
+        mx.mxfp4_gemm_unpacked(a, bq, bs, workspace=dev(torch.zeros(1024, dtype=torch.uint8)), stream=0)
+    assert len(lib.calls) == 1

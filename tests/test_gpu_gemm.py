@@ -530,3 +530,29 @@ def test_quantized_a_read_back_through_one_hot_b(M, K, path, splits):
     assert np.array_equal(want, oracle.dequantize(aq, as_)[:, :K]), "one-hot B must read A back"
     bad = np.argwhere(c != want)
     assert bad.size == 0, f"{len(bad)} entries differ, first at {tuple(bad[0])}: got {c[tuple(bad[0])]!r} want {want[tuple(bad[0])]!r}"
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 2112, 7168), (5, 300, 520), (64, 1024, 2048), (300, 384, 1536)])
+def test_unpacked_gemm_matches_prepacked(M, N, K):
+    # B as the quantizer writes it, prepacked inside the call: the prepacked call's bits, and
+    # back-to-back calls with different weights on one workspace each see their own weights
+    mx = _mx()
+    a = workloads.random_bf16(M, K, seed=M + 17).cuda()
+    outs = []
+    for seed in (1, 2):
+        bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=N + seed).cuda())
+        want = mx.mxfp4_gemm(a, mx.mxfp4_prepack_b(bq, bs), N)
+        outs.append((bq, bs, want))
+    ws = None
+    for bq, bs, want in outs + outs:        # alternate the weights on the same stream and workspace
+        c = mx.mxfp4_gemm_unpacked(a, bq, bs, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(c.view(torch.int16), want.view(torch.int16))
+    assert mx.mxfp4_device_status() == 0
+    L = mx.load_library()
+    need = L.mxfp4_gemm_unpacked_workspace_size(M, N, K)
+    assert need >= mx.mxfp4_prepack_b_size(N, K) + mx.mxfp4_gemm_workspace_size(M, N, K)
+    raw = torch.empty(need + 1024, dtype=torch.uint8, device="cuda")
+    small = raw[(-raw.data_ptr()) % 1024:][:mx.mxfp4_prepack_b_size(N, K) - 1]
+    with pytest.raises(ValueError):   # the binding refuses a workspace below the size query
+        mx.mxfp4_gemm_unpacked(a, outs[0][0], outs[0][1], workspace=small)
