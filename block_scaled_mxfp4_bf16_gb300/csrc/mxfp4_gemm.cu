@@ -17,12 +17,16 @@
 //               stages are requested before the CTA waits on the previous grid (the weights never
 //               depend on it).
 //   warps 1-2 : tensor-memory allocation (warp 1) and two MMA-issuing threads (alternate 256-K
-//               steps, two accumulators): per 256-K step a thread copies the scale factors into
-//               tensor memory (tcgen05.cp) and issues four 128 x N x 64 block-scaled MMAs.
+//               steps, two accumulators; on tiles of more than 128 tokens each takes part of
+//               every step's tokens, one accumulator between them): per 256-K step a thread
+//               copies the scale factors into tensor memory (tcgen05.cp) and issues four
+//               128 x N x 64 block-scaled MMAs.
 //   warps 3-10: the epilogue: they move the accumulators out of tensor memory. In the fused path
 //               they first warm L2 with the CTA's A rows while the previous grid finishes and
 //               zero the staged bytes past K of a 1x32 block that K cuts. On the two-kernel path,
-//               when every step has a stage of its own, warp 3 is a third MMA issuer first.
+//               when every step has a stage of its own, warp 3 is a third MMA issuer first; when
+//               the ring refills (or steps are shared), warps 4-7 first write each stage's scale
+//               factors into tensor memory (tcgen05.st), so the MMA threads issue MMAs only.
 // In the fused path every warp first quantizes the staged slice into the token-block layout (the
 // pages' in-register A quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel`): the copy
 // and MMA warps have nothing else to do until those blocks exist.
