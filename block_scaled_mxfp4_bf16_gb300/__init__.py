@@ -47,7 +47,10 @@ class Mxfp4Error(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("splits", ctypes.c_int), ("m_tile", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("flags", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+
+
+GEMM_A_READY = 1   # mxfp4_gemm_options.flags: MXFP4_GEMM_A_READY
 
 
 def load_library() -> ctypes.CDLL:
@@ -157,8 +160,8 @@ def _out_bytes(t: torch.Tensor, shape: tuple, device: torch.device, name: str) -
         raise ValueError(f"{name} must be a contiguous uint8 tensor of shape {list(shape)} on {device}")
 
 
-def _opts(path: int, splits: int, m_tile: int = 0):
-    return ctypes.byref(_Options(path, splits, m_tile))
+def _opts(path: int, splits: int, m_tile: int = 0, flags: int = 0):
+    return ctypes.byref(_Options(path, splits, m_tile, flags))
 
 
 def mxfp4_version() -> int:
@@ -344,7 +347,7 @@ def _workspace(device: torch.device, nbytes: int, stream, st: int) -> torch.Tens
     return ws
 
 
-def _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile) -> tuple:
+def _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile, a_ready=False) -> tuple:
     """(C, the checked arguments of one mxfp4_gemm_ex call in C order)."""
     L = load_library()
     _dev(a, "a")
@@ -369,16 +372,20 @@ def _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile) 
         workspace = _workspace(dev, need, stream, st) if need else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    opts = _opts(path, splits, m_tile) if (path or splits or m_tile) else None   # NULL: automatic plan
+    flags = GEMM_A_READY if a_ready else 0
+    # NULL: the automatic plan without flags
+    opts = _opts(path, splits, m_tile, flags) if (path or splits or m_tile or flags) else None
     return c, (a.data_ptr(), M, K, a.stride(0), packed_b.data_ptr(), N, c.data_ptr(), c.stride(0), ws_ptr, ws_bytes,
                opts, st), workspace
 
 
 def mxfp4_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
-               stream=None, m_tile: int = 0) -> torch.Tensor:
-    """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b."""
-    c, args, _ = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
+               stream=None, m_tile: int = 0, a_ready: bool = False) -> torch.Tensor:
+    """C [M, N] bf16 = MXFP4(a) . MXFP4(B)^T, `packed_b` from mxfp4_prepack_b. a_ready: the
+    caller guarantees MXFP4_GEMM_A_READY (every write to `a` finished before the operation just
+    before this call on the stream began to run), so the kernels read A without waiting for it."""
+    c, args, _ = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile, a_ready)
     _check(load_library().mxfp4_gemm_ex(*args), "mxfp4_gemm")
     return c
 
@@ -457,10 +464,10 @@ class PreparedCall:
 
 def prepare_gemm(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch.Tensor,
                  workspace: torch.Tensor | None = None, path: int = 0, splits: int = 0,
-                 stream=None, m_tile: int = 0) -> PreparedCall:
+                 stream=None, m_tile: int = 0, a_ready: bool = False) -> PreparedCall:
     """mxfp4_gemm prepared for repeated calls on the same buffers (see PreparedCall); `c` is
-    required, the other arguments are those of mxfp4_gemm."""
-    c, args, ws = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile)
+    required, the other arguments are those of mxfp4_gemm (a_ready holds for every run)."""
+    c, args, ws = _gemm_call_args(a, packed_b, N, c, workspace, path, splits, stream, m_tile, a_ready)
     return PreparedCall(load_library().mxfp4_call_create, args[:-1], args[-1], "mxfp4_call_create",
                         (a, packed_b, c, ws))
 

@@ -129,6 +129,7 @@ struct GemmArgs {
     uint32_t tmem_cols;
     int fused;
     int sf_stores;         // scale factors into tensor memory by epilogue warps (two-kernel path)
+    int a_ready;           // the fused path's A rows may be requested before the previous grid finishes
     int c_vec4;            // C rows allow 8-byte stores of 4 bf16 (ldc % 4 == 0, C 8-byte aligned)
     uint64_t wait_limit_ns;
 #ifdef MXFP4_TEST_HOOKS
@@ -146,6 +147,7 @@ struct ResidentArgs {
     int M, N, K;
     int m_tile, m_tiles, n_tiles, splits, k_atoms;
     int issuers;           // MMA-issuing warps: 2, or 3 (16-token tiles of at least three steps)
+    int a_ready;           // A may be loaded before the previous grid has finished (caller's guarantee)
     uint32_t a_block;      // bytes of one token block
     uint32_t off_a, off_recv, off_bar;   // shared-memory offsets from the 1 KB-aligned base
     uint32_t tmem_cols;
@@ -200,8 +202,10 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* q,
                             uint8_t* scales, cudaStream_t s);
 // Token blocks for the GEMM, [m_tiles][k_atoms][a_block]; rows past `rows` and K past `K` zeroed.
+// a_ready: x may be read before the previous grid finishes (the stores still wait for it).
 cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* blocks,
-                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s);
+                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, bool a_ready,
+                                   cudaStream_t s);
 // bf16 rows [rows, K] at row stride lda (elements; 16-byte aligned rows, K % 8 == 0) from
 // device-accessible host memory -> packed device rows [rows, K]; PDL-chained (see the kernel).
 // early: read src before waiting for the previous grid (the caller declared it host-written only)

@@ -446,7 +446,7 @@ static int check_gemm_args(const void* a, int64_t M, int64_t K, int64_t lda, con
 // quantize_a = false: the two-kernel plan's token blocks are already in `ws` (the GEMM alone).
 static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, int64_t M, int64_t K, int64_t lda,
                     const void* packed_b, int64_t N, void* c, int64_t ldc, uint8_t* ws, cudaStream_t s,
-                    bool quantize_a = true) {
+                    bool quantize_a = true, bool a_ready = false) {
     if (plan.path == 3) {
         ResidentArgs r = {};
         r.a = static_cast<const uint16_t*>(a);
@@ -464,6 +464,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
         r.splits = plan.splits;
         r.k_atoms = plan.k_atoms;
         r.issuers = plan.issuers;
+        r.a_ready = a_ready ? 1 : 0;
         r.a_block = plan.a_block;
         r.off_a = plan.off_a;
         r.off_recv = plan.off_recv;
@@ -478,7 +479,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     }
     if (plan.path == 2 && quantize_a) {
         cudaError_t e = launch_quantize_blocks(static_cast<const uint16_t*>(a), M, K, lda, ws, plan.m_tile,
-                                               plan.m_tiles, plan.k_atoms, plan.a_block, s);
+                                               plan.m_tiles, plan.k_atoms, plan.a_block, a_ready, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     GemmArgs g = {};
@@ -512,6 +513,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
     g.tmem_cols = plan.tmem_cols;
     g.fused = plan.path == 1 ? 1 : 0;
     g.sf_stores = plan.sf_stores;
+    g.a_ready = a_ready ? 1 : 0;
     g.c_vec4 = (ldc % 4 == 0 && aligned(c, 8)) ? 1 : 0;
     g.wait_limit_ns = g_wait_limit_ns;
 #ifdef MXFP4_TEST_HOOKS
@@ -688,6 +690,7 @@ struct mxfp4_call {
     mxfp4::DeviceInfo di;
     mxfp4::GemmPlan plan;
     bool empty;              // M == 0 or N == 0: nothing to enqueue
+    bool a_ready;            // MXFP4_GEMM_A_READY
     // the GEMM itself
     const void* a;           // the device A the GEMM reads (a_dev for host buffers)
     int64_t M, K, lda, N;
@@ -714,7 +717,9 @@ static int resolve_device_call(const void* a, int64_t M, int64_t K, int64_t lda,
                                void* c, int64_t ldc, void* workspace, size_t ws_bytes,
                                const mxfp4_gemm_options* opts, mxfp4_call* call) {
     if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (opts && (opts->flags & ~MXFP4_GEMM_A_READY) != 0) return MXFP4_ERR_ARG;
     *call = mxfp4_call{};
+    call->a_ready = opts && (opts->flags & MXFP4_GEMM_A_READY) != 0;
     int st = check_gemm_args(a, M, K, lda, packed_b, N, c, ldc);
     if (st != MXFP4_OK) return st;
     call->empty = M == 0 || N == 0;
@@ -800,7 +805,7 @@ static int run_call(const mxfp4_call& call, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_fail(e);
     }
     const int st = run_gemm(call.plan, call.di, call.a, call.M, call.K, call.lda, call.packed_b, call.N, call.c,
-                            call.ldc, call.ws, s);
+                            call.ldc, call.ws, s, true, call.a_ready);
     if (st != MXFP4_OK || !call.c_host) return st;
     e = call.c_host_ld == call.N
             ? cudaMemcpyAsync(call.c_host, call.c_dev, c_row * call.M, cudaMemcpyDeviceToHost, s)
@@ -944,7 +949,7 @@ int mxfp4_quantize_tokens(const void* a, int64_t M, int64_t K, int64_t lda, int 
     const uint32_t a_block = static_cast<uint32_t>(mt) * 128u + static_cast<uint32_t>(nmc) * 2u * kSfChunk;
     cudaError_t e = launch_quantize_blocks(static_cast<const uint16_t*>(a), M, K, lda, static_cast<uint8_t*>(blocks),
                                            mt, static_cast<int>(cdiv(M, mt)), static_cast<int>(cdiv(K, kAtomK)),
-                                           a_block, static_cast<cudaStream_t>(stream));
+                                           a_block, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MXFP4_OK : cuda_fail(e);
 }
 

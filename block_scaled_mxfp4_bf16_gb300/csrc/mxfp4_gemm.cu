@@ -386,9 +386,24 @@ mxfp4_gemm_kernel(const GemmArgs p) {
     if (warp == 0) {
         // The weight ring's first stages go before the dependency wait (the weights never depend
         // on the previous grid). In the fused path only two: the A slice is the first thing the
-        // CTA needs once the wait returns, and copies leave in issue order.
+        // CTA needs once the wait returns, and copies leave in issue order. When the caller has
+        // declared A ready before the launch (a_ready), the fused path requests the A slice first
+        // and the whole prologue before the wait.
         const uint64_t pol_b = policy_evict_first();
-        const int nfirst = fused ? min(npro, 2) : npro;
+        const bool a_early = fused && p.a_ready;
+        auto load_a_slice = [&]() {
+            // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip, one
+            // row per lane so that the rows' copies are issued together
+            const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
+            const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
+            if (lane == 0) mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
+            __syncwarp();
+            for (int r = lane; r < m_valid; r += 32)
+                bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw, policy_evict_last());
+            __syncwarp();
+        };
+        if (a_early) load_a_slice();
+        const int nfirst = fused && !a_early ? min(npro, 2) : npro;
         if (lane == 0) {
             for (int j = 0; j < nfirst; ++j) {
                 mbar_arrive_expect_tx(&full[j], tx_bytes);
@@ -399,15 +414,7 @@ mxfp4_gemm_kernel(const GemmArgs p) {
         pdl_wait_prior_grid();   // A and the token blocks may be written by the previous grid
         MXFP4_PHASE(2);
         if (fused) {
-            // the whole bf16 slice A[m0 .. m0+m_valid, a0*256 .. +kslice] in one round trip, one
-            // row per lane so that the rows' copies are issued together
-            const uint32_t row_bytes = static_cast<uint32_t>(kslice) * 2u;
-            const uint16_t* arow = p.a + static_cast<int64_t>(m0) * p.lda + a0 * kAtomK;
-            if (lane == 0) mbar_arrive_expect_tx(a_raw, row_bytes * static_cast<uint32_t>(m_valid));
-            __syncwarp();
-            for (int r = lane; r < m_valid; r += 32)
-                bulk_load(smem + p.off_araw + r * raw_row, arow + r * p.lda, row_bytes, a_raw, policy_evict_last());
-            __syncwarp();
+            if (!a_early) load_a_slice();
             if (lane == 0) {
                 for (int j = nfirst; j < npro; ++j) {
                     mbar_arrive_expect_tx(&full[j], tx_bytes);

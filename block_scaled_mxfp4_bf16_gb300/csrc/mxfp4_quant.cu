@@ -50,7 +50,7 @@ template <bool kNarrow>
 __global__ void __launch_bounds__(256)
 quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                        uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block,
-                       FastDiv fd_row, FastDiv fd_mtile) {
+                       FastDiv fd_row, FastDiv fd_mtile, int a_ready) {
     pdl_launch_dependents();
     const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
@@ -60,7 +60,9 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
         const int64_t r = div_items<kNarrow>(it0, row_items, fd_row), kbp = it0 - r * row_items;
         if (it0 < items && r < rows && kbp < nblk) prefetch_l2(x + r * ld + kbp * 32);
     }
-    pdl_wait_prior_grid();
+    // x may come from the previous grid, which may also still read `blocks`: wait before the
+    // first load -- or, when the caller declared A ready, only before the first store
+    if (!a_ready) pdl_wait_prior_grid();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int lane = threadIdx.x & 31;
     // the loop bound is uniform per warp (warps start at multiples of 32) so the shuffles below
@@ -80,6 +82,7 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
         uint32_t word = byte << (8 * (lane & 3));
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (a_ready) pdl_wait_prior_grid();
         if (in_range) {
             const int mt = static_cast<int>(div_items<kNarrow>(r, m_tile, fd_mtile));
             const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
@@ -104,7 +107,7 @@ quantize_blocks_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, 
 __global__ void __launch_bounds__(256)
 quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
                         uint8_t* __restrict__ blocks, int m_tile, int m_tiles, int k_atoms, uint32_t a_block,
-                        FastDiv fd_row, FastDiv fd_mtile) {
+                        FastDiv fd_row, FastDiv fd_mtile, int a_ready) {
     pdl_launch_dependents();
     const int64_t nblk = (K + 31) / 32;
     const int64_t row_items = 8 * static_cast<int64_t>(k_atoms);
@@ -118,7 +121,7 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
         const int64_t r = fast_div(static_cast<uint32_t>(it0), fd_row), kbp = it0 - r * row_items;
         if (it0 < items && r < rows && kbp * 32 + part * 8 < K) prefetch_l2(x + r * ld + kbp * 32 + part * 8);
     }
-    pdl_wait_prior_grid();
+    if (!a_ready) pdl_wait_prior_grid();   // as in quantize_blocks_kernel
     // the loop bound is uniform per warp, so the shuffles below always see all 32 lanes
     for (int64_t base = warp_id * 8; base < items; base += warps * 8) {
         const int64_t it = base + (lane >> 2);
@@ -147,6 +150,7 @@ quantize_blocks4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
         const uint32_t rr = static_cast<uint32_t>(r - static_cast<int64_t>(mt) * m_tile);
         const uint32_t c = static_cast<uint32_t>(kbp & 7);
         uint8_t* blk = blocks + (static_cast<size_t>(mt) * k_atoms + static_cast<size_t>(kbp >> 3)) * a_block;
+        if (a_ready) pdl_wait_prior_grid();
         *reinterpret_cast<uint32_t*>(blk + swz_chunk_offset(rr, c) + part * 4) = codes;
         if ((lane & 15) == 0)
             *reinterpret_cast<uint32_t*>(blk + static_cast<uint32_t>(m_tile) * 128u + block_sf_offset(rr, c)) = word;
@@ -222,7 +226,9 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t 
 }
 
 cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* blocks,
-                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, cudaStream_t s) {
+                                   int m_tile, int m_tiles, int k_atoms, uint32_t a_block, bool a_ready,
+                                   cudaStream_t s) {
+    const int ready = a_ready ? 1 : 0;
     const int threads = 256;
     const int64_t items = static_cast<int64_t>(m_tiles) * m_tile * 8 * k_atoms;
     // few blocks: four lanes each (shorter chains, the launch is latency-bound); many blocks: one
@@ -231,7 +237,7 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
     const FastDiv fd_mtile = make_fastdiv(static_cast<uint32_t>(m_tile));
     if (items <= kQuantFourLaneMaxBlocks)
         return launch_pdl(quantize_blocks4_kernel, dim3(grid_for(items * 4, threads)), dim3(threads), 0, s, x, rows,
-                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile, ready);
     // One lane per block in 128-thread blocks: more, smaller blocks than 256-thread ones shorten
     // the launch's tail (256x4096x7168 11.85 -> 11.65 us per call, 512x4096x7168 14.23 -> 13.60;
     // the four-lane kernel above measured mixed with 128 threads and keeps 256).
@@ -240,9 +246,9 @@ cudaError_t launch_quantize_blocks(const uint16_t* x, int64_t rows, int64_t K, i
     const int64_t span = items + static_cast<int64_t>(grid_for(items, threads1)) * threads1;
     if (span <= static_cast<int64_t>(UINT32_MAX))
         return launch_pdl(quantize_blocks_kernel<true>, dim3(grid_for(items, threads1)), dim3(threads1), 0, s, x, rows,
-                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+                          K, ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile, ready);
     return launch_pdl(quantize_blocks_kernel<false>, dim3(grid_for(items, threads1)), dim3(threads1), 0, s, x, rows, K,
-                      ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile);
+                      ld, blocks, m_tile, m_tiles, k_atoms, a_block, fd_row, fd_mtile, ready);
 }
 
 cudaError_t launch_stage_rows(const void* src, int64_t lda, void* dst, int64_t rows, int64_t K, bool early,

@@ -170,8 +170,22 @@ typedef struct {
                     2 = standalone quantize kernel into the workspace, then the GEMM */
     int splits;  /* 0 = automatic, else the number of K slices per output tile (>= 1) */
     int m_tile;  /* 0 = automatic, else tokens per tile: a multiple of 16 in [16, 256] */
-    int reserved[5];
+    int flags;   /* 0, or MXFP4_GEMM_A_READY (below); other bits: MXFP4_ERR_ARG */
+    int reserved[4];
 } mxfp4_gemm_options;
+
+/* MXFP4_GEMM_A_READY -- the caller guarantees that every write to A was made by work that had
+ * finished before the operation enqueued just before this call on the stream began to run. The
+ * call's kernels may start as soon as that operation starts (they are launched as programmatic
+ * dependents, and the calls of this library let their dependents start early), so A must not be
+ * written by that operation nor by anything still running when it starts. Typical use: the
+ * second and later of several calls that read the same A (projections of one activation,
+ * experts on one gathered batch), when the first of them follows A's producer and that producer
+ * is an ordinary kernel or copy. Not valid for A written by the call just before, nor for the C
+ * of a call of this library whose successor is the first reader. With the flag the call loads
+ * and quantizes A as soon as its kernels start, overlapping the work before it; it still writes
+ * nothing (C, workspace) before that work has finished. Results are the same bits either way. */
+#define MXFP4_GEMM_A_READY 1
 
 /* mxfp4_gemm with an explicit plan. The workspace must be at least
  * mxfp4_gemm_workspace_size_ex(M, N, K, opts). opts == NULL is the automatic plan. */

@@ -114,3 +114,27 @@ def test_prepared_call_null_checks(lib):
     # a null A is refused by the argument checks and leaves no handle behind
     assert lib.mxfp4_call_create(None, 8, 512, 512, None, 256, None, 256, None, 0, None, ctypes.byref(out)) == 1
     assert out.value is None
+
+
+def test_gemm_options_flags_are_checked_first(lib):
+    # mxfp4_gemm_options is {path, splits, m_tile, flags, reserved[4]}; a flag bit other than
+    # MXFP4_GEMM_A_READY is an argument error found before any device query, while the known
+    # bit passes the argument checks (and the call then fails only for want of a device)
+    import torch
+    import block_scaled_mxfp4_bf16_gb300 as mx
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert ctypes.sizeof(mx._Options) == 32 and mx._Options.flags.offset == 12
+    assert "#define MXFP4_GEMM_A_READY 1" in open(HEADER).read() and mx.GEMM_A_READY == 1
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.mxfp4_gemm_ex.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, ctypes.c_size_t, vp, vp]
+    lib.mxfp4_gemm_ex.restype = ctypes.c_int
+    big = ctypes.create_string_buffer(8192)
+    q = ctypes.addressof(big) + (-ctypes.addressof(big)) % 1024
+    before = big.raw
+    for flags, refused in ((2, True), (1 << 30, True), (3, True), (1, False), (0, False)):
+        opts = mx._Options(0, 0, 0, flags)
+        st = lib.mxfp4_gemm_ex(q, 1, 64, 64, q, 16, q + 2048, 16, q + 4096, 4096, ctypes.byref(opts), None)
+        assert (st == 1) == refused, (flags, st)
+        assert st != 0
+    assert big.raw == before

@@ -84,6 +84,17 @@ def test_gemm_passes_pointers_sizes_and_strides(lib):
     assert args[8] is None and args[9] == 0 and args[10] is None   # no workspace, automatic plan
 
 
+def test_gemm_a_ready_sets_the_options_flag(lib):
+    # a_ready is MXFP4_GEMM_A_READY in the options; alone it keeps the automatic plan (zeros)
+    a, packed, N = _gemm_operands()
+    mx.mxfp4_gemm(a, packed, N, stream=0, a_ready=True)
+    mx.mxfp4_gemm(a, packed, N, stream=0, path=2, splits=3, a_ready=True)
+    mx.prepare_gemm(a, packed, N, dev(torch.zeros(8, N, dtype=torch.bfloat16)), stream=0, a_ready=True)
+    seen = [(o.path, o.splits, o.m_tile, o.flags, list(o.reserved))
+            for o in (lib.calls[0][1][10]._obj, lib.calls[1][1][10]._obj, lib.calls[2][1][10]._obj)]
+    assert seen == [(0, 0, 0, 1, [0] * 4), (2, 3, 0, 1, [0] * 4), (0, 0, 0, 1, [0] * 4)]
+    assert lib.calls[2][0] == "mxfp4_call_create"
+
 def test_gemm_refuses_buffers_before_any_call(lib):
     a, packed, N = _gemm_operands()
     with pytest.raises(ValueError):   # packed weights too small

@@ -420,6 +420,40 @@ def test_prepared_calls_every_plan(M, N, K, path, splits, m_tile):
     assert mx.mxfp4_device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
+    (8, 2112, 7168, 0, 0, 0),        # weight-resident, six K slices
+    (16, 3072, 1536, 0, 0, 0),       # weight-resident, three K slices
+    (5, 300, 520, 1, 2, 0),          # fused, K tail
+    (64, 7168, 2048, 0, 0, 0),       # two-kernel, four-lane quantizer
+    (300, 384, 1536, 2, 1, 192),     # two-kernel, one-lane quantizer, wide token tile
+])
+def test_a_ready_gives_the_same_bits(M, N, K, path, splits, m_tile):
+    # MXFP4_GEMM_A_READY used as its contract allows: A rewritten by an ordinary copy, read by a
+    # call without the flag, then by calls with it (their predecessor began after the copy had
+    # finished). Each seed rewrites A, so a flagged call that read A too early would see the
+    # previous seed's values. Every call gives the bits of the plain call, plain and prepared.
+    mx = _mx()
+    bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=M + 11).cuda())
+    packed = mx.mxfp4_prepack_b(bq, bs)
+    a = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    kw = dict(path=path, splits=splits, m_tile=m_tile)
+    prepared = mx.prepare_gemm(a, packed, N, outs[3], a_ready=True, **kw)
+    xs = [workloads.random_bf16(M, K, seed=s).cuda() for s in (21, 22, 23)]
+    wants = [mx.mxfp4_gemm(x, packed, N, **kw) for x in xs]
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for x, want in zip(xs, wants):
+            a.copy_(x)
+            mx.mxfp4_gemm(a, packed, N, c=outs[0], **kw)
+            mx.mxfp4_gemm(a, packed, N, c=outs[1], a_ready=True, **kw)
+            mx.mxfp4_gemm(a, packed, N, c=outs[2], a_ready=True, **kw)
+            prepared()
+            torch.cuda.synchronize()
+            for i, c in enumerate(outs):
+                assert torch.equal(c.view(torch.int16), want.view(torch.int16)), (rep, i)
+    assert mx.mxfp4_device_status() == 0
+
 def test_prepared_host_calls_chain_through_host_memory():
     # C of one prepared host call is A of the next (K == N): the second call's staging must read
     # the first call's C only once it is complete
