@@ -15,7 +15,7 @@
 //   warp 0    : copy producer -- weight blocks (17 KB), the fused path's bf16 A slice (one
 //               bulk copy per row) or the two-kernel path's token blocks. The first weight
 //               stages are requested before the CTA waits on the previous grid (the weights never
-//               depend on it).
+//               depend on it); when the caller declared A ready, the fused path's A rows too.
 //   warps 1-2 : tensor-memory allocation (warp 1) and two MMA-issuing threads (alternate 256-K
 //               steps, two accumulators; on tiles of more than 128 tokens each takes part of
 //               every step's tokens, one accumulator between them): per 256-K step a thread

@@ -8,8 +8,9 @@
 // bulk copy each) the moment it starts, before it waits for the previous grid: the weights
 // never depend on it. After that wait:
 //   warps 0, 3..11: each thread loads its 1x32 blocks of bf16 A straight from global memory
-//                   into registers (the addresses are computed, and the lines prefetched into
-//                   L2, before the wait), quantizes them (the pages' in-register A
+//                   into registers (the addresses are computed, and on short slices the lines
+//                   prefetched into L2, before the wait; on short slices whose caller declared
+//                   A ready the loads themselves go first), quantizes them (the pages' in-register A
 //                   quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel` with
 //                   `_mxfp4_quant_tile`) and writes the token blocks into shared memory;
 //   warps 1, 2:     warp 1 allocates tensor memory; lane 0 of each copies its 256-K steps' weight
