@@ -1,5 +1,6 @@
 """Seeded random shapes through the plan knobs (path, K slices, token tile, row strides) against
-the fp64 oracle: B's bytes bit-exact, C within the tolerance, nothing written outside C. The cases
+the fp64 oracle: B's bytes bit-exact, C within the tolerance, nothing written outside C, and the
+same bits again with A declared ready (MXFP4_GEMM_A_READY). The cases
 are drawn once from a fixed seed, so a failure names a reproducible shape."""
 import numpy as np
 import pytest
@@ -35,7 +36,8 @@ def _cases(n: int = 80, seed: int = 20261203):
 def test_random_shape_vs_oracle(M, N, K, path, splits, m_tile, lda_pad, ldc_pad):
     a = workloads.random_bf16(M, K, seed=M * 7919 + K)
     b = workloads.random_bf16(N, K, seed=N * 104729 + K, scale=0.5)
-    c, bq, bs = run_gemm(a, b, path=path, splits=splits, lda_pad=lda_pad, ldc_pad=ldc_pad, m_tile=m_tile)
+    c, bq, bs = run_gemm(a, b, path=path, splits=splits, lda_pad=lda_pad, ldc_pad=ldc_pad, m_tile=m_tile,
+                         also_a_ready=True)
     rq, rs = oracle.quantize(workloads.bf16_bits(b))
     assert_bytes_equal(bq, rq, "B e2m1")
     assert_bytes_equal(bs, rs, "B scales")
@@ -63,5 +65,6 @@ def _wide_cases(n: int = 24, seed: int = 20261204):
 def test_random_refilled_and_wide_tiles_vs_oracle(M, N, K, splits, m_tile, lda_pad, ldc_pad):
     a = workloads.random_bf16(M, K, seed=M * 31 + K)
     b = workloads.random_bf16(N, K, seed=N * 37 + K, scale=0.5)
-    c, bq, bs = run_gemm(a, b, path=2, splits=splits, lda_pad=lda_pad, ldc_pad=ldc_pad, m_tile=m_tile)
+    c, bq, bs = run_gemm(a, b, path=2, splits=splits, lda_pad=lda_pad, ldc_pad=ldc_pad, m_tile=m_tile,
+                         also_a_ready=True)
     check_tolerance(c, oracle_c(a, bq, bs), f"{M}x{N}x{K} two-kernel splits {splits} m_tile {m_tile}")
