@@ -546,23 +546,26 @@ def mxfp4_gemm_noalloc(a: torch.Tensor, packed_b: torch.Tensor, N: int, c: torch
 
 
 _PLAN_FIELDS = ("path", "splits", "m_tile", "ctas", "stages", "issuers", "reduction", "recv_dedicated",
-                "smem_bytes", "tmem_cols", "scale_stores")
+                "smem_bytes", "tmem_cols", "scale_stores", "a_early")
 
 
 class _PlanInfo(ctypes.Structure):
-    _fields_ = [(name, ctypes.c_int) for name in _PLAN_FIELDS] + [("reserved", ctypes.c_int * 5)]
+    _fields_ = [(name, ctypes.c_int) for name in _PLAN_FIELDS] + [("reserved", ctypes.c_int * 4)]
 
 
-def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0) -> dict:
-    """The plan mxfp4_gemm would run, as a dict of the mxfp4_plan_info fields."""
+def mxfp4_gemm_plan(M: int, N: int, K: int, path: int = 0, splits: int = 0, m_tile: int = 0,
+                    a_ready: bool = False) -> dict:
+    """The plan mxfp4_gemm would run (with a_ready: the plan of a call that declares A ready), as
+    a dict of the mxfp4_plan_info fields."""
     L = load_library()
     info = _PlanInfo()
-    _check(L.mxfp4_gemm_plan_info(M, N, K, _opts(path, splits, m_tile), ctypes.byref(info)), "mxfp4_gemm_plan_info")
+    _check(L.mxfp4_gemm_plan_info(M, N, K, _opts(path, splits, m_tile, GEMM_A_READY if a_ready else 0),
+                                  ctypes.byref(info)), "mxfp4_gemm_plan_info")
     return {name: getattr(info, name) for name in _PLAN_FIELDS}
 
 
 def mxfp4_gemm_plan_model(M: int, N: int, K: int, sm_count: int, cluster_caps=None, path: int = 0,
-                          splits: int = 0, m_tile: int = 0) -> dict:
+                          splits: int = 0, m_tile: int = 0, a_ready: bool = False) -> dict:
     """The planner alone for a described device (no GPU needed): `cluster_caps` lists, for cluster
     sizes 1..16, how many clusters can be resident at once (None: no limit)."""
     L = load_library()
@@ -570,7 +573,8 @@ def mxfp4_gemm_plan_model(M: int, N: int, K: int, sm_count: int, cluster_caps=No
     caps = None
     if cluster_caps is not None:
         caps = (ctypes.c_int * 17)(0, *[int(c) for c in cluster_caps])
-    _check(L.mxfp4_gemm_plan_model(M, N, K, _opts(path, splits, m_tile), sm_count, caps, ctypes.byref(info)),
+    _check(L.mxfp4_gemm_plan_model(M, N, K, _opts(path, splits, m_tile, GEMM_A_READY if a_ready else 0), sm_count,
+                                   caps, ctypes.byref(info)),
            "mxfp4_gemm_plan_model")
     return {name: getattr(info, name) for name in _PLAN_FIELDS}
 

@@ -96,6 +96,8 @@ struct GemmPlan {
     int stages;
     int issuers;       // MMA-issuing threads (1 to 3); one accumulator each, or halves of one
     int sf_stores;     // two-kernel path: scale factors written into tensor memory by epilogue warps
+    int a_early;       // weight-resident path: A read before the dependency wait (the caller
+                       // declared it ready and the plan leaves the SM room for it)
     int ctas;
     uint32_t a_block;  // bytes of one token block
     // shared-memory layout (bytes from a 1 KB-aligned base): weight stages at 0, token blocks
@@ -147,7 +149,7 @@ struct ResidentArgs {
     int M, N, K;
     int m_tile, m_tiles, n_tiles, splits, k_atoms;
     int issuers;           // MMA-issuing warps: 2, or 3 (16-token tiles of at least three steps)
-    int a_ready;           // A may be loaded before the previous grid has finished (caller's guarantee)
+    int a_early;           // A loaded before the previous grid has finished (GemmPlan::a_early)
     uint32_t a_block;      // bytes of one token block
     uint32_t off_a, off_recv, off_bar;   // shared-memory offsets from the 1 KB-aligned base
     uint32_t tmem_cols;
@@ -169,8 +171,10 @@ struct DeviceInfo {
 int device_info(DeviceInfo* out);   // MXFP4_OK or an error status
 // cluster_caps: if not null, cluster_caps[s] (s = 1..kMaxSplits) is how many clusters of s CTAs
 // can be resident at once, used instead of asking the current device (no CUDA call is made).
+// a_ready: the caller declared A ready (MXFP4_GEMM_A_READY), which can change the weight-resident
+// plan (GemmPlan::a_early).
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
-              GemmPlan* plan, const int* cluster_caps = nullptr);
+              GemmPlan* plan, const int* cluster_caps = nullptr, bool a_ready = false);
 size_t packed_b_bytes(int64_t N, int64_t K);
 
 // Exact unsigned 32-bit division by a divisor fixed at launch: the round-up multiplier with one

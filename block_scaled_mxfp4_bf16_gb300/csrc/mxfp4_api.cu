@@ -237,8 +237,19 @@ static int plan_resident_layout(GemmPlan& p, bool one_per_sm) {
 //   * with split-K, shared memory is not padded, so the next call's CTAs start beside this
 //     call's and request their weights early (8x2112x7168: 4.00 -> 3.70 us); without it one CTA
 //     per SM measured faster (32x4096x512: 2.50 -> 2.38 us, 4x2880x512: 2.04 -> 1.91 us).
+// Whether the quantizing warps may load A before the dependency wait (a caller that declared A
+// ready): when two CTAs share an SM and their shared memory leaves the L1 cache less than a
+// 196 KB carve-out would, the early loads measured slower (8x2112x7168, six 112 KB slices:
+// 3.39 -> 3.74 us per call; 8x2112x5120, six 91 KB slices: 3.06 -> 2.91, but 3.14 -> 3.28 with
+// the same slices padded to 112 KB); with one CTA per SM they measured faster (the six 112 KB
+// slices padded past half the SM: 3.74 -> 3.50).
+static bool res_early_ok(const GemmPlan& q) {
+    const size_t per_cta = q.smem_bytes + 1024, sm_smem = 233472;
+    return 2 * per_cta > sm_smem || 2 * per_cta <= 196u * 1024u;
+}
+
 static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, int mtile_req, int sm_count,
-                              GemmPlan* P, const int* cluster_caps) {
+                              GemmPlan* P, const int* cluster_caps, bool a_ready) {
     GemmPlan p = {};
     p.path = 3;
     if (mtile_req != 0 && mtile_req != 16 && mtile_req != 32) return MXFP4_ERR_ARG;
@@ -254,6 +265,7 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
         p.splits = std::max(1, std::min({splits_req, p.k_atoms, kMaxSplits}));
         const int st = plan_resident_layout(p, p.splits == 1);
         if (st != MXFP4_OK) return st;
+        p.a_early = a_ready && res_early_ok(p) ? 1 : 0;
         *P = p;
         return MXFP4_OK;
     }
@@ -271,6 +283,28 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
         const int resident = cluster_caps ? cluster_caps[s] : active_clusters_resident(dev, s, q.smem_bytes);
         if (s == 1 || units <= resident) {
             if (s > 1 && (last = plan_resident_layout(q, false)) != MXFP4_OK) break;
+            q.a_early = a_ready && res_early_ok(q) ? 1 : 0;
+            if (a_ready && !q.a_early) {
+                // A declared ready but this plan's slices leave no room to read it early: the
+                // most slices whose CTAs fill at most half the SMs, one per SM, so that the next
+                // call's CTAs start on the other half, take their weights and quantize their A
+                // while this call runs (8x2112x7168: six slices 3.39 us per call, four slices on
+                // 68 SMs 2.83; 4x2112x7168 3.08 -> 2.82)
+                const int s_half = static_cast<int>(std::min<int64_t>(
+                    {static_cast<int64_t>(kAutoMaxSplits), std::max(1, p.k_atoms / 2),
+                     std::max<int64_t>(1, sm_count / 2 / std::max<int64_t>(1, units))}));
+                for (int s2 = std::min(s_half, s - 1); s2 >= 1; --s2) {
+                    GemmPlan h = p;
+                    h.splits = s2;
+                    if (units * s2 * 2 > sm_count || plan_resident_layout(h, true) != MXFP4_OK) break;
+                    const int res2 = cluster_caps ? cluster_caps[s2] : active_clusters_resident(dev, s2, h.smem_bytes);
+                    if (s2 == 1 || units <= res2) {
+                        h.a_early = 1;
+                        *P = h;
+                        return MXFP4_OK;
+                    }
+                }
+            }
             *P = q;
             return MXFP4_OK;
         }
@@ -293,11 +327,11 @@ static int token_tile(int64_t M, int64_t K, int mtile_req) {
 }
 
 int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int mtile_req, int sm_count,
-              GemmPlan* P, const int* cluster_caps) {
+              GemmPlan* P, const int* cluster_caps, bool a_ready) {
     GemmPlan p = {};
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_SHAPE;
     if (mtile_req < 0 || mtile_req > kMaxMTile || mtile_req % 16 != 0) return MXFP4_ERR_ARG;
-    if (path_req == 3) return make_resident_plan(M, N, K, splits_req, mtile_req, sm_count, P, cluster_caps);
+    if (path_req == 3) return make_resident_plan(M, N, K, splits_req, mtile_req, sm_count, P, cluster_caps, a_ready);
     p.m_tile = token_tile(M, K, mtile_req);
     p.nmc = (p.m_tile + 127) / 128;
     p.m_tiles = static_cast<int>(cdiv(M, p.m_tile));
@@ -310,7 +344,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
     // Up to 32 tokens the weight-resident kernel is the automatic choice wherever its K slices
     // fit (it measured faster than both other paths on every such workload).
     if (path_req == 0 && M <= 32 && mtile_req == 0 &&
-        make_resident_plan(M, N, K, splits_req, 0, sm_count, P, cluster_caps) == MXFP4_OK)
+        make_resident_plan(M, N, K, splits_req, 0, sm_count, P, cluster_caps, a_ready) == MXFP4_OK)
         return MXFP4_OK;
     // Fused quantization puts A's load and quantization on the GEMM's critical path (behind the
     // dependency wait), while the two-kernel path overlaps them with the weight prologue but adds
@@ -397,9 +431,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int path_req, int splits_req, int
 // a small per-thread table instead of running the planner on every call (about 0.5 us of host
 // time a call on the benchmark's workloads).
 static int cached_plan(const DeviceInfo& di, int64_t M, int64_t N, int64_t K, int path_req, int splits_req,
-                       int mtile_req, GemmPlan* P) {
+                       int mtile_req, GemmPlan* P, bool a_ready = false) {
     struct Entry {
         int device, path, splits, mtile;
+        bool a_ready;
         int64_t M, N, K;
         GemmPlan plan;
         bool used;
@@ -410,16 +445,16 @@ static int cached_plan(const DeviceInfo& di, int64_t M, int64_t N, int64_t K, in
     for (int i = 0; i < kEntries; ++i) {
         const Entry& e = table[i];
         if (e.used && e.M == M && e.N == N && e.K == K && e.device == di.device && e.path == path_req &&
-            e.splits == splits_req && e.mtile == mtile_req) {
+            e.splits == splits_req && e.mtile == mtile_req && e.a_ready == a_ready) {
             *P = e.plan;
             return MXFP4_OK;
         }
     }
-    const int st = make_plan(M, N, K, path_req, splits_req, mtile_req, di.sm_count, P);
+    const int st = make_plan(M, N, K, path_req, splits_req, mtile_req, di.sm_count, P, nullptr, a_ready);
     if (st != MXFP4_OK) return st;
     Entry& e = table[next];
     next = (next + 1) % kEntries;
-    e = Entry{di.device, path_req, splits_req, mtile_req, M, N, K, *P, true};
+    e = Entry{di.device, path_req, splits_req, mtile_req, a_ready, M, N, K, *P, true};
     return MXFP4_OK;
 }
 
@@ -464,7 +499,7 @@ static int run_gemm(const GemmPlan& plan, const DeviceInfo& di, const void* a, i
         r.splits = plan.splits;
         r.k_atoms = plan.k_atoms;
         r.issuers = plan.issuers;
-        r.a_ready = a_ready ? 1 : 0;
+        r.a_early = plan.a_early;
         r.a_block = plan.a_block;
         r.off_a = plan.off_a;
         r.off_recv = plan.off_recv;
@@ -529,6 +564,17 @@ using namespace mxfp4;
 
 // ====================================================================== C ABI
 
+// Options a call may not take: a negative override, a path out of range, or a flag bit other
+// than MXFP4_GEMM_A_READY.
+static bool bad_options(const mxfp4_gemm_options* o) {
+    return o && (o->path < 0 || o->path > 3 || o->splits < 0 || o->m_tile < 0 ||
+                 (o->flags & ~MXFP4_GEMM_A_READY) != 0);
+}
+
+static bool options_a_ready(const mxfp4_gemm_options* o) {
+    return o && (o->flags & MXFP4_GEMM_A_READY) != 0;
+}
+
 // The planner's decisions as the public mxfp4_plan_info.
 static void fill_plan_info(const mxfp4::GemmPlan& plan, mxfp4_plan_info* info) {
     using namespace mxfp4;
@@ -548,6 +594,7 @@ static void fill_plan_info(const mxfp4::GemmPlan& plan, mxfp4_plan_info* info) {
     out.smem_bytes = static_cast<int>(plan.smem_bytes);
     out.tmem_cols = static_cast<int>(plan.tmem_cols);
     out.scale_stores = plan.sf_stores;
+    out.a_early = plan.a_early;
     *info = out;
 }
 
@@ -569,7 +616,7 @@ const char* mxfp4_status_string(int status) {
 
 int mxfp4_last_cuda_error(void) { return t_last_cuda_error; }
 
-int mxfp4_version(void) { return 203; }
+int mxfp4_version(void) { return 204; }
 
 int mxfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld, void* q, void* scales, void* stream) {
     if (rows < 0 || K < 0) return MXFP4_ERR_ARG;
@@ -611,11 +658,12 @@ int mxfp4_prepack_b(const void* bq, const void* bs, int64_t N, int64_t K, void* 
 }
 
 size_t mxfp4_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* opts) {
-    if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0) return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0 || bad_options(opts)) return 0;
     DeviceInfo di;
     if (device_info(&di) != MXFP4_OK) return 0;
     GemmPlan plan;
-    if (cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan) != MXFP4_OK)
+    if (cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan,
+                    options_a_ready(opts)) != MXFP4_OK)
         return 0;
     return plan.ws_total;
 }
@@ -635,12 +683,13 @@ int mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_options* o
                     int* m_tile, int* ctas, int* stages) {
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (bad_options(opts)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
+    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan,
+                    options_a_ready(opts));
     if (st != MXFP4_OK) return st;
     if (path) *path = plan.path;
     if (splits) *splits = plan.splits;
@@ -654,12 +703,13 @@ int mxfp4_gemm_plan_info(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_optio
     if (!info) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (bad_options(opts)) return MXFP4_ERR_ARG;
     DeviceInfo di;
     int st = device_info(&di);
     if (st != MXFP4_OK) return st;
     GemmPlan plan;
-    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan);
+    st = cached_plan(di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0, &plan,
+                    options_a_ready(opts));
     if (st != MXFP4_OK) return st;
     fill_plan_info(plan, info);
     return MXFP4_OK;
@@ -670,12 +720,12 @@ int mxfp4_gemm_plan_model(int64_t M, int64_t N, int64_t K, const mxfp4_gemm_opti
     if (!info || sm_count < 1) return MXFP4_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_ARG;
     if (K % 8 != 0) return MXFP4_ERR_SHAPE;
-    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
+    if (bad_options(opts)) return MXFP4_ERR_ARG;
     int caps[kMaxSplits + 1];
     for (int s = 0; s <= kMaxSplits; ++s) caps[s] = cluster_caps ? cluster_caps[s] : (1 << 30);
     GemmPlan plan;
     const int st = make_plan(M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0,
-                             sm_count, &plan, caps);
+                             sm_count, &plan, caps, options_a_ready(opts));
     if (st != MXFP4_OK) return st;
     fill_plan_info(plan, info);
     return MXFP4_OK;
@@ -716,8 +766,7 @@ namespace mxfp4 {
 static int resolve_device_call(const void* a, int64_t M, int64_t K, int64_t lda, const void* packed_b, int64_t N,
                                void* c, int64_t ldc, void* workspace, size_t ws_bytes,
                                const mxfp4_gemm_options* opts, mxfp4_call* call) {
-    if (opts && (opts->path < 0 || opts->path > 3 || opts->splits < 0 || opts->m_tile < 0)) return MXFP4_ERR_ARG;
-    if (opts && (opts->flags & ~MXFP4_GEMM_A_READY) != 0) return MXFP4_ERR_ARG;
+    if (bad_options(opts)) return MXFP4_ERR_ARG;
     *call = mxfp4_call{};
     call->a_ready = opts && (opts->flags & MXFP4_GEMM_A_READY) != 0;
     int st = check_gemm_args(a, M, K, lda, packed_b, N, c, ldc);
@@ -727,7 +776,7 @@ static int resolve_device_call(const void* a, int64_t M, int64_t K, int64_t lda,
     st = device_info(&call->di);
     if (st != MXFP4_OK) return st;
     st = cached_plan(call->di, M, N, K, opts ? opts->path : 0, opts ? opts->splits : 0, opts ? opts->m_tile : 0,
-                     &call->plan);
+                     &call->plan, call->a_ready);
     if (st != MXFP4_OK) return st;
     if (call->plan.ws_total > 0) {
         if (!workspace || ws_bytes < call->plan.ws_total) return MXFP4_ERR_WORKSPACE;

@@ -9,8 +9,8 @@
 // never depend on it. After that wait:
 //   warps 0, 3..11: each thread loads its 1x32 blocks of bf16 A straight from global memory
 //                   into registers (the addresses are computed, and on short slices the lines
-//                   prefetched into L2, before the wait; on short slices whose caller declared
-//                   A ready the loads themselves go first), quantizes them (the pages' in-register A
+//                   prefetched into L2, before the wait; when the caller declared A ready and
+//                   the plan allows it, the loads themselves go first), quantizes them (the pages' in-register A
 //                   quantization, submission 711914 `mxfp4_gemm_fused_k512_kernel` with
 //                   `_mxfp4_quant_tile`) and writes the token blocks into shared memory;
 //   warps 1, 2:     warp 1 allocates tensor memory; lane 0 of each copies its 256-K steps' weight
@@ -198,12 +198,9 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
             if (it1.valid && it1.avail > 0) prefetch_l2(it1.src);
         }
         // A may be written by the previous grid, unless the caller declared it ready before the
-        // launch (the token blocks go to this CTA's shared memory only, and C is written after
-        // warp 1's wait). Read early only on slices of at most two 256-K steps, like the
-        // prefetch: on longer ones the early read measured slower per call in back-to-back
-        // calls (8x2112x7168 3.38 -> 3.73 us, 16x2112x7168 4.20 -> 4.36; 32x4096x512 2.38 ->
-        // 1.90, 16x3072x1536 2.90 -> 2.58)
-        if (!(p.a_ready && na <= 2)) pdl_wait_prior_grid();
+        // launch and the plan reads it early (a_early; the token blocks go to this CTA's shared
+        // memory only, and C is written after warp 1's wait)
+        if (!p.a_early) pdl_wait_prior_grid();
         if (threadIdx.x == 0) RES_PHASE(2);
         uint32_t w0[16], w1[16];
         if (it0.valid && it0.avail > 0) load_a_block(it0.src, it0.avail, w0);

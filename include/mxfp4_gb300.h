@@ -65,7 +65,8 @@ int mxfp4_last_cuda_error(void);
 /* Library ABI version (major*100 + minor). 2.01: K any multiple of 8 (was a multiple of 64).
  * 2.02: token-block entry points (mxfp4_quantize_tokens, mxfp4_gemm_tokens). 2.03: prepared
  * calls (mxfp4_call_create, mxfp4_call_create_host, mxfp4_call_run, mxfp4_call_destroy), the
- * scale_stores field of mxfp4_plan_info, mxfp4_gemm_unpacked. */
+ * scale_stores field of mxfp4_plan_info, mxfp4_gemm_unpacked. 2.04: mxfp4_gemm_options.flags
+ * (MXFP4_GEMM_A_READY) and mxfp4_plan_info.a_early. */
 int mxfp4_version(void);
 
 /*
@@ -184,7 +185,11 @@ typedef struct {
  * is an ordinary kernel or copy. Not valid for A written by the call just before, nor for the C
  * of a call of this library whose successor is the first reader. With the flag the call loads
  * and quantizes A as soon as its kernels start, overlapping the work before it; it still writes
- * nothing (C, workspace) before that work has finished. Results are the same bits either way. */
+ * nothing (C, workspace) before that work has finished. With an explicit plan (path and splits
+ * given) the results are the same bits either way. The automatic plan may differ with the flag
+ * (mxfp4_plan_info.a_early; on the weight-resident path, fewer K slices whose CTAs fill at most
+ * half the SMs, when the flagless plan leaves no room to read A early), and C then differs from
+ * the flagless call's only by the order of the split-K sum, within the same tolerance. */
 #define MXFP4_GEMM_A_READY 1
 
 /* mxfp4_gemm with an explicit plan. The workspace must be at least
@@ -356,7 +361,10 @@ typedef struct mxfp4_plan_info {
     int tmem_cols;       /* tensor-memory columns allocated per CTA */
     int scale_stores;    /* 1: epilogue warps write each stage's scale factors into tensor memory
                             (the tensor pipe then runs MMAs only); 0: the MMA threads copy them */
-    int reserved[5];
+    int a_early;         /* 1: the weight-resident kernel loads and quantizes A before waiting for
+                            the work ahead of it (only with MXFP4_GEMM_A_READY, on plans whose
+                            shared memory leaves the SM room for it) */
+    int reserved[4];
 } mxfp4_plan_info;
 
 /* The full plan mxfp4_gemm_ex would run on the current device (superset of mxfp4_gemm_plan).

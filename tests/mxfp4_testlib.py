@@ -55,8 +55,9 @@ def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: in
              ldc_pad: int = 0, canary: float = 777.0, m_tile: int = 0, also_a_ready: bool = False):
     """Quantize B and prepack it on the GPU, run mxfp4_gemm, check the B bytes against the
     oracle and that nothing outside C[:M,:N] was written. Returns (C as fp64 [M,N], Bq, Bs).
-    also_a_ready: run the call a second time with A declared ready (its predecessor, the first
-    call, began after A was written) into a second canaried C, which must hold the same bits."""
+    also_a_ready: run the call again with A declared ready (its predecessor began after A was
+    written) into a second canaried C, which must hold the bits of a flagless call on the plan
+    the flag selects (the automatic plan may differ with it)."""
     import block_scaled_mxfp4_bf16_gb300 as mx
     M, K = a_cpu.shape
     N = b_cpu.shape[0]
@@ -77,14 +78,16 @@ def run_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, path: int = 0, splits: in
     outside[:M, :N] = False
     assert bool((c_store[outside] == canary).all()), "GEMM wrote outside C"
     if also_a_ready:
+        rp = mx.mxfp4_gemm_plan(M, N, K, path, splits, m_tile, a_ready=True)
         c2_store = torch.full_like(c_store, canary)
-        c2 = c2_store[:M, :N]
-        mx.mxfp4_gemm(a, packed, N, c=c, path=path, splits=splits, m_tile=m_tile)
+        c3_store = torch.full_like(c_store, canary)
+        c2, c3 = c2_store[:M, :N], c3_store[:M, :N]
+        mx.mxfp4_gemm(a, packed, N, c=c3, path=rp["path"], splits=rp["splits"], m_tile=rp["m_tile"])
         mx.mxfp4_gemm(a, packed, N, c=c2, path=path, splits=splits, m_tile=m_tile, a_ready=True)
         torch.cuda.synchronize()
         assert mx.mxfp4_device_status() == 0
         assert bool((c2_store[outside] == canary).all()), "GEMM with A declared ready wrote outside C"
-        assert torch.equal(c2.view(torch.int16), c.view(torch.int16)), "A declared ready changed C"
+        assert torch.equal(c2.view(torch.int16), c3.view(torch.int16)), "A declared ready changed C"
     return bf16_to_f64(c.cpu()), to_np_u8(bq), to_np_u8(bs)
 
 

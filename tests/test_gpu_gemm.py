@@ -431,21 +431,24 @@ def test_a_ready_gives_the_same_bits(M, N, K, path, splits, m_tile):
     # MXFP4_GEMM_A_READY used as its contract allows: A rewritten by an ordinary copy, read by a
     # call without the flag, then by calls with it (their predecessor began after the copy had
     # finished). Each seed rewrites A, so a flagged call that read A too early would see the
-    # previous seed's values. Every call gives the bits of the plain call, plain and prepared.
+    # previous seed's values. Every call gives the bits of a flagless call on the plan the flag
+    # selects (the same plan, except where the automatic weight-resident plan changes with it).
     mx = _mx()
     bq, bs = mx.mxfp4_quantize(workloads.random_bf16(N, K, seed=M + 11).cuda())
     packed = mx.mxfp4_prepack_b(bq, bs)
     a = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
     outs = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     kw = dict(path=path, splits=splits, m_tile=m_tile)
+    rp = mx.mxfp4_gemm_plan(M, N, K, a_ready=True, **kw)
+    kw_plan = dict(path=rp["path"], splits=rp["splits"], m_tile=rp["m_tile"])
     prepared = mx.prepare_gemm(a, packed, N, outs[3], a_ready=True, **kw)
     xs = [workloads.random_bf16(M, K, seed=s).cuda() for s in (21, 22, 23)]
-    wants = [mx.mxfp4_gemm(x, packed, N, **kw) for x in xs]
+    wants = [mx.mxfp4_gemm(x, packed, N, **kw_plan) for x in xs]
     torch.cuda.synchronize()
     for rep in range(2):
         for x, want in zip(xs, wants):
             a.copy_(x)
-            mx.mxfp4_gemm(a, packed, N, c=outs[0], **kw)
+            mx.mxfp4_gemm(a, packed, N, c=outs[0], **kw_plan)
             mx.mxfp4_gemm(a, packed, N, c=outs[1], a_ready=True, **kw)
             mx.mxfp4_gemm(a, packed, N, c=outs[2], a_ready=True, **kw)
             prepared()

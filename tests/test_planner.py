@@ -143,3 +143,36 @@ def test_errors(mx):
         mx.mxfp4_gemm_plan_model(8, 2112, 7168, 0, CLUSTER_CAPS)
     with pytest.raises(m.Mxfp4Error):
         plan(mx, 8, 2112, 7168, m_tile=24)   # token tile must be a multiple of 16
+
+
+@pytest.mark.parametrize("M,N,K,plain_s,ready_s,ready_ctas,early", [
+    (8, 2112, 7168, 6, 4, 68, 1),    # six 112 KB slices leave no room: four slices on 68 SMs
+    (4, 2112, 7168, 6, 4, 68, 1),
+    (16, 2112, 7168, 6, 6, 102, 0),  # four slices would take four blocks of A per thread: it waits
+    (8, 4096, 5120, 4, 4, 128, 0),   # two slices would take ten steps each: it waits
+    (16, 3072, 1536, 3, 3, 72, 1),   # room to read A early: the same plan
+    (32, 4096, 512, 1, 1, 64, 1),
+    (8, 2112, 5120, 6, 6, 102, 1),
+])
+def test_plans_with_a_declared_ready(mx, M, N, K, plain_s, ready_s, ready_ctas, early):
+    # MXFP4_GEMM_A_READY: A is read before the dependency wait where two CTAs of 112 KB do not
+    # share an SM; where they would, the most slices whose CTAs fill at most half the SMs, one per
+    # SM, if the slices fit; otherwise the flagless plan, waiting as before
+    p = plan(mx, M, N, K)
+    r = plan(mx, M, N, K, a_ready=True)
+    assert p["path"] == 3 and p["splits"] == plain_s and p["a_early"] == 0
+    assert (r["path"], r["splits"], r["ctas"], r["a_early"]) == (3, ready_s, ready_ctas, early)
+    if r["splits"] != p["splits"]:
+        assert 2 * r["ctas"] <= SM_COUNT and 2 * (r["smem_bytes"] + 1024) > 233472
+
+
+def test_a_early_only_where_it_is_read(mx):
+    # the flag changes nothing on the streaming paths, and an explicit resident plan keeps its
+    # slices: it reads early only where the shared memory leaves room
+    for M, N, K in ((64, 7168, 2048), (256, 4096, 7168), (300, 384, 1536)):
+        assert plan(mx, M, N, K, a_ready=True) == plan(mx, M, N, K)
+    six = plan(mx, 8, 2112, 7168, path=3, splits=6, a_ready=True)
+    four = plan(mx, 8, 2112, 7168, path=3, splits=4, a_ready=True)
+    assert (six["splits"], six["a_early"]) == (6, 0)
+    assert (four["splits"], four["a_early"]) == (4, 1)
+    assert plan(mx, 8, 2112, 7168, path=3, splits=4)["a_early"] == 0
