@@ -208,7 +208,7 @@ def bench_workload(mx, w, steps: int, warmup: int, l2_bytes: int, soak_s: float 
     packs = [packed0] + [packed0.clone() for _ in range(copies - 1)]
     As = [a0] + [a0.clone() for _ in range(copies - 1)]
     Cs = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(copies)]
-    plan = mx.mxfp4_gemm_plan(w.M, w.N, w.K)
+    plan = mx.mxfp4_gemm_plan(w.M, w.N, w.K, a_ready=a_ready)
     ws = torch.empty(max(1, mx.mxfp4_gemm_workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=dev)
     side = torch.cuda.Stream()
 
@@ -562,6 +562,7 @@ def main():
                                    "fp4_frac": round(tf / fp4_peak, 4),
                                    "warm_l2_us_per_call": round(rw["us_per_call"], 3),
                                    "a_ready_steady_us_per_call": round(ra["us_per_call"], 3),
+                                   "a_ready_plan": {k: ra["plan"][k] for k in ("path", "splits", "ctas", "a_early")},
                                    "warm_l2_fp4_frac": round(tf_warm / fp4_peak, 4),
                                    "gemm_dram_bytes": traffic[0] if traffic else None,
                                    "quantizer_dram_bytes": traffic[1] if traffic else None,
