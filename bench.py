@@ -38,23 +38,23 @@ METRIC = "µs/call and TFLOPS (2MNK/t) per shape; % of HBM or FP4 tensor rooflin
 # Per workload: (GEMM launch bytes, standalone token-block quantizer launch bytes or None, source
 # hash, plan signature); from the per-configuration ncu capture in profiles/.
 MEASURED_TRAFFIC = {
-    "M16_N3072_K1536": (2594816, None, "2958f9d141f701c1",
+    "M16_N3072_K1536": (2594816, None, "1b5a93632b1fd20e",
                         "path=3,splits=3,m_tile=16,ctas=72,stages=2,issuers=2,reduction=4,recv_dedicated=1"),
-    "M8_N2112_K7168": (8441600, None, "2958f9d141f701c1",
+    "M8_N2112_K7168": (8439808, None, "1b5a93632b1fd20e",
                        "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M32_N4096_K512": (1185536, None, "2958f9d141f701c1",
+    "M32_N4096_K512": (1185536, None, "1b5a93632b1fd20e",
                        "path=3,splits=1,m_tile=16,ctas=64,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M64_N7168_K2048": (7941120, 271104, "c1979272286486f6",
+    "M64_N7168_K2048": (7940864, 270848, "8b89230104543f78",
                         "path=2,splits=1,m_tile=64,ctas=56,stages=8,issuers=3,reduction=0,recv_dedicated=0"),
-    "M256_N4096_K7168": (16640768, 3679488, "c1979272286486f6",
+    "M256_N4096_K7168": (16641024, 3679744, "8b89230104543f78",
                          "path=2,splits=2,m_tile=128,ctas=128,stages=6,issuers=2,reduction=3,recv_dedicated=0"),
-    "M4_N2880_K512": (843776, None, "2958f9d141f701c1",
+    "M4_N2880_K512": (843520, None, "1b5a93632b1fd20e",
                       "path=3,splits=1,m_tile=16,ctas=23,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M32_N2880_K512": (872192, None, "2958f9d141f701c1",
+    "M32_N2880_K512": (872192, None, "1b5a93632b1fd20e",
                        "path=3,splits=1,m_tile=16,ctas=46,stages=2,issuers=2,reduction=0,recv_dedicated=0"),
-    "M16_N2112_K7168": (8554240, None, "2958f9d141f701c1",
+    "M16_N2112_K7168": (8554240, None, "1b5a93632b1fd20e",
                         "path=3,splits=6,m_tile=16,ctas=102,stages=5,issuers=3,reduction=4,recv_dedicated=1"),
-    "M256_N3072_K1536": (2796032, 795392, "c1979272286486f6",
+    "M256_N3072_K1536": (2796800, 795136, "8b89230104543f78",
                          "path=2,splits=1,m_tile=64,ctas=96,stages=6,issuers=3,reduction=0,recv_dedicated=0"),
 }
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s the method's throughput target is stated against

@@ -77,6 +77,9 @@ constexpr int kResQuantThreads = kResThreads - 64;   // the other 10 quantize A
 constexpr int kResMaxAtoms = 8;
 constexpr int kResMaxMTile = 32;
 constexpr int kResMaxItemsPerThread = 2;   // 1x32 blocks of A per quantizing thread
+// ... on plans that read A before the dependency wait, where the A phase overlaps the call ahead
+// (a separate instantiation of the kernel, three blocks in flight per thread at a time)
+constexpr int kResManyItemsPerThread = 6;
 // Rows of the 128-row weight tile each cluster rank owns in the split-K reduction, and the
 // fp32 words one owned row takes per source in the receive buffer (tokens rounded up to 4).
 __host__ __device__ inline int res_rows_per_owner(int splits) { return (kTileN + splits - 1) / splits; }
@@ -98,6 +101,8 @@ struct GemmPlan {
     int sf_stores;     // two-kernel path: scale factors written into tensor memory by epilogue warps
     int a_early;       // weight-resident path: A read before the dependency wait (the caller
                        // declared it ready and the plan leaves the SM room for it)
+    int many_items;    // weight-resident path: more than kResMaxItemsPerThread blocks of A per
+                       // quantizing thread (only with a_early)
     int ctas;
     uint32_t a_block;  // bytes of one token block
     // shared-memory layout (bytes from a 1 KB-aligned base): weight stages at 0, token blocks

@@ -195,11 +195,14 @@ static int active_clusters_resident(int device, int size, size_t smem) {
 // count are set. one_per_sm pads shared memory so that no second CTA fits on an SM; otherwise a
 // CTA of the next call can start beside one of this call (and request its weights early).
 // MXFP4_ERR_SHAPE if the slice does not fit the kernel.
-static int plan_resident_layout(GemmPlan& p, bool one_per_sm) {
+// max_items: 1x32 blocks of A a quantizing thread may take (kResManyItemsPerThread only on plans
+// that read A before the dependency wait).
+static int plan_resident_layout(GemmPlan& p, bool one_per_sm, int max_items = kResMaxItemsPerThread) {
     p.atoms_max = static_cast<int>(cdiv(p.k_atoms, p.splits));
     if (p.atoms_max > kResMaxAtoms) return MXFP4_ERR_SHAPE;
-    if (static_cast<int64_t>(p.raw_rows) * p.atoms_max * 8 > static_cast<int64_t>(kResQuantThreads) * kResMaxItemsPerThread)
-        return MXFP4_ERR_SHAPE;                   // at most two 1x32 blocks of A per thread
+    const int64_t blocks = static_cast<int64_t>(p.raw_rows) * p.atoms_max * 8;
+    if (blocks > static_cast<int64_t>(kResQuantThreads) * max_items) return MXFP4_ERR_SHAPE;
+    p.many_items = blocks > static_cast<int64_t>(kResQuantThreads) * kResMaxItemsPerThread ? 1 : 0;
     p.nmc = 1;
     p.a_block = static_cast<uint32_t>(p.m_tile) * 128u + 2u * kSfChunk;
     p.stages = p.atoms_max;
@@ -263,7 +266,10 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
     if (units * kMaxSplits > (int64_t(1) << 31) - 1) return MXFP4_ERR_SHAPE;
     if (splits_req > 0) {
         p.splits = std::max(1, std::min({splits_req, p.k_atoms, kMaxSplits}));
-        const int st = plan_resident_layout(p, p.splits == 1);
+        int st = plan_resident_layout(p, p.splits == 1);
+        // a slice with more of A than two blocks per quantizing thread: the kernel variant that
+        // takes up to kResManyItemsPerThread (chosen automatically only where A is read early)
+        if (st != MXFP4_OK) st = plan_resident_layout(p, p.splits == 1, kResManyItemsPerThread);
         if (st != MXFP4_OK) return st;
         p.a_early = a_ready && res_early_ok(p) ? 1 : 0;
         *P = p;
@@ -274,6 +280,30 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
     const int s_max = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(kAutoMaxSplits),
                                                           std::max(1, p.k_atoms / 2),
                                                           std::max<int64_t>(1, sm_count / std::max<int64_t>(1, units))}));
+    // A declared ready but the flagless plan leaves no room to read it early (or there is no
+    // flagless plan): the most slices whose CTAs fill at most half the SMs, one per SM, so that
+    // the next call's CTAs start on the other half, take their weights and quantize their A while
+    // this call runs (8x2112x7168: six slices 3.39 us per call, four slices on 68 SMs 2.83;
+    // 4x2112x7168 3.08 -> 2.82). Its A phase overlaps the call ahead, so a quantizing thread may
+    // take up to kResManyItemsPerThread blocks.
+    auto side_by_side = [&](int s_below, GemmPlan* out) {
+        const int s_half = static_cast<int>(std::min<int64_t>(
+            {static_cast<int64_t>(kAutoMaxSplits), std::max(1, p.k_atoms / 2),
+             std::max<int64_t>(1, sm_count / 2 / std::max<int64_t>(1, units))}));
+        if (units * 2 > sm_count) return false;
+        for (int s2 = std::min(s_half, s_below); s2 >= 1; --s2) {
+            GemmPlan h = p;
+            h.splits = s2;
+            if (plan_resident_layout(h, true, kResManyItemsPerThread) != MXFP4_OK) return false;
+            const int res2 = cluster_caps ? cluster_caps[s2] : active_clusters_resident(dev, s2, h.smem_bytes);
+            if (s2 == 1 || units <= res2) {
+                h.a_early = 1;
+                *out = h;
+                return true;
+            }
+        }
+        return false;
+    };
     int last = MXFP4_ERR_SHAPE;
     for (int s = s_max; s >= 1; --s) {
         GemmPlan q = p;
@@ -284,31 +314,12 @@ static int make_resident_plan(int64_t M, int64_t N, int64_t K, int splits_req, i
         if (s == 1 || units <= resident) {
             if (s > 1 && (last = plan_resident_layout(q, false)) != MXFP4_OK) break;
             q.a_early = a_ready && res_early_ok(q) ? 1 : 0;
-            if (a_ready && !q.a_early) {
-                // A declared ready but this plan's slices leave no room to read it early: the
-                // most slices whose CTAs fill at most half the SMs, one per SM, so that the next
-                // call's CTAs start on the other half, take their weights and quantize their A
-                // while this call runs (8x2112x7168: six slices 3.39 us per call, four slices on
-                // 68 SMs 2.83; 4x2112x7168 3.08 -> 2.82)
-                const int s_half = static_cast<int>(std::min<int64_t>(
-                    {static_cast<int64_t>(kAutoMaxSplits), std::max(1, p.k_atoms / 2),
-                     std::max<int64_t>(1, sm_count / 2 / std::max<int64_t>(1, units))}));
-                for (int s2 = std::min(s_half, s - 1); s2 >= 1; --s2) {
-                    GemmPlan h = p;
-                    h.splits = s2;
-                    if (units * s2 * 2 > sm_count || plan_resident_layout(h, true) != MXFP4_OK) break;
-                    const int res2 = cluster_caps ? cluster_caps[s2] : active_clusters_resident(dev, s2, h.smem_bytes);
-                    if (s2 == 1 || units <= res2) {
-                        h.a_early = 1;
-                        *P = h;
-                        return MXFP4_OK;
-                    }
-                }
-            }
+            if (a_ready && !q.a_early && side_by_side(s - 1, P)) return MXFP4_OK;
             *P = q;
             return MXFP4_OK;
         }
     }
+    if (a_ready && side_by_side(s_max, P)) return MXFP4_OK;
     return last;
 }
 

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "internal.h"
@@ -106,6 +107,9 @@ __device__ __forceinline__ void quantize_item(const AItem& it, const uint32_t (&
 
 }  // namespace
 
+// kMany: up to kResManyItemsPerThread blocks of A per quantizing thread, loaded three at a time
+// (plans that read A before the dependency wait); otherwise at most two, all loaded at once.
+template <bool kMany>
 __global__ void __launch_bounds__(kResThreads, 1)
 mxfp4_gemm_resident_kernel(const ResidentArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -187,6 +191,24 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         const int nb8 = na * 8;                       // 1x32 blocks of the slice per token row
         const int items = m_valid * nb8;
         const uint32_t a_rows = static_cast<uint32_t>(p.m_tile) * 128u;
+        if constexpr (kMany) {
+            // every block of the slice from this CTA's A rows, three per thread at a time
+            if (!p.a_early) pdl_wait_prior_grid();   // (the planner pairs kMany with a_early)
+            if (threadIdx.x == 0) RES_PHASE(2);
+            for (int b = qt; b < items; b += 3 * kResQuantThreads) {
+                const AItem i0 = make_item(p, b, items, nb8, m0, a0, a_rows);
+                const AItem i1 = make_item(p, b + kResQuantThreads, items, nb8, m0, a0, a_rows);
+                const AItem i2 = make_item(p, b + 2 * kResQuantThreads, items, nb8, m0, a0, a_rows);
+                uint32_t w0[16], w1[16], w2[16];
+                if (i0.valid && i0.avail > 0) load_a_block(i0.src, i0.avail, w0);
+                if (i1.valid && i1.avail > 0) load_a_block(i1.src, i1.avail, w1);
+                if (i2.valid && i2.avail > 0) load_a_block(i2.src, i2.avail, w2);
+                quantize_item(i0, w0, sA);
+                quantize_item(i1, w1, sA);
+                quantize_item(i2, w2, sA);
+            }
+            if (threadIdx.x == 0) RES_PHASE(3);
+        } else {
         const AItem it0 = make_item(p, qt, items, nb8, m0, a0, a_rows);
         const AItem it1 = make_item(p, qt + kResQuantThreads, items, nb8, m0, a0, a_rows);
         // warm L2 with this thread's A while the previous grid finishes (see prefetch_l2), on
@@ -208,6 +230,7 @@ mxfp4_gemm_resident_kernel(const ResidentArgs p) {
         quantize_item(it0, w0, sA);
         if (threadIdx.x == 0) RES_PHASE(3);
         quantize_item(it1, w1, sA);
+        }
 #ifdef MXFP4_TEST_HOOKS
         // test build: the token blocks of weight tile 0's CTAs, as quantized, to the dump buffer
         // [m_tiles][k_atoms][a_block]
@@ -486,14 +509,17 @@ static cudaError_t set_resident_attributes() {
     if (attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        cudaFuncAttributes fa = {};
-        e = cudaFuncGetAttributes(&fa, mxfp4_gemm_resident_kernel);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mxfp4_gemm_resident_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemLimit - fa.sharedSizeBytes));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mxfp4_gemm_resident_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
+        for (const void* fn : {reinterpret_cast<const void*>(mxfp4_gemm_resident_kernel<false>),
+                               reinterpret_cast<const void*>(mxfp4_gemm_resident_kernel<true>)}) {
+            cudaFuncAttributes fa = {};
+            e = cudaFuncGetAttributes(&fa, fn);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemLimit - fa.sharedSizeBytes));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
         attr_set[dev].store(true, std::memory_order_release);
     }
     return cudaSuccess;
@@ -513,7 +539,7 @@ int max_active_clusters_resident(int cluster_size, size_t smem_bytes) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_resident_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_resident_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -537,7 +563,8 @@ cudaError_t launch_gemm_resident(const GemmPlan& plan, const ResidentArgs& args,
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = plan.splits > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_resident_kernel, args);
+    if (plan.many_items) return cudaLaunchKernelEx(&cfg, mxfp4_gemm_resident_kernel<true>, args);
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_resident_kernel<false>, args);
 }
 
 }  // namespace mxfp4

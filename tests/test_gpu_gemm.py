@@ -421,7 +421,9 @@ def test_prepared_calls_every_plan(M, N, K, path, splits, m_tile):
 
 
 @pytest.mark.parametrize("M,N,K,path,splits,m_tile", [
-    (8, 2112, 7168, 0, 0, 0),        # weight-resident, six K slices
+    (8, 2112, 7168, 0, 0, 0),        # weight-resident, six K slices (four with the flag)
+    (16, 2112, 7168, 0, 0, 0),       # four slices with the flag: three blocks of A per thread
+    (32, 2112, 7168, 0, 0, 0),       # two-kernel without the flag, weight-resident with it
     (16, 3072, 1536, 0, 0, 0),       # weight-resident, three K slices
     (5, 300, 520, 1, 2, 0),          # fused, K tail
     (64, 7168, 2048, 0, 0, 0),       # two-kernel, four-lane quantizer

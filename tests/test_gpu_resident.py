@@ -44,6 +44,12 @@ CASES = [
     (6, 300, 1792, 1, 16),
     (4, 256, 2048, 1, 16),
     (9, 200, 3840, 2, 16),
+    # more than two 1x32 blocks of A per quantizing thread (the kernel variant that loads three at
+    # a time): three, four, six; a ragged token tile; a K tail
+    (16, 300, 7168, 4, 16),
+    (24, 260, 7168, 4, 32),
+    (32, 200, 7168, 4, 32),
+    (20, 129, 2040, 1, 32),
 ]
 
 

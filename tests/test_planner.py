@@ -63,7 +63,9 @@ def test_invariants_over_a_grid(mx):
                             # a third issuing warp only for 16-token tiles of three or more steps
                             assert p["issuers"] == (3 if p["m_tile"] == 16 and steps >= 3 else 2), p
                             assert p["issuers"] * p["m_tile"] + 16 * steps <= p["tmem_cols"], p
-                            assert min(M, p["m_tile"]) * steps * 8 <= 640, (M, N, K, p)
+                            # explicit plans may take the kernel variant with up to six blocks
+                            # of A per quantizing thread
+                            assert min(M, p["m_tile"]) * steps * 8 <= 320 * 6, (M, N, K, p)
                             assert p["smem_bytes"] <= 227 * 1024, p
                         if p["issuers"] == 3 and p["path"] == 2:   # the lent epilogue warp: only without refills
                             assert p["stages"] == steps and p["m_tile"] <= 128, p
@@ -145,25 +147,31 @@ def test_errors(mx):
         plan(mx, 8, 2112, 7168, m_tile=24)   # token tile must be a multiple of 16
 
 
-@pytest.mark.parametrize("M,N,K,plain_s,ready_s,ready_ctas,early", [
-    (8, 2112, 7168, 6, 4, 68, 1),    # six 112 KB slices leave no room: four slices on 68 SMs
-    (4, 2112, 7168, 6, 4, 68, 1),
-    (16, 2112, 7168, 6, 6, 102, 0),  # four slices would take four blocks of A per thread: it waits
-    (8, 4096, 5120, 4, 4, 128, 0),   # two slices would take ten steps each: it waits
-    (16, 3072, 1536, 3, 3, 72, 1),   # room to read A early: the same plan
-    (32, 4096, 512, 1, 1, 64, 1),
-    (8, 2112, 5120, 6, 6, 102, 1),
+@pytest.mark.parametrize("M,N,K,plain,ready,early", [
+    (8, 2112, 7168, (3, 6, 102), (3, 4, 68), 1),    # six 112 KB slices leave no room: four on 68 SMs
+    (4, 2112, 7168, (3, 6, 102), (3, 4, 68), 1),
+    (16, 2112, 7168, (3, 6, 102), (3, 4, 68), 1),   # three blocks of A per quantizing thread
+    (32, 2112, 7168, (2, 5, 85), (3, 4, 68), 1),    # six: no flagless resident plan fits
+    (24, 2112, 7168, (2, 5, 85), (3, 4, 68), 1),
+    (8, 4096, 5120, (3, 4, 128), (3, 4, 128), 0),   # two slices would take ten steps each: it waits
+    (16, 3072, 1536, (3, 3, 72), (3, 3, 72), 1),    # room to read A early: the same plan
+    (32, 4096, 512, (3, 1, 64), (3, 1, 64), 1),
+    (8, 2112, 5120, (3, 6, 102), (3, 6, 102), 1),
 ])
-def test_plans_with_a_declared_ready(mx, M, N, K, plain_s, ready_s, ready_ctas, early):
+def test_plans_with_a_declared_ready(mx, M, N, K, plain, ready, early):
     # MXFP4_GEMM_A_READY: A is read before the dependency wait where two CTAs of 112 KB do not
-    # share an SM; where they would, the most slices whose CTAs fill at most half the SMs, one per
-    # SM, if the slices fit; otherwise the flagless plan, waiting as before
+    # share an SM; where they would (or no flagless resident plan fits), the most slices whose
+    # CTAs fill at most half the SMs, one per SM, if the slices fit; otherwise the flagless plan,
+    # waiting as before
     p = plan(mx, M, N, K)
     r = plan(mx, M, N, K, a_ready=True)
-    assert p["path"] == 3 and p["splits"] == plain_s and p["a_early"] == 0
-    assert (r["path"], r["splits"], r["ctas"], r["a_early"]) == (3, ready_s, ready_ctas, early)
-    if r["splits"] != p["splits"]:
+    assert (p["path"], p["splits"], p["ctas"], p["a_early"]) == plain + (0,)
+    assert (r["path"], r["splits"], r["ctas"], r["a_early"]) == ready + (early,)
+    if ready != plain:
         assert 2 * r["ctas"] <= SM_COUNT and 2 * (r["smem_bytes"] + 1024) > 233472
+        # the same slices can be forced without the flag (the kernel then waits before reading A)
+        f = plan(mx, M, N, K, path=3, splits=r["splits"], m_tile=r["m_tile"])
+        assert (f["splits"], f["ctas"], f["a_early"]) == (r["splits"], r["ctas"], 0)
 
 
 def test_a_early_only_where_it_is_read(mx):
