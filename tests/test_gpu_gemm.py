@@ -443,6 +443,8 @@ def test_a_ready_gives_the_same_bits(M, N, K, path, splits, m_tile):
     kw = dict(path=path, splits=splits, m_tile=m_tile)
     rp = mx.mxfp4_gemm_plan(M, N, K, a_ready=True, **kw)
     kw_plan = dict(path=rp["path"], splits=rp["splits"], m_tile=rp["m_tile"])
+    if (M, N, K) == (8, 2112, 7168):   # the flagless six slices leave no room: side by side
+        assert rp["path"] == 3 and rp["a_early"] == 1 and 2 * rp["ctas"] <= 152, rp
     prepared = mx.prepare_gemm(a, packed, N, outs[3], a_ready=True, **kw)
     xs = [workloads.random_bf16(M, K, seed=s).cuda() for s in (21, 22, 23)]
     wants = [mx.mxfp4_gemm(x, packed, N, **kw_plan) for x in xs]
