@@ -187,9 +187,10 @@ typedef struct {
  * and quantizes A as soon as its kernels start, overlapping the work before it; it still writes
  * nothing (C, workspace) before that work has finished. With an explicit plan (path and splits
  * given) the results are the same bits either way. The automatic plan may differ with the flag
- * (mxfp4_plan_info.a_early; on the weight-resident path, fewer K slices whose CTAs fill at most
- * half the SMs, when the flagless plan leaves no room to read A early), and C then differs from
- * the flagless call's only by the order of the split-K sum, within the same tolerance. */
+ * (mxfp4_plan_info.a_early): up to 32 tokens, fewer K slices whose CTAs fill at most half the
+ * SMs, when the flagless weight-resident plan leaves no room to read A early or none fits (the
+ * flagless call then runs the two-kernel path); C then differs from the flagless call's only by
+ * the order of the split-K sum, within the same tolerance. */
 #define MXFP4_GEMM_A_READY 1
 
 /* mxfp4_gemm with an explicit plan. The workspace must be at least
