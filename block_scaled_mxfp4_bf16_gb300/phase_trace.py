@@ -52,9 +52,9 @@ def _library():
     return L
 
 
-class _Opts(ctypes.Structure):
+class _Opts(ctypes.Structure):   # mxfp4_gemm_options (flags 0: the flagless plans)
     _fields_ = [("path", ctypes.c_int), ("splits", ctypes.c_int), ("m_tile", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("flags", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 def trace(w: workloads.Workload, path: int = 0, splits: int = 0, m_tile: int = 0, calls: int = 60,
